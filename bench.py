@@ -1,0 +1,494 @@
+#!/usr/bin/env python3
+"""Benchmark of the row-major GEMM library on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-extras] [--no-cpu-baseline]
+
+One step is one C-ABI call computing C = alpha*A*B + beta*C on the named
+workload (default: bf16 8192^3, the tensor-core path). Inputs are resident in
+HBM before the timed region; A + B alone exceed the 129 MB L2, so no L2 flush
+is needed between steps. The device-timed value uses CUDA events on the
+launching stream around exactly K back-to-back steps, after W warm-up steps,
+bracketed by a barrier and a device synchronise; the max over ranks is taken.
+
+The printed JSON line also carries:
+  e2e           the same metric through the C ABI with pinned HOST buffers:
+                every step copies A and B host->device and C device->host.
+  roofline      achieved TFLOP/s of the dominant kernel against the measured
+                peak of its pipe, and ncu DRAM traffic per launch when a
+                capture of the current kernel source is recorded.
+  cpu_baseline  the CPU oracle timed on this host's cores on a bounded row
+                sample of the same workload (rank 0, N = 1 only).
+  clocks        SM clock (median) and throttle reasons sampled by nvidia-smi
+                during the timed region.
+  extras        the other workloads (fp32 4096^3, fp16 8192^3, int8 8192^3),
+                each with its own roofline fraction.
+
+--impl reference times the CPU oracle itself (the only reference that exists
+for this path) on the same workload, a bounded row sample per step.
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(weak scaling, no data exchange); value = all ranks' flops / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (TOPS int8) and % of FP32/tensor-pipe peak at M=N=K=4096/8192"
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "sm_max_mhz": 2070.0}
+
+# workload name -> description, entry point, pipe that bounds it
+WORKLOADS = {
+    "bf16_8192": ("bf16 GEMM, row-major, M=N=K=8192, N(0,1) rounded to bf16, fp32 accumulate "
+                  "and fp32 C, alpha=1, beta=0", "bf16", "tensor", 1),
+    "f16_8192": ("fp16 GEMM, row-major, M=N=K=8192, N(0,1) rounded to fp16, fp32 accumulate "
+                 "and fp32 C, alpha=1, beta=0", "f16", "tensor", 1),
+    "f32_4096": ("fp32 SGEMM (SIMT, exact fp32), row-major, M=N=K=4096, N(0,1), alpha=1, beta=0",
+                 "f32", "alu", 1),
+    "s8_8192": ("int8 GEMM, row-major, M=N=K=8192, uniform -128..127, exact int32 accumulate "
+                "and int32 C, alpha=1, beta=0", "s8", "tensor", 3),
+}
+
+# Sources whose change invalidates recorded ncu traffic for a workload.
+KERNEL_SOURCES = {
+    "bf16_8192": ["gemm_tc.cu", "ptx.cuh"],
+    "f16_8192": ["gemm_tc.cu", "ptx.cuh"],
+    "s8_8192": ["gemm_tc.cu", "ptx.cuh"],
+    "f32_4096": ["sgemm_simt.cu", "ptx.cuh"],
+}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest(name: str) -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[name]:
+        with open(os.path.join(ROOT, "dense_gemm_row_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(name: str):
+    """DRAM bytes per launch from profiles/ncu_traffic.txt, only if recorded
+    for the current kernel source (digest match)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    digest = source_digest(name)
+    for line in lines:
+        parts = line.split()
+        if len(parts) >= 3 and not line.startswith("#") and parts[0] == name and parts[1] == digest:
+            return float(parts[2])
+    return None
+
+
+# --------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi in the background; samples are kept with their wall time."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._reader, daemon=True)
+        self.thread.start()
+        time.sleep(0.5)  # let the first samples arrive
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        def parse(line):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                return None
+            try:
+                return {"sm": float(f[1]), "max": float(f[2]),
+                        "reasons": {"hw_slowdown": f[5], "hw_thermal_slowdown": f[6],
+                                    "sw_thermal_slowdown": f[7], "sw_power_cap": f[8]}}
+            except ValueError:
+                return None
+        rows = [(t, parse(l)) for t, l in self.samples]
+        rows = [(t, r) for t, r in rows if r]
+        inside = [r for t, r in rows if t0 - 0.15 <= t <= t1 + 0.15]
+        window = "timed"
+        if not inside:
+            inside = [r for _, r in rows]
+            window = "warmup+timed"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "window": "none"}
+        reasons = sorted({k for r in inside for k, v in r["reasons"].items() if v == "Active"})
+        return {"sm_mhz": statistics.median(r["sm"] for r in inside),
+                "sm_max_mhz": max(r["max"] for r in inside), "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+# ----------------------------------------------------------------- GPU timing
+
+def flops_of(M, N, K):
+    return 2.0 * M * N * K
+
+
+def entry(binding, kind):
+    return {"bf16": binding.gemm_bf16, "f16": binding.gemm_f16, "f32": binding.gemm_f32,
+            "s8": binding.gemm_s8}[kind]
+
+
+def time_device(binding, torch, kind, p_dev, steps, warmup, stream, dist=None):
+    A, B, C, alpha, beta = p_dev
+    M, K = A.shape
+    N = B.shape[1]
+    fn = entry(binding, kind)
+    args = (M, N, K, alpha, A, A.stride(0), B, B.stride(0), beta, C, C.stride(0), stream)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            fn(*args)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    ev0.record(stream)
+    for _ in range(steps):
+        fn(*args)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    return ms, t0, t1
+
+
+def time_e2e(binding, torch, kind, p_host, p_dev, steps, stream):
+    """Host -> device copy of A and B, the C-ABI call, device -> host copy of C."""
+    (Ah, Bh, Ch), (A, B, C, alpha, beta) = p_host, p_dev
+    M, K = A.shape
+    N = B.shape[1]
+    fn = entry(binding, kind)
+    args = (M, N, K, alpha, A, A.stride(0), B, B.stride(0), beta, C, C.stride(0), stream)
+
+    def step():
+        with torch.cuda.stream(stream):
+            A.copy_(Ah, non_blocking=True)
+            B.copy_(Bh, non_blocking=True)
+            fn(*args)
+            Ch.copy_(C, non_blocking=True)
+    step()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    h2d = Ah.numel() * Ah.element_size() + Bh.numel() * Bh.element_size()
+    d2h = Ch.numel() * Ch.element_size()
+    return ev0.elapsed_time(ev1), h2d, d2h
+
+
+def device_problem(torch, p):
+    A = p.A.cuda()
+    B = p.B.cuda()
+    C = p.C0.cuda()
+    return A, B, C, p.alpha, p.beta
+
+
+def peak_for(kind, peaks, sm_count, sustained=False):
+    if kind == "f32":
+        # FP32 SIMT: SMs x 128 FMA lanes x 2 flops x maximum SM clock.
+        mhz = float(peaks.get("sm_max_mhz", 2070.0))
+        return sm_count * 128 * 2 * mhz * 1e6 / 1e12
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    # fp16 and the int8 path (run as integer-valued fp16 on kind::f16) share the
+    # bf16 dense rate of the tensor pipe.
+    return float(peaks.get(key, FALLBACK_PEAKS[key]))
+
+
+# ------------------------------------------------------------- CPU baseline
+
+def cpu_oracle_sample(p, seconds: float):
+    """Times the oracle on a row sample of p sized for about `seconds`."""
+    import torch  # noqa: F401
+    from oracle import oracle as o
+    M, K = p.A.shape
+    N = p.B.shape[1]
+
+    def run(rows):
+        idx = list(range(rows))
+        t = time.perf_counter()
+        o.gemm_rows(p.A, p.B, idx, p.alpha, p.beta, p.C0)
+        return time.perf_counter() - t
+
+    probe = min(M, 8)
+    t_probe = run(probe)
+    rows = probe
+    if t_probe < seconds:
+        rows = int(min(M, max(probe, probe * seconds / max(t_probe, 1e-6))))
+    t = run(rows) if rows != probe else t_probe
+    return {"rows": rows, "seconds": t, "flops": flops_of(rows, N, K), "cores": o.num_threads(),
+            "sample": f"rows 0..{rows - 1} of A ({rows} of {M}) against all of B; "
+                      f"{flops_of(rows, N, K) / 1e9:.1f} GFLOP per sample"}
+
+
+# ------------------------------------------------------------------ reference
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    from dense_gemm_row_gb300 import workloads as w
+    name = args.workload
+    desc, kind, bound, _ = WORKLOADS[name]
+    p = w.config(name)
+    M, K = p.A.shape
+    N = p.B.shape[1]
+    # Size one step so the whole run ends within about two minutes.
+    total_steps = max(1, args.steps + args.warmup)
+    per_step = min(20.0, max(0.5, 120.0 / total_steps))
+    cal = cpu_oracle_sample(p, per_step)
+    rows = cal["rows"]
+    from oracle import oracle as o
+    idx = list(range(rows))
+    for _ in range(args.warmup):
+        o.gemm_rows(p.A, p.B, idx, p.alpha, p.beta, p.C0)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        o.gemm_rows(p.A, p.B, idx, p.alpha, p.beta, p.C0)
+    elapsed = time.perf_counter() - t
+    value = flops_of(rows, N, K) * args.steps / elapsed / 1e12
+    unit = "TOPS" if kind == "s8" else "TFLOP/s"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int64" if kind == "s8" else "f64", "data": "synthetic",
+        "config": {"workload": desc, "M": M, "N": N, "K": K, "parallelism": "cpu-host"},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": cal["cores"], "kind": "oracle",
+                         "sample": cal["sample"] + " per step"},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="bf16_8192", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    import torch
+    from dense_gemm_row_gb300 import binding
+    from dense_gemm_row_gb300 import workloads as w
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        dist = tdist
+
+    peaks, peak_src = load_peaks()
+    props = torch.cuda.get_device_properties(local_rank)
+    sm_count = props.multiProcessorCount
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(props.uuid)
+    except Exception:
+        pass
+
+    name = args.workload
+    desc, kind, bound, launches_per_step = WORKLOADS[name]
+    p = w.config(name)
+    M, K = p.A.shape
+    N = p.B.shape[1]
+    p_dev = device_problem(torch, p)
+    stream = torch.cuda.Stream()
+
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    ms, t0, t1 = time_device(binding, torch, kind, p_dev, args.steps, args.warmup, stream, dist)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+    binding.check_device_error()
+
+    ms_max = ms
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    step_ms = ms_max / args.steps
+    flops = flops_of(M, N, K)
+    value = world * flops * args.steps / (ms_max / 1e3) / 1e12
+
+    if rank != 0:
+        if dist is not None:
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+
+    unit = "TOPS" if kind == "s8" else "TFLOP/s"
+    peak = peak_for(kind, peaks, sm_count)
+    kernel_ms = ms / args.steps
+    achieved = flops / (kernel_ms / 1e3) / 1e12
+    traffic = recorded_traffic(name)
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                "peak_source": (f"{peak_src}: " + ("SMs x 128 FP32 lanes x 2 x max SM clock "
+                                                   f"({sm_count} SMs, {peaks.get('sm_max_mhz')} MHz)"
+                                                   if kind == "f32" else "bf16_tflops (burst)")),
+                "kernel": "gemm_tc_kernel" if kind != "f32" else "sgemm_simt_kernel",
+                "kernel_ms": kernel_ms}
+    if kind == "s8":
+        roofline["note"] = "step time includes the two int8->fp16 widening launches"
+
+    # End to end through the C ABI with pinned host buffers.
+    Ah = p.A.pin_memory()
+    Bh = p.B.pin_memory()
+    Ch = torch.empty(p.C0.shape, dtype=p.C0.dtype).pin_memory()
+    e2e_ms, h2d, d2h = time_e2e(binding, torch, kind, (Ah, Bh, Ch), p_dev, args.e2e_steps,
+                                stream)
+    e2e = {"value": flops * args.e2e_steps / (e2e_ms / 1e3) / 1e12, "unit": unit,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "ms_per_step": e2e_ms / args.e2e_steps}
+
+    extras = {}
+    if not args.no_extras:
+        for other in ("f32_4096", "f16_8192", "s8_8192", "bf16_8192"):
+            if other == name:
+                continue
+            odesc, okind, obound, _ = WORKLOADS[other]
+            q = w.config(other)
+            q_dev = device_problem(torch, q)
+            Mo, Ko = q.A.shape
+            No = q.B.shape[1]
+            steps = 100 if okind != "f32" else 50
+            oms, _, _ = time_device(binding, torch, okind, q_dev, steps, 5, stream)
+            f = flops_of(Mo, No, Ko)
+            ach = f / (oms / steps / 1e3) / 1e12
+            opk = peak_for(okind, peaks, sm_count)
+            extras[other] = {"workload": odesc, "value": ach,
+                             "unit": "TOPS" if okind == "s8" else "TFLOP/s",
+                             "ms_per_step": oms / steps, "bound": obound, "peak": opk,
+                             "frac": ach / opk, "traffic": recorded_traffic(other)}
+            if okind == "f32":
+                mhz = clocks.get("sm_mhz")
+                if mhz:
+                    extras[other]["frac_at_sampled_clock"] = ach / (
+                        sm_count * 128 * 2 * mhz * 1e6 / 1e12)
+            del q_dev
+            torch.cuda.empty_cache()
+        binding.check_device_error()
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cal = cpu_oracle_sample(p, args.cpu_seconds)
+        cpu = {"value": cal["flops"] / cal["seconds"] / 1e12, "unit": unit,
+               "cores": cal["cores"], "kind": "oracle", "sample": cal["sample"],
+               "seconds": cal["seconds"]}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": {"bf16": "bf16", "f16": "f16", "f32": "f32", "s8": "s8"}[kind],
+        "data": "synthetic (seeded; no dataset)",
+        "config": {"workload": desc, "M": M, "N": N, "K": K,
+                   "l2": "no flush: A+B exceed the 129 MB L2" if kind != "f32"
+                   else "no flush: A+B+C = 192 MiB exceed the 129 MB L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
+                   "reasons": clocks["reasons"], "samples": clocks["samples"],
+                   "window": clocks["window"]},
+        "extras": extras,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,151 @@
+"""ctypes binding of libdense_gemm_row.so (include/dense_gemm_row.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library. Importing this module loads the library and raises ImportError when
+it has not been built; there is no fallback.
+
+Two layers:
+
+* ``gemm_f32 / gemm_bf16 / gemm_f16 / gemm_s8(M, N, K, alpha, A, lda, B, ldb,
+  beta, C, ldc, stream=None)`` mirror the C entry points. A, B and C are raw
+  device addresses (int) or tensors (their ``data_ptr()`` is passed). ``stream``
+  is a raw ``cudaStream_t`` (int), a ``torch.cuda.Stream``, or None for torch's
+  current stream. A non-zero status raises :class:`GemmError`.
+* ``gemm(A, B, C, alpha, beta)`` takes 2-D CUDA tensors with unit column stride
+  (row stride = leading dimension), picks the entry point from A's dtype and
+  runs on torch's current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdense_gemm_row.so")
+
+STATUS = {
+    0: "GEMM_OK",
+    1: "GEMM_ERR_INVALID_VALUE",
+    2: "GEMM_ERR_UNSUPPORTED_LAYOUT",
+    3: "GEMM_ERR_LAUNCH",
+    4: "GEMM_ERR_DEVICE",
+    5: "GEMM_ERR_TIMEOUT",
+}
+
+# Every function include/dense_gemm_row.h declares.
+EXPORTED = ("gemm_f32", "gemm_bf16", "gemm_f16", "gemm_s8", "gemm_status_string",
+            "gemm_check_device_error", "gemm_version")
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {STATUS.get(self.status, self.status)}")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with `python -m dense_gemm_row_gb300.build` "
+            "(or __graft_entry__.build()). There is no CPU fallback.")
+    lib = ctypes.CDLL(LIB_PATH)
+    i64, vp = ctypes.c_int64, ctypes.c_void_p
+    f32, i32 = ctypes.c_float, ctypes.c_int32
+    for name in ("gemm_f32", "gemm_bf16", "gemm_f16"):
+        fn = getattr(lib, name)
+        fn.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
+        fn.restype = ctypes.c_int
+    lib.gemm_s8.argtypes = [i64, i64, i64, i32, vp, i64, vp, i64, i32, vp, i64, vp]
+    lib.gemm_s8.restype = ctypes.c_int
+    lib.gemm_status_string.argtypes = [ctypes.c_int]
+    lib.gemm_status_string.restype = ctypes.c_char_p
+    lib.gemm_check_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    lib.gemm_check_device_error.restype = ctypes.c_int
+    lib.gemm_version.argtypes = []
+    lib.gemm_version.restype = ctypes.c_int
+    return lib
+
+
+lib = _load()
+
+
+def _addr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(s, int):
+        return s
+    return int(s.cuda_stream)
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise GemmError(status, where)
+
+
+def gemm_f32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
+    _check(lib.gemm_f32(M, N, K, alpha, _addr(A), lda, _addr(B), ldb, beta, _addr(C), ldc,
+                        _stream(stream)), "gemm_f32")
+
+
+def gemm_bf16(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
+    _check(lib.gemm_bf16(M, N, K, alpha, _addr(A), lda, _addr(B), ldb, beta, _addr(C), ldc,
+                         _stream(stream)), "gemm_bf16")
+
+
+def gemm_f16(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
+    _check(lib.gemm_f16(M, N, K, alpha, _addr(A), lda, _addr(B), ldb, beta, _addr(C), ldc,
+                        _stream(stream)), "gemm_f16")
+
+
+def gemm_s8(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
+    _check(lib.gemm_s8(M, N, K, int(alpha), _addr(A), lda, _addr(B), ldb, int(beta), _addr(C),
+                       ldc, _stream(stream)), "gemm_s8")
+
+
+def check_device_error() -> int:
+    """Reads and clears the device error word; raises GemmError(GEMM_ERR_TIMEOUT)
+    if a kernel gave up a bounded wait. Returns the raw word otherwise (0)."""
+    w = ctypes.c_uint32(0)
+    st = lib.gemm_check_device_error(ctypes.byref(w))
+    if st != 0:
+        raise GemmError(st, f"device error word 0x{w.value:08x}")
+    return int(w.value)
+
+
+def _ld(t, name) -> int:
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D")
+    if t.shape[0] > 0 and t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} needs unit column stride (row-major)")
+    return max(int(t.stride(0)), int(t.shape[1]), 1)
+
+
+def gemm(A, B, C, alpha=1.0, beta=0.0, stream=None):
+    """C = alpha*A*B + beta*C for 2-D CUDA tensors; dtype selects the entry point:
+    float32 -> gemm_f32, bfloat16 -> gemm_bf16, float16 -> gemm_f16 (C float32),
+    int8 -> gemm_s8 (C int32)."""
+    import torch
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K or tuple(C.shape) != (M, N):
+        raise ValueError("gemm: shapes do not chain (A: MxK, B: KxN, C: MxN)")
+    if A.dtype != B.dtype:
+        raise TypeError("gemm: A and B must share a dtype")
+    fns = {torch.float32: (gemm_f32, torch.float32), torch.bfloat16: (gemm_bf16, torch.float32),
+           torch.float16: (gemm_f16, torch.float32), torch.int8: (gemm_s8, torch.int32)}
+    if A.dtype not in fns:
+        raise TypeError(f"gemm: unsupported dtype {A.dtype}")
+    fn, c_dtype = fns[A.dtype]
+    if C.dtype != c_dtype:
+        raise TypeError(f"gemm: C must be {c_dtype} for {A.dtype} inputs")
+    fn(M, N, K, alpha, A, _ld(A, "A"), B, _ld(B, "B"), beta, C, _ld(C, "C"), stream)
+    return C

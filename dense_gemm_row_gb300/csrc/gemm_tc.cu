@@ -1,0 +1,524 @@
+// gemm_tc.cu -- tensor-core GEMM for sm_103a: tcgen05.mma with the
+// accumulator in tensor memory (TMEM), operands staged by TMA.
+//
+//     C = alpha * A * B + beta * C       A: M x K, B: K x N, C: M x N, row-major
+//
+// 16-bit inputs (bf16 or fp16), fp32 accumulation, and either
+//   * fp32 output (gemm_bf16 / gemm_f16), or
+//   * exact int32 output from integer-valued fp16 operands (the int8 path: an
+//     int8 value is exact in fp16, a product of two is at most 2^14 in
+//     magnitude, and a sum of at most 1024 such products is an integer of at
+//     most 2^24 in magnitude, which fp32 represents exactly. The kernel
+//     therefore restarts the fp32 accumulator every 1024 values of k, and the
+//     epilogue adds each finished partial sum into int32 registers).
+//
+// Sources: C++ warp-matrix-function page (D = A*B + C on tensor cores; type
+// table: half / bfloat16 inputs with float accumulate, signed char inputs with
+// int accumulate); "Sgemm [128,128,8]" (C = alpha*A*B + beta*C, row-major, the
+// alpha/beta epilogue); "使用CUDA和瓦片算法计算矩阵乘法" (residual tiles act as
+// zeros: here the TMA unit fills out-of-range elements with zeros).
+//
+// Structure (one CTA per SM, persistent):
+//   warp 0      one thread issues TMA loads of A (128 x 64, K-major, 128-byte
+//               swizzle) and B (64 x 256 as four 64 x 64 boxes, N-major,
+//               128-byte swizzle) into a kStages-deep ring guarded by
+//               full/empty mbarriers.
+//   warp 1      allocates 512 TMEM columns; one thread issues
+//               tcgen05.mma.cta_group::1.kind::f16 (M=128, N=256, K=16) into
+//               one of two 256-column accumulators and commits each stage's
+//               completion to that stage's empty barrier.
+//   warps 2..9  epilogue: tcgen05.ld of the finished accumulator (each warp
+//               reads its 32-lane quarter and one 128-column half), then
+//               alpha/beta and guarded stores to C. The two accumulators let
+//               the epilogue of one tile overlap the main loop of the next.
+// Tiles are visited in groups of kGroupM tile rows so that the CTAs resident
+// at one time share A rows and B columns in L2.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <type_traits>
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace dgr {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;         // 64 16-bit values = one 128-byte swizzle row
+constexpr int kStages = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kGroupM = 16;
+constexpr int kChunkKB = 16;    // int mode: k-blocks per exact fp32 chunk (16 * 64 = 1024)
+constexpr uint32_t kTmemCols = 512;  // two 256-column fp32 accumulators
+
+constexpr uint32_t kABytes = kBM * kBK * 2;        // 16 KiB
+constexpr uint32_t kBBoxBytes = 64 * kBK * 2;      // one 64(N) x 64(K) box: 8 KiB
+constexpr uint32_t kBBytes = kBK * kBN * 2;        // 32 KiB
+constexpr uint32_t kStageBytes = kABytes + kBBytes;
+
+struct __align__(1024) TcSmem {
+  uint8_t a[kStages][kABytes];
+  uint8_t b[kStages][kBBytes];
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <bool kInt>
+struct TcArgs {
+  using Out = typename std::conditional<kInt, int32_t, float>::type;
+  int M, N, K;
+  Out alpha, beta;
+  Out *C;
+  int64_t ldc;
+  int tiles_m, tiles_n;
+  int c_vec_ok;  // C 16-byte aligned and ldc % 4 == 0
+  uint32_t idesc;
+  uint32_t *err_word;
+};
+
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &tm, int &tn) {
+  const int per_group = kGroupM * tiles_n;
+  const int g = t / per_group;
+  const int first = g * kGroupM;
+  const int rows = min(tiles_m - first, kGroupM);
+  const int r = t - g * per_group;
+  tm = first + r % rows;
+  tn = r / rows;
+}
+
+// Waits without looking at the abort flag (used to drain in-flight work).
+__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint32_t *err_word) {
+  volatile int never = 0;
+  return mbar_wait_bounded(bar, parity, &never, err_word, kWaitDrain);
+}
+
+// alpha*acc + beta*c (the c term only when use_c). fp32: two roundings, or one
+// when the compiler fuses them. int32: wrap-around, computed in unsigned
+// arithmetic so that overflow is defined.
+__device__ __forceinline__ float scale_add(float alpha, float acc, float beta, float c,
+                                           bool use_c) {
+  return use_c ? alpha * acc + beta * c : alpha * acc;
+}
+__device__ __forceinline__ int32_t scale_add(int32_t alpha, int32_t acc, int32_t beta, int32_t c,
+                                             bool use_c) {
+  uint32_t r = static_cast<uint32_t>(alpha) * static_cast<uint32_t>(acc);
+  if (use_c) r += static_cast<uint32_t>(beta) * static_cast<uint32_t>(c);
+  return static_cast<int32_t>(r);
+}
+
+template <bool kInt>
+__device__ __forceinline__ void store_row_chunk(const TcArgs<kInt> &p, int row, int col,
+                                                const typename TcArgs<kInt>::Out (&v)[32]) {
+  using Out = typename TcArgs<kInt>::Out;
+  Out *crow = p.C + static_cast<int64_t>(row) * p.ldc;
+  const Out alpha = p.alpha, beta = p.beta;
+  const bool use_c = beta != Out(0);
+  if (p.c_vec_ok && col + 31 < p.N) {
+    using Vec = typename std::conditional<kInt, int4, float4>::type;
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+      Vec c = {};
+      if (use_c) c = *reinterpret_cast<const Vec *>(crow + col + j);
+      Vec o;
+      o.x = scale_add(alpha, v[j], beta, c.x, use_c);
+      o.y = scale_add(alpha, v[j + 1], beta, c.y, use_c);
+      o.z = scale_add(alpha, v[j + 2], beta, c.z, use_c);
+      o.w = scale_add(alpha, v[j + 3], beta, c.w, use_c);
+      *reinterpret_cast<Vec *>(crow + col + j) = o;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (col + j < p.N) {
+        const Out c = use_c ? crow[col + j] : Out(0);
+        crow[col + j] = scale_add(alpha, v[j], beta, c, use_c);
+      }
+    }
+  }
+}
+
+template <bool kInt>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const TcArgs<kInt> p) {
+  using Out = typename TcArgs<kInt>::Out;
+  extern __shared__ uint8_t smem_raw[];
+  // Swizzled TMA destinations need 1024-byte alignment.
+  TcSmem &sm = *reinterpret_cast<TcSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  volatile int *abort = &sm.abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&sm.full[s]), 1);
+      mbar_init(smem_u32(&sm.empty[s]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&sm.tmem_full[i]), 1);
+      mbar_init(smem_u32(&sm.tmem_empty[i]), kEpiWarps);
+    }
+    mbar_init(smem_u32(&sm.drain), 1);
+    sm.abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = sm.tmem_base;
+
+  const int num_tiles = p.tiles_m * p.tiles_n;
+  const int KB = (p.K + kBK - 1) / kBK;
+  const int chunk_kb = kInt ? kChunkKB : KB;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t issued = 0;             // stages with a load issued
+      uint32_t issued_parity = 0;      // parity of the last load issued per stage
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        int tm, tn;
+        tile_coords(t, p.tiles_m, p.tiles_n, tm, tn);
+        const int m0 = tm * kBM, n0 = tn * kBN;
+        for (int kb = 0; kb < KB; ++kb) {
+          const uint32_t empty_bar = smem_u32(&sm.empty[stage]);
+          if (!mbar_wait_bounded(empty_bar, phase ^ 1u, abort, p.err_word, kWaitEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full_bar = smem_u32(&sm.full[stage]);
+          mbar_arrive_expect_tx(full_bar, kStageBytes);
+          tma_load_2d(smem_u32(sm.a[stage]), &tmA, full_bar, kb * kBK, m0);
+#pragma unroll
+          for (int j = 0; j < kBN / 64; ++j)
+            tma_load_2d(smem_u32(sm.b[stage] + j * kBBoxBytes), &tmB, full_bar, n0 + 64 * j,
+                        kb * kBK);
+          issued |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Never leave with a copy still writing into shared memory.
+      for (int s = 0; s < kStages; ++s)
+        if (issued & (1u << s)) drain_wait(smem_u32(&sm.full[s]), (issued_parity >> s) & 1u, p.err_word);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, chunk = 0;
+      bool ok = true;
+      bool any = false;
+      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        for (int kb0 = 0; ok && kb0 < KB; kb0 += chunk_kb) {
+          const int kb1 = min(KB, kb0 + chunk_kb);
+          const uint32_t buf = chunk & 1u, use = (chunk >> 1) & 1u;
+          ++chunk;
+          if (!mbar_wait_bounded(smem_u32(&sm.tmem_empty[buf]), use ^ 1u, abort, p.err_word,
+                                 kWaitTmemEmpty)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t d_tmem = tmem_base + buf * kBN;
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait_bounded(smem_u32(&sm.full[stage]), phase, abort, p.err_word,
+                                   kWaitFull)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t a_addr = smem_u32(sm.a[stage]);
+            const uint32_t b_addr = smem_u32(sm.b[stage]);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              // A: K-major rows of 128 B; 16 values of k = 32 B further along the row.
+              const uint64_t adesc = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+              // B: N-major; 16 rows of k = 16 * 128 B further. LBO = 8 KiB between the
+              // 64-column boxes, SBO = 1 KiB between groups of 8 k-rows.
+              const uint64_t bdesc = smem_desc_sw128(b_addr + kk * 2048, kBBoxBytes, 1024);
+              tc_mma_f16(d_tmem, adesc, bdesc, p.idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+            }
+            any = true;
+            tc_commit(smem_u32(&sm.empty[stage]));
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          tc_commit(smem_u32(&sm.tmem_full[buf]));
+        }
+      }
+      // Never leave with an MMA still reading shared memory or writing TMEM.
+      if (any) {
+        tc_commit(smem_u32(&sm.drain));
+        drain_wait(smem_u32(&sm.drain), 0, p.err_word);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int e = warp - 2;
+    const int quarter = warp & 3;          // TMEM lanes this warp may access
+    const int col_half = e >> 2;           // which 128 columns of the tile
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    uint32_t chunk = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+      int tm, tn;
+      tile_coords(t, p.tiles_m, p.tiles_n, tm, tn);
+      const int row = tm * kBM + quarter * 32 + lane;
+      const int col0 = tn * kBN + col_half * 128;
+      uint32_t acc[kInt ? 128 : 1];  // int mode: running int32 sums (wrap-around)
+      if constexpr (kInt) {
+#pragma unroll
+        for (int j = 0; j < 128; ++j) acc[j] = 0;
+      }
+      for (int kb0 = 0; kb0 < KB; kb0 += chunk_kb) {
+        const uint32_t buf = chunk & 1u, use = (chunk >> 1) & 1u;
+        ++chunk;
+        int got = 1;
+        if (lane == 0)
+          got = mbar_wait_bounded(smem_u32(&sm.tmem_full[buf]), use, abort, p.err_word,
+                                  kWaitTmemFull);
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t taddr = tmem_base + lane_base + buf * kBN + col_half * 128;
+#pragma unroll
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr + c, r);
+          tmem_ld_wait();
+          if constexpr (kInt) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              acc[c + j] += static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[j])));
+          } else {
+            if (row < p.M) {
+              float v[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+              store_row_chunk<kInt>(p, row, col0 + c, v);
+            }
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm.tmem_empty[buf]));
+      }
+      if constexpr (kInt) {
+        if (ok && row < p.M) {
+#pragma unroll
+          for (int c = 0; c < 128; c += 32) {
+            int32_t v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = static_cast<int32_t>(acc[c + j]);
+            store_row_chunk<kInt>(p, row, col0 + c, v);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Row-major rows x cols matrix of 16-bit elements, row stride ld (elements),
+// boxes of box_rows x 64 elements with 128-byte swizzle.
+bool make_tmap(CUtensorMap *tm, CUtensorMapDataType dt, const void *base, int64_t rows,
+               int64_t cols, int64_t ld, uint32_t box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(tm, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <bool kInt>
+cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf16, int M, int N,
+                      int K, typename TcArgs<kInt>::Out alpha, const void *A, int64_t lda,
+                      const void *B, int64_t ldb, typename TcArgs<kInt>::Out beta,
+                      typename TcArgs<kInt>::Out *C, int64_t ldc, cudaStream_t stream) {
+  CUtensorMap tmA, tmB;
+  if (!make_tmap(&tmA, dt, A, M, K, lda, kBM)) return cudaErrorInvalidValue;
+  if (!make_tmap(&tmB, dt, B, K, N, ldb, kBK)) return cudaErrorInvalidValue;
+  TcArgs<kInt> p;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.alpha = alpha;
+  p.beta = beta;
+  p.C = C;
+  p.ldc = ldc;
+  p.tiles_m = (M + kBM - 1) / kBM;
+  p.tiles_n = (N + kBN - 1) / kBN;
+  p.c_vec_ok = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0);
+  p.idesc = idesc_f16(is_bf16, false, true, kBM, kBN);
+  p.err_word = dev.err_word;
+  const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const size_t smem = sizeof(TcSmem) + 1024;
+  auto kern = gemm_tc_kernel<kInt>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int grid = static_cast<int>(tiles < dev.sm_count ? tiles : dev.sm_count);
+  kern<<<grid, kThreads, smem, stream>>>(tmA, tmB, p);
+  return cudaGetLastError();
+}
+
+// int8 -> fp16, exact (|x| <= 128). dst has row stride ldd (multiple of 8) and
+// its padding columns [cols, ldd) are written with zeros.
+__global__ void widen_s8_kernel(const int8_t *__restrict__ src, int64_t lds, __half *dst,
+                                int64_t ldd, int rows, int cols) {
+  const int64_t chunks_per_row = ldd / 8;
+  const int64_t total = static_cast<int64_t>(rows) * chunks_per_row;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / chunks_per_row;
+    const int c0 = static_cast<int>((i - r * chunks_per_row) * 8);
+    const int8_t *s = src + r * lds;
+    __align__(16) __half h[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c = c0 + j;
+      h[j] = __int2half_rn(c < cols ? static_cast<int>(s[c]) : 0);
+    }
+    *reinterpret_cast<uint4 *>(dst + r * ldd + c0) = *reinterpret_cast<const uint4 *>(h);
+  }
+}
+
+cudaError_t widen_s8(const DeviceInfo &dev, const int8_t *src, int64_t lds, __half *dst,
+                     int64_t ldd, int rows, int cols, cudaStream_t stream) {
+  const int64_t total = static_cast<int64_t>(rows) * (ldd / 8);
+  const int threads = 256;
+  int64_t blocks = (total + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(dev.sm_count) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  widen_s8_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(src, lds, dst, ldd,
+                                                                        rows, cols);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc_f16(const DeviceInfo &dev, bool is_bf16, int M, int N, int K,
+                               float alpha, const void *A, int64_t lda, const void *B,
+                               int64_t ldb, float beta, float *C, int64_t ldc,
+                               cudaStream_t stream) {
+  const CUtensorMapDataType dt =
+      is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return launch_tc<false>(dev, dt, is_bf16, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                          stream);
+}
+
+// The int8 path widens A and B to fp16 in stream-ordered scratch memory from a
+// library-owned pool, runs the tensor-core kernel in exact-integer mode and
+// returns the scratch to the pool on the same stream.
+cudaError_t launch_gemm_s8(const DeviceInfo &dev, int M, int N, int K, int32_t alpha,
+                           const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
+                           int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream) {
+  const int64_t lda16 = (static_cast<int64_t>(K) + 7) / 8 * 8;
+  const int64_t ldb16 = (static_cast<int64_t>(N) + 7) / 8 * 8;
+  const size_t a_bytes = static_cast<size_t>(M) * lda16 * 2;
+  const size_t a_off = (a_bytes + 255) / 256 * 256;
+  const size_t total = a_off + static_cast<size_t>(K) * ldb16 * 2;
+
+  static std::mutex mu;
+  static cudaMemPool_t pools[64] = {};
+  cudaMemPool_t pool = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+    if (!pools[dev.device]) {
+      cudaMemPoolProps props;
+      std::memset(&props, 0, sizeof props);
+      props.allocType = cudaMemAllocationTypePinned;
+      props.handleTypes = cudaMemHandleTypeNone;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev.device;
+      cudaMemPool_t pl;
+      cudaError_t e = cudaMemPoolCreate(&pl, &props);
+      if (e != cudaSuccess) return e;
+      uint64_t keep = ~0ull;  // keep freed scratch mapped for the next call
+      cudaMemPoolSetAttribute(pl, cudaMemPoolAttrReleaseThreshold, &keep);
+      pools[dev.device] = pl;
+    }
+    pool = pools[dev.device];
+  }
+  void *scratch = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&scratch, total, pool, stream);
+  if (e != cudaSuccess) return e;
+  __half *a16 = static_cast<__half *>(scratch);
+  __half *b16 = reinterpret_cast<__half *>(static_cast<uint8_t *>(scratch) + a_off);
+  e = widen_s8(dev, A, lda, a16, lda16, M, K, stream);
+  if (e == cudaSuccess) e = widen_s8(dev, B, ldb, b16, ldb16, K, N, stream);
+  if (e == cudaSuccess)
+    e = launch_tc<true>(dev, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, false, M, N, K, alpha, a16, lda16,
+                        b16, ldb16, beta, C, ldc, stream);
+  cudaError_t f = cudaFreeAsync(scratch, stream);
+  return e != cudaSuccess ? e : f;
+}
+
+}  // namespace dgr

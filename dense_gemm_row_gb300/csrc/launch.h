@@ -1,0 +1,47 @@
+// launch.h -- internal interface between the C-ABI layer (abi.cu) and the
+// kernel translation units. Not installed; not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime_api.h>
+
+namespace dgr {
+
+// Layout of the per-device error word (read and cleared by
+// gemm_check_device_error): bit 0 = a bounded wait gave up; bits 8..15 = the
+// code of the first wait that gave up.
+constexpr uint32_t kErrTimeoutBit = 1u;
+constexpr uint32_t kWaitFull = 1, kWaitEmpty = 2, kWaitTmemFull = 3, kWaitTmemEmpty = 4,
+                   kWaitDrain = 5, kWaitTest = 7;
+
+// Per-device facts gathered once by the ABI layer.
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+  uint32_t *err_word = nullptr;  // device address of this device's error word
+};
+
+// All sizes are already validated: M, N >= 1, K >= 1, each < 2^31, ld >= row length.
+cudaError_t launch_sgemm_simt(const DeviceInfo &dev, int M, int N, int K, float alpha,
+                              const float *A, int64_t lda, const float *B, int64_t ldb,
+                              float beta, float *C, int64_t ldc, cudaStream_t stream);
+
+// 16-bit inputs (is_bf16 selects bf16 or fp16), fp32 output. Layout already
+// checked: A, B 16-byte aligned, lda and ldb multiples of 8.
+cudaError_t launch_gemm_tc_f16(const DeviceInfo &dev, bool is_bf16, int M, int N, int K,
+                               float alpha, const void *A, int64_t lda, const void *B,
+                               int64_t ldb, float beta, float *C, int64_t ldc,
+                               cudaStream_t stream);
+
+cudaError_t launch_gemm_s8(const DeviceInfo &dev, int M, int N, int K, int32_t alpha,
+                           const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
+                           int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream);
+
+// K == 0: C = beta * C (C = 0 when beta == 0), M x N window only.
+cudaError_t launch_scale_f32(int M, int N, float beta, float *C, int64_t ldc,
+                             cudaStream_t stream);
+cudaError_t launch_scale_s32(int M, int N, int32_t beta, int32_t *C, int64_t ldc,
+                             cudaStream_t stream);
+
+}  // namespace dgr

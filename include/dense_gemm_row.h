@@ -1,0 +1,144 @@
+/*
+ * dense_gemm_row.h -- C ABI of the GB300 (sm_103a) row-major dense GEMM library
+ * (libdense_gemm_row.so).
+ *
+ * Every entry point computes
+ *
+ *     C = alpha * A * B + beta * C
+ *
+ * with A an M x K matrix, B a K x N matrix and C an M x N matrix, all stored
+ * row-major with a leading dimension (row stride, in elements):
+ *
+ *     A(i,k) = A[i*lda + k],  B(k,j) = B[k*ldb + j],  C(i,j) = C[i*ldc + j]
+ *
+ * Sources for the operation: "Sgemm [128,128,8]" (jianshu page) defines
+ * gemm as C = alpha*A*B + beta*C with all matrices row-major and indexes them
+ * through the A(i,j) / B(i,j) / C(i,j) macros with lda, ldb, ldc; its host
+ * reference routine host_gemm is the same loop nest. "使用CUDA和瓦片算法计算
+ * 矩阵乘法" (the tiled-multiply page) requires shapes that are not multiples of
+ * the tile to give correct results (residual tile cells act as zeros). The C++
+ * warp-matrix-function page's type table fixes the precisions: half and
+ * bfloat16 inputs accumulate in float, signed char inputs accumulate in int.
+ *
+ * Common contract of gemm_f32 / gemm_bf16 / gemm_f16 / gemm_s8:
+ *
+ *   Sizes   M, N, K >= 0 and each < 2^31. When M > 0 and K > 0, lda >= K; when
+ *           K > 0 and N > 0, ldb >= N; when M > 0 and N > 0, ldc >= N.
+ *   Memory  A, B and C are device pointers (or pointers the device can access)
+ *           owned by the caller; the library neither allocates nor frees them.
+ *           A pointer may be NULL only when its matrix is empty. Only the
+ *           M x K, K x N and M x N windows are read or written; row padding
+ *           beyond the row length is never touched. C must not overlap A or B.
+ *   beta    When beta == 0, C is write-only: its old contents (even NaN/Inf)
+ *           are never read. When alpha == 0 the product is still formed and
+ *           scaled by zero.
+ *   K == 0  C = beta * C (C = 0 when beta == 0).
+ *   M or N == 0  Nothing is launched; GEMM_OK is returned.
+ *   Stream  The call only enqueues work on `stream` (0 = the legacy default
+ *           stream) and returns; results are ready when the stream is.
+ *   Device  The current CUDA device must be an sm_103 (GB300) GPU.
+ *   Errors  Never aborts and never prints. Argument checks run on the host
+ *           before anything is enqueued; a failed check returns a status and
+ *           launches nothing. A kernel that waits on its own pipeline gives up
+ *           after a bounded time, records the fact in a device error word and
+ *           returns; gemm_check_device_error() reads and clears that word.
+ *
+ * Thread safety: the entry points may be called from several host threads;
+ * per-device set-up (kernel attributes, device properties) is done once under
+ * a lock.
+ */
+#ifndef DENSE_GEMM_ROW_H
+#define DENSE_GEMM_ROW_H
+
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define GEMM_API __attribute__((visibility("default")))
+#else
+#define GEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_VALUE = 1,      /* negative size, ld < row length, NULL operand */
+    GEMM_ERR_UNSUPPORTED_LAYOUT = 2, /* tensor-core path: base or row stride not 16-byte aligned */
+    GEMM_ERR_LAUNCH = 3,             /* a CUDA call or kernel launch failed */
+    GEMM_ERR_DEVICE = 4,             /* no current device, or it is not an sm_103 GPU */
+    GEMM_ERR_TIMEOUT = 5             /* a kernel's bounded pipeline wait gave up */
+} gemm_status_t;
+
+/* Bit patterns of 16-bit floats, as stored in memory. */
+typedef uint16_t gemm_bf16_t; /* bfloat16: the upper half of an IEEE binary32 */
+typedef uint16_t gemm_f16_t;  /* IEEE binary16 */
+
+/*
+ * gemm_f32 -- exact-fp32 SGEMM on the SIMT FP32 pipe (no TF32).
+ * A, B, C: float. Each output is one fp32 sum of the K products in some order,
+ * then alpha*acc + beta*C in fp32. Any alignment and any ld are accepted.
+ * Sources: "Sgemm [128,128,8]" (the 128x128x8 tiled kernel with 8x8 per-thread
+ * register blocks); "CUDA学习之路[11]：矩阵乘法计算详解", sections V1 2D Thread,
+ * V2 Tile and V3 双缓冲 (register tiling, float4 loads, double buffering).
+ */
+GEMM_API gemm_status_t gemm_f32(int64_t M, int64_t N, int64_t K, float alpha,
+                       const float *A, int64_t lda, const float *B, int64_t ldb,
+                       float beta, float *C, int64_t ldc, cudaStream_t stream);
+
+/*
+ * gemm_bf16 / gemm_f16 -- tensor-core GEMM: 16-bit inputs, fp32 accumulation,
+ * fp32 output C. Each product of two 16-bit values is exact in fp32; sums are
+ * accumulated in fp32 in the tensor core's order.
+ * Layout rule (the same one the WMMA page states for ldm, and the one the
+ * tensor-memory copy engine requires): A and B must start on a 16-byte boundary
+ * and lda, ldb must be multiples of 8 elements; otherwise
+ * GEMM_ERR_UNSUPPORTED_LAYOUT is returned and nothing is launched. C has no
+ * alignment requirement.
+ * Source: C++ warp-matrix-function page, section mma_sync and the type table
+ * rows __half x __half -> float and __nv_bfloat16 x __nv_bfloat16 -> float.
+ */
+GEMM_API gemm_status_t gemm_bf16(int64_t M, int64_t N, int64_t K, float alpha,
+                        const gemm_bf16_t *A, int64_t lda, const gemm_bf16_t *B,
+                        int64_t ldb, float beta, float *C, int64_t ldc,
+                        cudaStream_t stream);
+
+GEMM_API gemm_status_t gemm_f16(int64_t M, int64_t N, int64_t K, float alpha,
+                       const gemm_f16_t *A, int64_t lda, const gemm_f16_t *B,
+                       int64_t ldb, float beta, float *C, int64_t ldc,
+                       cudaStream_t stream);
+
+/*
+ * gemm_s8 -- int8 inputs, exact int32 accumulation, int32 output C.
+ * C = alpha*acc + beta*C in int32 two's-complement wrap-around arithmetic: the
+ * result is the exact integer value modulo 2^32.
+ * Source: C++ warp-matrix-function page, type table row signed char x signed
+ * char -> int.
+ */
+GEMM_API gemm_status_t gemm_s8(int64_t M, int64_t N, int64_t K, int32_t alpha,
+                      const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
+                      int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream);
+
+/* A constant, human-readable name for a status. Never NULL. */
+GEMM_API const char *gemm_status_string(gemm_status_t status);
+
+/*
+ * Reads and clears the current device's error word. Synchronises the device.
+ * Returns GEMM_ERR_TIMEOUT if a kernel gave up a bounded wait since the last
+ * call, GEMM_OK otherwise (or GEMM_ERR_DEVICE / GEMM_ERR_LAUNCH when the device
+ * cannot be queried). Optionally stores the raw word in *word (may be NULL):
+ * bit 0 = a wait timed out, bits 8..15 = the code of the first wait that did.
+ */
+GEMM_API gemm_status_t gemm_check_device_error(uint32_t *word);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+GEMM_API int gemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DENSE_GEMM_ROW_H */

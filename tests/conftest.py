@@ -17,3 +17,12 @@ def oracle_mod():
     from oracle import oracle as o
     o.build()
     return o
+
+
+@pytest.fixture(scope="session")
+def gemm_mod():
+    """The ctypes binding, building the library first if needed."""
+    from dense_gemm_row_gb300 import build as b
+    b.build(quiet=True)
+    from dense_gemm_row_gb300 import binding as g
+    return g

@@ -1,0 +1,238 @@
+"""GPU parity: every C-ABI entry point against the CPU oracle on the same seeded
+inputs. Bit-exact for int8 and for integer-valued fp32 (and for integer-valued
+16-bit inputs whose sums stay below 2^24); relative Frobenius error <= 1e-5
+against the float64 oracle otherwise."""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+from dense_gemm_row_gb300 import workloads as w
+from tests.gpu_util import Banded, dev_copy, rel_frobenius, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-5
+FLOAT_DTYPES = [torch.float32, torch.bfloat16, torch.float16]
+ALL_DTYPES = FLOAT_DTYPES + [torch.int8]
+
+
+@pytest.fixture(autouse=True)
+def clean_error_word(gemm_mod):
+    gemm_mod.check_device_error()
+    yield
+    torch.cuda.synchronize()
+    assert gemm_mod.check_device_error() == 0
+
+
+def poison_of(dtype):
+    return w.INT8_POISON if dtype == torch.int8 else float("nan")
+
+
+def run_gpu(gemm_mod, p: w.Problem, ldc=None) -> tuple[torch.Tensor, Banded]:
+    A = dev_copy(p.A, poison_of(p.A.dtype))
+    B = dev_copy(p.B, poison_of(p.B.dtype))
+    out = Banded(p.C0.contiguous(), ldc)
+    gemm_mod.gemm(A, B, out.C, p.alpha, p.beta)
+    torch.cuda.synchronize()
+    return out.result(), out
+
+
+def oracle_of(oracle_mod, p: w.Problem, rows=None):
+    if rows is None:
+        if p.A.dtype == torch.int8:
+            return oracle_mod.gemm_s8(p.A, p.B, int(p.alpha), int(p.beta), p.C0)
+        return oracle_mod.gemm(p.A, p.B, p.alpha, p.beta, p.C0)
+    return oracle_mod.gemm_rows(p.A, p.B, rows, p.alpha, p.beta, p.C0)
+
+
+def assert_parity(got, ref, exact):
+    got = got.numpy() if isinstance(got, torch.Tensor) else got
+    if exact:
+        np.testing.assert_array_equal(got.astype(np.float64) if got.dtype != np.int32 else got,
+                                      ref)
+    else:
+        err = rel_frobenius(got, ref)
+        assert err <= TOL, f"relative Frobenius error {err:.3e} > {TOL}"
+
+
+# ----------------------------------------------------------- the five configs
+
+def test_config_f32_int128_bit_exact(gemm_mod, oracle_mod):
+    p = w.config("f32_int128")
+    got, out = run_gpu(gemm_mod, p)
+    assert_parity(got, oracle_of(oracle_mod, p), exact=True)
+    out.check_canaries()
+
+
+def test_config_f32_ragged(gemm_mod, oracle_mod):
+    p = w.config("f32_ragged")
+    got, out = run_gpu(gemm_mod, p)
+    assert_parity(got, oracle_of(oracle_mod, p), exact=False)
+    out.check_canaries()
+
+
+@pytest.mark.parametrize("name", ["f32_4096", "bf16_8192", "f16_8192", "s8_8192"])
+def test_config_full_size_sampled_rows(gemm_mod, oracle_mod, name):
+    """Full-size configs in the benchmark's launch configuration; the oracle
+    computes a sample of rows covering first/last tiles and tile boundaries."""
+    p = w.config(name)
+    got, _ = run_gpu(gemm_mod, p)
+    rows = sample_rows(p.A.shape[0], 40, seed=7)
+    ref = oracle_of(oracle_mod, p, rows)
+    assert_parity(got[rows], ref, exact=(p.A.dtype == torch.int8))
+
+
+# ------------------------------------------------------------- edge sweep
+
+EDGE = [1, 2, 3, 7, 8, 9, 15, 16, 17, 31, 33, 63, 65, 127, 128, 129, 255, 257]
+
+
+def edge_shapes(count, seed):
+    rng = np.random.default_rng(seed)
+    allc = list(itertools.product(EDGE, EDGE, EDGE))
+    idx = rng.choice(len(allc), size=count, replace=False)
+    picked = [allc[i] for i in idx]
+    return picked + [(1, 1, 1), (257, 257, 257), (129, 1, 257), (1, 257, 129)]
+
+
+def ld_for(dtype, cols):
+    # The tensor-core entry points need row strides that are multiples of 8.
+    if dtype in (torch.bfloat16, torch.float16):
+        return (cols + 7) // 8 * 8
+    return None
+
+
+@pytest.mark.parametrize("dtype", ALL_DTYPES, ids=str)
+@pytest.mark.parametrize("shape", edge_shapes(24, 3), ids=lambda s: "x".join(map(str, s)))
+def test_edge_sweep(gemm_mod, oracle_mod, dtype, shape):
+    M, N, K = shape
+    if dtype == torch.int8:
+        p = w.problem(M, N, K, dtype, "int8", 100 + M + 7 * N + 13 * K, alpha=3, beta=-2,
+                      c_dist="int")
+    else:
+        p = w.problem(M, N, K, dtype, "uniform_pm1", 100 + M + 7 * N + 13 * K, alpha=1.5,
+                      beta=-0.5, c_dist="uniform_pm1", lda=ld_for(dtype, K), ldb=ld_for(dtype, N))
+    got, out = run_gpu(gemm_mod, p, ldc=N + 3)
+    assert_parity(got, oracle_of(oracle_mod, p), exact=(dtype == torch.int8))
+    out.check_canaries()
+
+
+@pytest.mark.parametrize("dtype", ALL_DTYPES, ids=str)
+def test_many_tiles_ragged_tail(gemm_mod, oracle_mod, dtype):
+    """Several tiles in each direction plus a ragged tail in M, N and K."""
+    M, N, K = 397, 611, 1111
+    if dtype == torch.int8:
+        p = w.problem(M, N, K, dtype, "int8", 41, alpha=-1, beta=1, c_dist="int",
+                      lda=1120, ldb=640)
+    else:
+        p = w.problem(M, N, K, dtype, "normal", 41, alpha=0.5, beta=2.0, c_dist="normal",
+                      lda=1120, ldb=616)
+    got, out = run_gpu(gemm_mod, p, ldc=650)
+    assert_parity(got, oracle_of(oracle_mod, p), exact=(dtype == torch.int8))
+    out.check_canaries()
+
+
+@pytest.mark.parametrize("dtype", ALL_DTYPES, ids=str)
+def test_tiled_page_odd_shape_exact(gemm_mod, oracle_mod, dtype):
+    """The tiled-multiply page's harness: 47 x 804 times 804 x 53 with integers
+    0..99 (rand() % 100). Every partial sum is an integer below 2^24 and the
+    values are exact in every input type, so every path must be bit-exact."""
+    M, K, N = 47, 804, 53
+    A = w.matrix(M, K, torch.float32, "int0_99", 51)
+    B = w.matrix(K, N, torch.float32, "int0_99", 52)
+    lda, ldb = (808, 56) if dtype in (torch.bfloat16, torch.float16) else (None, None)
+    Ap = torch.full((M, lda or K), 0.0)[:, :K] if lda else A
+    Bp = torch.full((K, ldb or N), 0.0)[:, :N] if ldb else B
+    if lda:
+        Ap.copy_(A)
+        Bp.copy_(B)
+    if dtype == torch.int8:
+        A8 = (Ap - 50).to(torch.int8)
+        B8 = (Bp - 50).to(torch.int8)
+        p = w.Problem("odd", A8, B8, torch.zeros(M, N, dtype=torch.int32), 1, 0)
+    else:
+        p = w.Problem("odd", Ap.to(dtype), Bp.to(dtype), torch.zeros(M, N), 1.0, 0.0)
+    got, out = run_gpu(gemm_mod, p)
+    assert_parity(got, oracle_of(oracle_mod, p), exact=True)
+    out.check_canaries()
+
+
+# ------------------------------------------------------------ special cases
+
+@pytest.mark.parametrize("dtype", ALL_DTYPES, ids=str)
+def test_beta_zero_never_reads_c(gemm_mod, oracle_mod, dtype):
+    M, N, K = 130, 260, 70
+    if dtype == torch.int8:
+        p = w.problem(M, N, K, dtype, "int8", 61, alpha=2, beta=0)
+        p.C0 = torch.full((M, N), -7, dtype=torch.int32)
+    else:
+        p = w.problem(M, N, K, dtype, "normal", 61, alpha=2.0, beta=0.0, c_dist="nan",
+                      lda=ld_for(dtype, K), ldb=ld_for(dtype, N))
+    got, _ = run_gpu(gemm_mod, p)
+    if dtype != torch.int8:
+        assert torch.isfinite(got).all()
+    assert_parity(got, oracle_of(oracle_mod, p), exact=(dtype == torch.int8))
+
+
+@pytest.mark.parametrize("dtype", ALL_DTYPES, ids=str)
+def test_alpha_zero_and_k_zero(gemm_mod, oracle_mod, dtype):
+    M, N = 67, 45
+    for K, alpha in ((33, 0), (0, 1)):
+        if dtype == torch.int8:
+            p = w.problem(M, N, K, dtype, "int8", 71, alpha=alpha, beta=-3, c_dist="int")
+        else:
+            p = w.problem(M, N, K, dtype, "normal", 71, alpha=float(alpha), beta=-3.0,
+                          c_dist="normal", lda=ld_for(dtype, max(K, 1)), ldb=ld_for(dtype, N))
+        got, out = run_gpu(gemm_mod, p, ldc=N + 5)
+        ref = oracle_of(oracle_mod, p)
+        # alpha*acc + beta*C with alpha = 0 or an empty sum is exactly beta*C.
+        assert_parity(got, ref, exact=True)
+        out.check_canaries()
+
+
+def test_int8_extremes_and_chunk_boundary(gemm_mod, oracle_mod):
+    """All -128: every output is K * 16384. At K = 8192 the int8 path's exact
+    fp32 partial sums reach 2^24 per 1024-long chunk."""
+    for K in (1023, 1024, 1025, 8192):
+        A = torch.full((200, K), -128, dtype=torch.int8)
+        B = torch.full((K, 300), -128, dtype=torch.int8)
+        p = w.Problem("ext", A, B, torch.zeros(200, 300, dtype=torch.int32), 1, 0)
+        got, _ = run_gpu(gemm_mod, p)
+        assert (got == K * 16384).all()
+        B2 = torch.full((K, 300), 127, dtype=torch.int8)
+        p2 = w.Problem("ext2", A, B2, torch.zeros(200, 300, dtype=torch.int32), 1, 0)
+        got2, _ = run_gpu(gemm_mod, p2)
+        assert (got2 == -K * 16256).all()
+
+
+def test_int8_wraparound(gemm_mod, oracle_mod):
+    p = w.problem(150, 270, 2048, torch.int8, "int8", 81, alpha=2**31 - 1, beta=-2**31,
+                  c_dist="int")
+    got, _ = run_gpu(gemm_mod, p)
+    assert_parity(got, oracle_of(oracle_mod, p), exact=True)
+
+
+@pytest.mark.parametrize("dtype", FLOAT_DTYPES, ids=str)
+def test_identity_returns_b(gemm_mod, dtype):
+    """A = I: C = B exactly (each output is one product by 1 plus zeros)."""
+    K, N = 256, 264
+    I = torch.eye(K, dtype=dtype)
+    B = w.matrix(K, N, dtype, "normal", 91)
+    p = w.Problem("eye", I, B, torch.zeros(K, N), 1.0, 0.0)
+    got, _ = run_gpu(gemm_mod, p)
+    np.testing.assert_array_equal(got.numpy(), B.to(torch.float32).numpy())
+
+
+def test_streams_are_respected(gemm_mod, oracle_mod):
+    """Work is enqueued on the given stream: results are ready after that
+    stream is synchronised."""
+    p = w.problem(512, 512, 512, torch.bfloat16, "normal", 95)
+    A, B = p.A.cuda(), p.B.cuda()
+    C = torch.zeros(512, 512, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        gemm_mod.gemm_bf16(512, 512, 512, 1.0, A, 512, B, 512, 0.0, C, 512, s)
+    s.synchronize()
+    assert rel_frobenius(C.cpu().numpy(), oracle_of(oracle_mod, p)) <= TOL
