@@ -369,7 +369,7 @@ def main():
 
     peaks, peak_src = load_peaks()
     props = torch.cuda.get_device_properties(local_rank)
-    sm_count = props.multiProcessorCount
+    sm_count = props.multi_processor_count
     gpu_id = None
     try:
         gpu_id = "GPU-" + str(props.uuid)

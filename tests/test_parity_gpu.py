@@ -142,18 +142,18 @@ def test_tiled_page_odd_shape_exact(gemm_mod, oracle_mod, dtype):
     M, K, N = 47, 804, 53
     A = w.matrix(M, K, torch.float32, "int0_99", 51)
     B = w.matrix(K, N, torch.float32, "int0_99", 52)
-    lda, ldb = (808, 56) if dtype in (torch.bfloat16, torch.float16) else (None, None)
-    Ap = torch.full((M, lda or K), 0.0)[:, :K] if lda else A
-    Bp = torch.full((K, ldb or N), 0.0)[:, :N] if ldb else B
-    if lda:
-        Ap.copy_(A)
-        Bp.copy_(B)
     if dtype == torch.int8:
-        A8 = (Ap - 50).to(torch.int8)
-        B8 = (Bp - 50).to(torch.int8)
-        p = w.Problem("odd", A8, B8, torch.zeros(M, N, dtype=torch.int32), 1, 0)
+        A, B = A - 50, B - 50  # int8 range
+        C0 = torch.zeros(M, N, dtype=torch.int32)
     else:
-        p = w.Problem("odd", Ap.to(dtype), Bp.to(dtype), torch.zeros(M, N), 1.0, 0.0)
+        C0 = torch.zeros(M, N)
+    lda, ldb = (808, 56) if dtype in (torch.bfloat16, torch.float16) else (K, N)
+    Ap = torch.zeros((M, lda), dtype=dtype)[:, :K]
+    Bp = torch.zeros((K, ldb), dtype=dtype)[:, :N]
+    Ap.copy_(A)
+    Bp.copy_(B)
+    one, zero = (1, 0) if dtype == torch.int8 else (1.0, 0.0)
+    p = w.Problem("odd", Ap, Bp, C0, one, zero)
     got, out = run_gpu(gemm_mod, p)
     assert_parity(got, oracle_of(oracle_mod, p), exact=True)
     out.check_canaries()
@@ -183,7 +183,9 @@ def test_alpha_zero_and_k_zero(gemm_mod, oracle_mod, dtype):
         if dtype == torch.int8:
             p = w.problem(M, N, K, dtype, "int8", 71, alpha=alpha, beta=-3, c_dist="int")
         else:
-            p = w.problem(M, N, K, dtype, "normal", 71, alpha=float(alpha), beta=-3.0,
+            # beta = -2: beta*C is exact in fp32, so the fp32 result equals the
+            # float64 oracle bit for bit.
+            p = w.problem(M, N, K, dtype, "normal", 71, alpha=float(alpha), beta=-2.0,
                           c_dist="normal", lda=ld_for(dtype, max(K, 1)), ldb=ld_for(dtype, N))
         got, out = run_gpu(gemm_mod, p, ldc=N + 5)
         ref = oracle_of(oracle_mod, p)
