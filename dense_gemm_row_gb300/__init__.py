@@ -9,7 +9,7 @@ raises ImportError if it is missing: there is no fallback path.
 """
 import importlib
 
-__all__ = ["gemm_f32", "gemm_bf16", "gemm_f16", "gemm_s8", "gemm", "GemmError",
+__all__ = ["gemm_f32", "gemm_bf16", "gemm_f16", "gemm_s8", "gemm_s8_noalloc", "gemm", "GemmError",
            "check_device_error", "lib"]
 
 

@@ -30,11 +30,12 @@ STATUS = {
     3: "GEMM_ERR_LAUNCH",
     4: "GEMM_ERR_DEVICE",
     5: "GEMM_ERR_TIMEOUT",
+    6: "GEMM_ERR_TOO_LARGE",
 }
 
 # Every function include/dense_gemm_row.h declares.
-EXPORTED = ("gemm_f32", "gemm_bf16", "gemm_f16", "gemm_s8", "gemm_status_string",
-            "gemm_check_device_error", "gemm_version")
+EXPORTED = ("gemm_f32", "gemm_bf16", "gemm_f16", "gemm_s8", "gemm_s8_noalloc",
+            "gemm_status_string", "gemm_check_device_error", "gemm_version")
 
 
 class GemmError(RuntimeError):
@@ -55,8 +56,10 @@ def _load():
         fn = getattr(lib, name)
         fn.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
         fn.restype = ctypes.c_int
-    lib.gemm_s8.argtypes = [i64, i64, i64, i32, vp, i64, vp, i64, i32, vp, i64, vp]
-    lib.gemm_s8.restype = ctypes.c_int
+    for name in ("gemm_s8", "gemm_s8_noalloc"):
+        fn = getattr(lib, name)
+        fn.argtypes = [i64, i64, i64, i32, vp, i64, vp, i64, i32, vp, i64, vp]
+        fn.restype = ctypes.c_int
     lib.gemm_status_string.argtypes = [ctypes.c_int]
     lib.gemm_status_string.restype = ctypes.c_char_p
     lib.gemm_check_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
@@ -109,6 +112,14 @@ def gemm_f16(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
 def gemm_s8(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
     _check(lib.gemm_s8(M, N, K, int(alpha), _addr(A), lda, _addr(B), ldb, int(beta), _addr(C),
                        ldc, _stream(stream)), "gemm_s8")
+
+
+def gemm_s8_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
+    """gemm_s8 on the library's fixed scratch array: allocates no device memory.
+    Problems needing more than 64 MiB of widened operands raise GemmError
+    (GEMM_ERR_TOO_LARGE); calls that overlap on the GPU race on the array."""
+    _check(lib.gemm_s8_noalloc(M, N, K, int(alpha), _addr(A), lda, _addr(B), ldb, int(beta),
+                               _addr(C), ldc, _stream(stream)), "gemm_s8_noalloc")
 
 
 def check_device_error() -> int:

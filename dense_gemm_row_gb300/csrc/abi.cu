@@ -114,6 +114,15 @@ cudaError_t launch_scale(int M, int N, T beta, T *C, int64_t ldc, cudaStream_t s
 
 }  // namespace
 
+int abi_check_args(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+                   int64_t ldb, const void *C, int64_t ldc, bool *nothing_to_do) {
+  return check_args(M, N, K, A, lda, B, ldb, C, ldc, nothing_to_do);
+}
+
+int abi_current_device(const DeviceInfo **out) { return current_device(out); }
+
+int abi_from_cuda(cudaError_t e) { return from_cuda(e); }
+
 cudaError_t launch_scale_f32(int M, int N, float beta, float *C, int64_t ldc,
                              cudaStream_t stream) {
   return launch_scale<float>(M, N, beta, C, ldc, stream);
@@ -198,6 +207,7 @@ const char *gemm_status_string(gemm_status_t status) {
     case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH";
     case GEMM_ERR_DEVICE: return "GEMM_ERR_DEVICE";
     case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT";
+    case GEMM_ERR_TOO_LARGE: return "GEMM_ERR_TOO_LARGE";
   }
   return "GEMM_ERR_UNKNOWN";
 }

@@ -521,4 +521,33 @@ cudaError_t launch_gemm_s8(const DeviceInfo &dev, int M, int N, int K, int32_t a
   return e != cudaSuccess ? e : f;
 }
 
+
+// The int8 path with scratch memory supplied by the caller instead of drawn
+// from the library's pool: widen A and B into `scratch` (which must hold
+// s8_scratch_bytes(M, N, K) bytes, 256-byte aligned) and run the tensor-core
+// kernel in exact-integer mode. Allocates nothing.
+size_t s8_scratch_bytes(int M, int N, int K) {
+  const int64_t lda16 = (static_cast<int64_t>(K) + 7) / 8 * 8;
+  const int64_t ldb16 = (static_cast<int64_t>(N) + 7) / 8 * 8;
+  const size_t a_off = (static_cast<size_t>(M) * lda16 * 2 + 255) / 256 * 256;
+  return a_off + static_cast<size_t>(K) * ldb16 * 2;
+}
+
+cudaError_t launch_gemm_s8_scratch(const DeviceInfo &dev, int M, int N, int K, int32_t alpha,
+                                   const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
+                                   int32_t beta, int32_t *C, int64_t ldc, void *scratch,
+                                   cudaStream_t stream) {
+  const int64_t lda16 = (static_cast<int64_t>(K) + 7) / 8 * 8;
+  const int64_t ldb16 = (static_cast<int64_t>(N) + 7) / 8 * 8;
+  const size_t a_off = (static_cast<size_t>(M) * lda16 * 2 + 255) / 256 * 256;
+  __half *a16 = static_cast<__half *>(scratch);
+  __half *b16 = reinterpret_cast<__half *>(static_cast<uint8_t *>(scratch) + a_off);
+  cudaError_t e = widen_s8(dev, A, lda, a16, lda16, M, K, stream);
+  if (e == cudaSuccess) e = widen_s8(dev, B, ldb, b16, ldb16, K, N, stream);
+  if (e == cudaSuccess)
+    e = launch_tc<true>(dev, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, false, M, N, K, alpha, a16, lda16,
+                        b16, ldb16, beta, C, ldc, stream);
+  return e;
+}
+
 }  // namespace dgr

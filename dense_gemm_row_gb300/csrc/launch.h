@@ -38,10 +38,25 @@ cudaError_t launch_gemm_s8(const DeviceInfo &dev, int M, int N, int K, int32_t a
                            const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
                            int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream);
 
+// Bytes of scratch the int8 path needs, and the int8 path on caller-provided
+// scratch (256-byte aligned, at least s8_scratch_bytes(M, N, K) bytes).
+size_t s8_scratch_bytes(int M, int N, int K);
+cudaError_t launch_gemm_s8_scratch(const DeviceInfo &dev, int M, int N, int K, int32_t alpha,
+                                   const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
+                                   int32_t beta, int32_t *C, int64_t ldc, void *scratch,
+                                   cudaStream_t stream);
+
 // K == 0: C = beta * C (C = 0 when beta == 0), M x N window only.
 cudaError_t launch_scale_f32(int M, int N, float beta, float *C, int64_t ldc,
                              cudaStream_t stream);
 cudaError_t launch_scale_s32(int M, int N, int32_t beta, int32_t *C, int64_t ldc,
                              cudaStream_t stream);
+
+// Accessors to the ABI layer's shared host logic (defined in abi.cu). The
+// status values are those of gemm_status_t.
+int abi_check_args(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+                   int64_t ldb, const void *C, int64_t ldc, bool *nothing_to_do);
+int abi_current_device(const DeviceInfo **out);
+int abi_from_cuda(cudaError_t e);
 
 }  // namespace dgr

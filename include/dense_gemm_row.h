@@ -70,7 +70,8 @@ typedef enum {
     GEMM_ERR_UNSUPPORTED_LAYOUT = 2, /* tensor-core path: base or row stride not 16-byte aligned */
     GEMM_ERR_LAUNCH = 3,             /* a CUDA call or kernel launch failed */
     GEMM_ERR_DEVICE = 4,             /* no current device, or it is not an sm_103 GPU */
-    GEMM_ERR_TIMEOUT = 5             /* a kernel's bounded pipeline wait gave up */
+    GEMM_ERR_TIMEOUT = 5,            /* a kernel's bounded pipeline wait gave up */
+    GEMM_ERR_TOO_LARGE = 6           /* gemm_s8_noalloc: problem needs more than its fixed scratch */
 } gemm_status_t;
 
 /* Bit patterns of 16-bit floats, as stored in memory. */
@@ -121,6 +122,40 @@ GEMM_API gemm_status_t gemm_f16(int64_t M, int64_t N, int64_t K, float alpha,
 GEMM_API gemm_status_t gemm_s8(int64_t M, int64_t N, int64_t K, int32_t alpha,
                       const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
                       int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream);
+
+/*
+ * gemm_s8_noalloc -- gemm_s8 for callers that must not allocate device memory.
+ * The pages have no counterpart of this entry point; it is part of this
+ * library's interface only.
+ *
+ * gemm_s8 widens A and B to fp16 in scratch memory that it takes from a
+ * library-owned stream-ordered pool. Some callers cannot allow that: a process
+ * whose device memory is entirely reserved up front by another allocator (so
+ * any extra allocation can fail or fragment it), a latency-critical loop that
+ * must never enter the driver's allocation path, or a deployment that forbids
+ * allocation after start-up. This variant computes exactly what gemm_s8
+ * computes (same arguments, same bit-exact result) but calls no cudaMalloc,
+ * cudaFree or allocating library routine: its scratch is a fixed 64 MiB array
+ * in the library's device memory, which every GPU that loads this part of the
+ * library keeps until the process exits. The caller still provides A, B and C.
+ *
+ * Limit: 2 * (M * ceil8(K) + K * ceil8(N)) bytes, with the A part rounded up
+ * to 256 bytes, must not exceed 64 MiB (for example M = N = K = 4096 fits);
+ * larger problems return GEMM_ERR_TOO_LARGE and launch nothing. Argument
+ * checks are those of gemm_s8.
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture begins. A failed look-up returns GEMM_ERR_DEVICE.
+ * Concurrency: all calls on a device share the one array, and each call
+ * overwrites every scratch element it later reads, so no state carries over
+ * from the previous call; but calls that can overlap on the GPU (different
+ * streams without ordering between them) race on the array and give wrong
+ * results. Order them on one stream, or use gemm_s8.
+ */
+GEMM_API gemm_status_t gemm_s8_noalloc(int64_t M, int64_t N, int64_t K, int32_t alpha,
+                                       const int8_t *A, int64_t lda, const int8_t *B,
+                                       int64_t ldb, int32_t beta, int32_t *C, int64_t ldc,
+                                       cudaStream_t stream);
 
 /* A constant, human-readable name for a status. Never NULL. */
 GEMM_API const char *gemm_status_string(gemm_status_t status);
