@@ -13,9 +13,14 @@
 //    values a thread needs for one k are two 16-byte shared loads ("Sgemm
 //    [128,128,8]", the transposed smema buffer; "CUDA学习之路[11]", section
 //    V3 双缓冲, the transposed A tile).
-//  * Staging uses cp.async with an S-stage ring instead of the pages' register
-//    prefetch plus two shared buffers (same overlap of the next tile's load
-//    with this tile's FMAs, without holding the prefetch in registers).
+//  * Staging uses cp.async with an S-stage ring (default: two stages of 32
+//    values of k) instead of the pages' register prefetch plus two shared
+//    buffers: the same overlap of the next tile's load with this tile's FMAs,
+//    without holding the prefetch in registers. The transposing copy of A is
+//    4 bytes per lane, arranged so a warp's 32 stores hit 32 distinct banks.
+//  * The 64 FMAs per k of a thread are issued as 32 packed fma.rn.f32x2
+//    (two independent fp32 FMAs, each rounded to nearest like fmaf), which
+//    halves the issue slots the FP32 pipe needs on sm_103a.
 //  * Residual tiles: out-of-range cells of the A and B tiles are filled with
 //    zeros by the copy itself (cp.async with a zero source size) and the
 //    epilogue's stores are guarded, so any M, N, K works ("使用CUDA和瓦片算法
@@ -38,6 +43,18 @@
 namespace dgr {
 namespace {
 
+#ifndef DGR_SIMT_FFMA2
+#define DGR_SIMT_FFMA2 1
+#endif
+
+// (c0, c1) = (a * b0 + c0, a * b1 + c1) with one packed fp32 FMA.
+__device__ __forceinline__ void ffma2(float &c0, float &c1, float a, float b0, float b1) {
+  asm("{\n .reg .b64 ra, rb, rc;\n mov.b64 ra, {%2, %2};\n mov.b64 rb, {%3, %4};\n"
+      " mov.b64 rc, {%0, %1};\n fma.rn.f32x2 rc, ra, rb, rc;\n mov.b64 {%0, %1}, rc;\n}\n"
+      : "+f"(c0), "+f"(c1)
+      : "f"(a), "f"(b0), "f"(b1));
+}
+
 constexpr int kBM = 128;
 constexpr int kBN = 128;
 constexpr int kThreads = 256;
@@ -56,10 +73,15 @@ struct SimtArgs {
   int c_vec_ok;  // C 16-byte aligned and ldc % 4 == 0
 };
 
+// Row stride of the transposed A tile: 132 = 128 + 4 floats. With it, the
+// 4-byte copies of one warp (4 rows x 8 consecutive k) land in 32 distinct
+// banks, and every 4-float group stays 16-byte aligned for the fragment loads.
+constexpr int kAStride = kBM + 4;
+
 template <int BK, int STAGES>
 struct SimtSmem {
-  float a[STAGES][BK][kBM];  // A tile, transposed: a[s][k][m]
-  float b[STAGES][BK][kBN];  // B tile: b[s][k][n]
+  float a[STAGES][BK][kAStride];  // A tile, transposed: a[s][k][m]
+  float b[STAGES][BK][kBN];       // B tile: b[s][k][n]
 };
 
 // Linear CTA index -> (tile_m, tile_n): groups of kGroupM tile rows are walked
@@ -75,22 +97,25 @@ __device__ __forceinline__ void tile_coords(int bid, int tiles_m, int tiles_n, i
 }
 
 template <int BK, bool VEC_B>
-__device__ __forceinline__ void load_tile(const SimtArgs &p, float (*sa)[kBM], float (*sb)[kBN],
-                                          int m0, int n0, int k0, int tid) {
-  // A: BK/2 elements per thread, one row each, consecutive k. A warp covers 32
-  // consecutive rows at one k, so the transposed shared stores never conflict.
+__device__ __forceinline__ void load_tile(const SimtArgs &p, float (*sa)[kAStride],
+                                          float (*sb)[kBN], int m0, int n0, int k0, int tid) {
+  // A: one warp instruction copies 4 rows x 8 consecutive k (lane = 8*row + k),
+  // i.e. four 32-byte global segments, into the transposed tile. The BK/2
+  // instructions of a thread walk (row group, k half) pairs of its warp.
   {
-    constexpr int kPer = BK / 2;
-    const int m = tid & (kBM - 1);
-    const int kq = (tid >> 7) * kPer;
-    const int gm = m0 + m;
-    const bool row_ok = gm < p.M;
-    const float *src = p.A + (row_ok ? static_cast<int64_t>(gm) * p.lda : 0);
+    static_assert(BK % 8 == 0, "A staging copies k in groups of 8");
+    constexpr int kGroupsK = BK / 8;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int r_lo = lane >> 3, k_lo = lane & 7;
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int gk = k0 + kq + i;
-      const bool ok = row_ok && gk < p.K;
-      cp_async_4(smem_u32(&sa[kq + i][m]), ok ? src + gk : p.A, ok ? 4u : 0u);
+    for (int i = 0; i < BK / 2; ++i) {
+      const int pair = warp * (BK / 2) + i;        // 0 .. 4*BK-1
+      const int m = (pair / kGroupsK) * 4 + r_lo;   // 32 groups of 4 rows
+      const int k = (pair % kGroupsK) * 8 + k_lo;   // groups of 8 k
+      const int gm = m0 + m, gk = k0 + k;
+      const bool ok = gm < p.M && gk < p.K;
+      const float *src = ok ? p.A + static_cast<int64_t>(gm) * p.lda + gk : p.A;
+      cp_async_4(smem_u32(&sa[k][m]), src, ok ? 4u : 0u);
     }
   }
   // B: row-major BK x 128 tile.
@@ -171,9 +196,17 @@ __global__ void __launch_bounds__(kThreads, 2) sgemm_simt_kernel(const SimtArgs 
       const float a[8] = {a_lo.x, a_lo.y, a_lo.z, a_lo.w, a_hi.x, a_hi.y, a_hi.z, a_hi.w};
       const float b[8] = {b_lo.x, b_lo.y, b_lo.z, b_lo.w, b_hi.x, b_hi.y, b_hi.z, b_hi.w};
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < 8; ++i) {
+#if DGR_SIMT_FFMA2
+        // Two lanes of one row per instruction: (acc[i][j], acc[i][j+1]) +=
+        // a[i] * (b[j], b[j+1]); one IEEE round-to-nearest per lane, as fmaf.
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) ffma2(acc[i][j], acc[i][j + 1], a[i], b[j], b[j + 1]);
+#else
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+#endif
+      }
     }
   }
   cp_async_wait<0>();
@@ -248,7 +281,13 @@ cudaError_t launch_sgemm_simt(const DeviceInfo &dev, int M, int N, int K, float 
   a.c_vec_ok = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0);
   if (static_cast<int64_t>(a.tiles_m) * a.tiles_n > 0x7fffffffLL) return cudaErrorInvalidValue;
   const bool vec_b = (reinterpret_cast<uintptr_t>(B) % 16 == 0) && (ldb % 4 == 0) && (N % 4 == 0);
-  constexpr int kBK = 16, kStages = 3;
+#ifndef DGR_SIMT_BK
+#define DGR_SIMT_BK 32
+#endif
+#ifndef DGR_SIMT_STAGES
+#define DGR_SIMT_STAGES 2
+#endif
+  constexpr int kBK = DGR_SIMT_BK, kStages = DGR_SIMT_STAGES;
   return vec_b ? launch_variant<kBK, kStages, true>(a, stream)
                : launch_variant<kBK, kStages, false>(a, stream);
 }
