@@ -333,6 +333,77 @@ def run_reference(args, world, rank):
     return 0
 
 
+# ------------------------------------------------------------ other workloads
+
+def measure_extra(binding, torch, w, name, peaks, sm_count, stream, gpu_id):
+    """Device-timed throughput of another named workload, with its own clock
+    samples and roofline fraction."""
+    desc, kind, bound, _ = WORKLOADS[name]
+    q = w.config(name)
+    q_dev = device_problem(torch, q)
+    M, K = q.A.shape
+    N = q.B.shape[1]
+    steps = 100 if kind != "f32" else 60
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    ms, t0, t1 = time_device(binding, torch, kind, q_dev, steps, 5, stream)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+    f = flops_of(M, N, K)
+    ach = f / (ms / steps / 1e3) / 1e12
+    pk = peak_for(kind, peaks, sm_count)
+    out = {"workload": desc, "value": ach, "unit": "TOPS" if kind == "s8" else "TFLOP/s",
+           "ms_per_step": ms / steps, "bound": bound, "peak": pk, "frac": ach / pk,
+           "traffic": recorded_traffic(name),
+           "clocks": {"sm_mhz": clocks["sm_mhz"], "reasons": clocks["reasons"],
+                      "samples": clocks["samples"]}}
+    if kind == "f32" and clocks["sm_mhz"]:
+        out["frac_at_sampled_clock"] = ach / (sm_count * 128 * 2 * clocks["sm_mhz"] * 1e6 / 1e12)
+    if kind == "s8":
+        out["note"] = "step includes the two int8->fp16 widening launches"
+    del q_dev
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_skinny(binding, torch, peaks, stream):
+    """Memory-bound shapes M in {1, 16, 64}, N = K = 8192: HBM GB/s of the
+    algorithmic bytes (A and B read once, C written once) against the measured
+    copy bandwidth."""
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1234)
+    N = K = 8192
+    out = {}
+    for kind, dt, cdt in (("bf16", torch.bfloat16, torch.float32),
+                          ("f16", torch.float16, torch.float32),
+                          ("f32", torch.float32, torch.float32),
+                          ("s8", torch.int8, torch.int32)):
+        if kind == "s8":
+            B = torch.randint(-128, 128, (K, N), device="cuda", dtype=torch.int8, generator=g)
+        else:
+            B = torch.randn(K, N, device="cuda", generator=g).to(dt)
+        for M in (1, 16, 64):
+            if kind == "s8":
+                A = torch.randint(-128, 128, (M, K), device="cuda", dtype=torch.int8,
+                                  generator=g)
+                alpha, beta = 1, 0
+            else:
+                A = torch.randn(M, K, device="cuda", generator=g).to(dt)
+                alpha, beta = 1.0, 0.0
+            C = torch.zeros(M, N, device="cuda", dtype=cdt)
+            ms, _, _ = time_device(binding, torch, kind, (A, B, C, alpha, beta), 20, 3, stream)
+            t = ms / 20 / 1e3
+            nbytes = (A.numel() * A.element_size() + B.numel() * B.element_size()
+                      + C.numel() * C.element_size())
+            out[f"{kind}_M{M}"] = {"M": M, "N": N, "K": K, "ms": t * 1e3,
+                                   "gbs": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / hbm,
+                                   "tflops": flops_of(M, N, K) / t / 1e12}
+        del B
+        torch.cuda.empty_cache()
+    return out
+
+
 # ----------------------------------------------------------------------- main
 
 def main():
@@ -343,6 +414,7 @@ def main():
     ap.add_argument("--workload", default="bf16_8192", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-skinny", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -436,27 +508,13 @@ def main():
         for other in ("f32_4096", "f16_8192", "s8_8192", "bf16_8192"):
             if other == name:
                 continue
-            odesc, okind, obound, _ = WORKLOADS[other]
-            q = w.config(other)
-            q_dev = device_problem(torch, q)
-            Mo, Ko = q.A.shape
-            No = q.B.shape[1]
-            steps = 100 if okind != "f32" else 50
-            oms, _, _ = time_device(binding, torch, okind, q_dev, steps, 5, stream)
-            f = flops_of(Mo, No, Ko)
-            ach = f / (oms / steps / 1e3) / 1e12
-            opk = peak_for(okind, peaks, sm_count)
-            extras[other] = {"workload": odesc, "value": ach,
-                             "unit": "TOPS" if okind == "s8" else "TFLOP/s",
-                             "ms_per_step": oms / steps, "bound": obound, "peak": opk,
-                             "frac": ach / opk, "traffic": recorded_traffic(other)}
-            if okind == "f32":
-                mhz = clocks.get("sm_mhz")
-                if mhz:
-                    extras[other]["frac_at_sampled_clock"] = ach / (
-                        sm_count * 128 * 2 * mhz * 1e6 / 1e12)
-            del q_dev
-            torch.cuda.empty_cache()
+            extras[other] = measure_extra(binding, torch, w, other, peaks, sm_count, stream,
+                                          gpu_id)
+        binding.check_device_error()
+
+    skinny = {}
+    if not args.no_skinny:
+        skinny = measure_skinny(binding, torch, peaks, stream)
         binding.check_device_error()
 
     cpu = None
@@ -482,6 +540,7 @@ def main():
                    "reasons": clocks["reasons"], "samples": clocks["samples"],
                    "window": clocks["window"]},
         "extras": extras,
+        "skinny": skinny,
     }
     print(json.dumps(line), flush=True)
     if dist is not None:

@@ -35,7 +35,8 @@ STATUS = {
 
 # Every function include/dense_gemm_row.h declares.
 EXPORTED = ("gemm_f32", "gemm_bf16", "gemm_f16", "gemm_s8", "gemm_s8_noalloc",
-            "gemm_status_string", "gemm_check_device_error", "gemm_version")
+            "gemm_status_string", "gemm_check_device_error", "gemm_selftest_wait_timeout",
+            "gemm_version")
 
 
 class GemmError(RuntimeError):
@@ -64,6 +65,8 @@ def _load():
     lib.gemm_status_string.restype = ctypes.c_char_p
     lib.gemm_check_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.gemm_check_device_error.restype = ctypes.c_int
+    lib.gemm_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
+    lib.gemm_selftest_wait_timeout.restype = ctypes.c_int
     lib.gemm_version.argtypes = []
     lib.gemm_version.restype = ctypes.c_int
     return lib

@@ -48,19 +48,36 @@
 namespace dgr {
 namespace {
 
+#ifndef DGR_TC_BK
+#define DGR_TC_BK 64
+#endif
+#ifndef DGR_TC_STAGES
+#define DGR_TC_STAGES 4
+#endif
+#ifndef DGR_TC_GROUP_M
+#define DGR_TC_GROUP_M 16
+#endif
+
 constexpr int kBM = 128;
 constexpr int kBN = 256;
-constexpr int kBK = 64;         // 64 16-bit values = one 128-byte swizzle row
-constexpr int kStages = 4;
+// k-block: 64 16-bit values (one 128-byte swizzle row of A) or 32 (64-byte rows).
+constexpr int kBK = DGR_TC_BK;
+static_assert(kBK == 64 || kBK == 32, "k-block of 32 or 64 values");
+constexpr int kStages = DGR_TC_STAGES;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr int kGroupM = 16;
-constexpr int kChunkKB = 16;    // int mode: k-blocks per exact fp32 chunk (16 * 64 = 1024)
+constexpr int kGroupM = DGR_TC_GROUP_M;
+// int mode: k-blocks per exact fp32 chunk (1024 values of k)
+constexpr int kChunkKB = 1024 / kBK;
 constexpr uint32_t kTmemCols = 512;  // two 256-column fp32 accumulators
 
-constexpr uint32_t kABytes = kBM * kBK * 2;        // 16 KiB
-constexpr uint32_t kBBoxBytes = 64 * kBK * 2;      // one 64(N) x 64(K) box: 8 KiB
-constexpr uint32_t kBBytes = kBK * kBN * 2;        // 32 KiB
+// A rows are kBK * 2 bytes long: 128-byte swizzle for 64 values, 64-byte for 32.
+constexpr uint32_t kARowBytes = kBK * 2;
+constexpr uint32_t kASwizzleMode = kBK == 64 ? 2u : 4u;   // descriptor encoding
+constexpr uint32_t kAAtomBytes = 8 * kARowBytes;          // 8-row swizzle atom
+constexpr uint32_t kABytes = kBM * kBK * 2;               // 16 or 8 KiB
+constexpr uint32_t kBBoxBytes = 64 * kBK * 2;             // one 64(N) x kBK box
+constexpr uint32_t kBBytes = kBK * kBN * 2;               // 32 or 16 KiB
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
 
 struct __align__(1024) TcSmem {
@@ -256,11 +273,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t b_addr = smem_u32(sm.b[stage]);
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk) {
-              // A: K-major rows of 128 B; 16 values of k = 32 B further along the row.
-              const uint64_t adesc = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
-              // B: N-major; 16 rows of k = 16 * 128 B further. LBO = 8 KiB between the
-              // 64-column boxes, SBO = 1 KiB between groups of 8 k-rows.
-              const uint64_t bdesc = smem_desc_sw128(b_addr + kk * 2048, kBBoxBytes, 1024);
+              // A: K-major swizzled rows; 16 values of k = 32 B further along the
+              // row; SBO = one 8-row swizzle atom.
+              const uint64_t adesc =
+                  smem_desc(a_addr + kk * 32, 16, kAAtomBytes, kASwizzleMode);
+              // B: N-major, 128-byte swizzle; 16 rows of k = 16 * 128 B further.
+              // LBO = one 64-column box, SBO = 1 KiB between groups of 8 k-rows.
+              const uint64_t bdesc = smem_desc(b_addr + kk * 2048, kBBoxBytes, 1024, 2u);
               tc_mma_f16(d_tmem, adesc, bdesc, p.idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
             }
             any = true;
@@ -379,17 +398,19 @@ EncodeTiledFn get_encode_fn() {
 }
 
 // Row-major rows x cols matrix of 16-bit elements, row stride ld (elements),
-// boxes of box_rows x 64 elements with 128-byte swizzle.
+// boxes of box_rows x box_cols elements; the swizzle spans one box row
+// (box_cols * 2 bytes: 128 or 64).
 bool make_tmap(CUtensorMap *tm, CUtensorMapDataType dt, const void *base, int64_t rows,
-               int64_t cols, int64_t ld, uint32_t box_rows) {
+               int64_t cols, int64_t ld, uint32_t box_rows, uint32_t box_cols) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(tm, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -400,8 +421,8 @@ cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf1
                       const void *B, int64_t ldb, typename TcArgs<kInt>::Out beta,
                       typename TcArgs<kInt>::Out *C, int64_t ldc, cudaStream_t stream) {
   CUtensorMap tmA, tmB;
-  if (!make_tmap(&tmA, dt, A, M, K, lda, kBM)) return cudaErrorInvalidValue;
-  if (!make_tmap(&tmB, dt, B, K, N, ldb, kBK)) return cudaErrorInvalidValue;
+  if (!make_tmap(&tmA, dt, A, M, K, lda, kBM, kBK)) return cudaErrorInvalidValue;
+  if (!make_tmap(&tmB, dt, B, K, N, ldb, kBK, 64)) return cudaErrorInvalidValue;
   TcArgs<kInt> p;
   p.M = M;
   p.N = N;
@@ -428,36 +449,50 @@ cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf1
 }
 
 // int8 -> fp16, exact (|x| <= 128). dst has row stride ldd (multiple of 8) and
-// its padding columns [cols, ldd) are written with zeros.
+// its padding columns [cols, ldd) are written with zeros. Each thread widens 16
+// consecutive elements of a row: one 16-byte load when the source row is
+// 16-byte aligned and the chunk is inside the matrix, byte loads otherwise,
+// and one or two 16-byte stores.
 __global__ void widen_s8_kernel(const int8_t *__restrict__ src, int64_t lds, __half *dst,
-                                int64_t ldd, int rows, int cols) {
-  const int64_t chunks_per_row = ldd / 8;
+                                int64_t ldd, int rows, int cols, int vec_ok) {
+  const int64_t chunks_per_row = (ldd + 15) / 16;
   const int64_t total = static_cast<int64_t>(rows) * chunks_per_row;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t r = i / chunks_per_row;
-    const int c0 = static_cast<int>((i - r * chunks_per_row) * 8);
+    const int c0 = static_cast<int>((i - r * chunks_per_row) * 16);
     const int8_t *s = src + r * lds;
-    __align__(16) __half h[8];
+    __align__(16) __half h[16];
+    if (vec_ok && c0 + 16 <= cols) {
+      const int4 v = *reinterpret_cast<const int4 *>(s + c0);
+      const int w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int c = c0 + j;
-      h[j] = __int2half_rn(c < cols ? static_cast<int>(s[c]) : 0);
+      for (int j = 0; j < 16; ++j)
+        h[j] = __int2half_rn(static_cast<int8_t>(static_cast<uint32_t>(w[j >> 2]) >> (8 * (j & 3))));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int c = c0 + j;
+        h[j] = __int2half_rn(c < cols ? static_cast<int>(s[c]) : 0);
+      }
     }
-    *reinterpret_cast<uint4 *>(dst + r * ldd + c0) = *reinterpret_cast<const uint4 *>(h);
+    uint4 *d = reinterpret_cast<uint4 *>(dst + r * ldd + c0);
+    d[0] = *reinterpret_cast<const uint4 *>(h);
+    if (c0 + 16 <= ldd) d[1] = *reinterpret_cast<const uint4 *>(h + 8);
   }
 }
 
 cudaError_t widen_s8(const DeviceInfo &dev, const int8_t *src, int64_t lds, __half *dst,
                      int64_t ldd, int rows, int cols, cudaStream_t stream) {
-  const int64_t total = static_cast<int64_t>(rows) * (ldd / 8);
+  const int64_t total = static_cast<int64_t>(rows) * ((ldd + 15) / 16);
   const int threads = 256;
   int64_t blocks = (total + threads - 1) / threads;
-  const int64_t cap = static_cast<int64_t>(dev.sm_count) * 8;
+  const int64_t cap = static_cast<int64_t>(dev.sm_count) * 16;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
+  const int vec_ok = (reinterpret_cast<uintptr_t>(src) % 16 == 0) && (lds % 16 == 0);
   widen_s8_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(src, lds, dst, ldd,
-                                                                        rows, cols);
+                                                                        rows, cols, vec_ok);
   return cudaGetLastError();
 }
 

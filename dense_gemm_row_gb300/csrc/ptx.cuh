@@ -20,6 +20,9 @@ namespace dgr {
 // Legitimate waits in these kernels last microseconds; two seconds is far
 // beyond any of them and still short enough to keep a faulty launch brief.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// Second safety net, should %globaltimer ever stand still: a wait also gives
+// up after this many polls.
+constexpr uint32_t kWaitMaxPolls = 1u << 28;
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
@@ -106,14 +109,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // kWaitLimitNs elapsed, in which case the device error word is set.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int *abort, uint32_t *err_word,
-                                                  uint32_t code) {
+                                                  uint32_t code,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0u) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns || it >= kWaitMaxPolls) {
         *abort = 1;
         record_timeout(err_word, code);
         return false;
@@ -210,17 +214,17 @@ __device__ __forceinline__ void tmem_ld_wait() {
 //   bits 16..29  leading-dimension byte offset >> 4
 //   bits 32..45  stride-dimension byte offset >> 4
 //   bits 46..47  descriptor version (1 on sm_100-family)
-//   bits 49..51  base offset (0: swizzle atoms are 1024-byte aligned)
+//   bits 49..51  base offset (0: swizzle atoms are aligned to their size)
 //   bit  52      leading-offset mode (0: relative)
 //   bits 61..63  swizzle: 0 none, 2 = 128-byte, 4 = 64-byte, 6 = 32-byte
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes,
-                                                    uint32_t sbo_bytes) {
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes,
+                                              uint32_t sbo_bytes, uint32_t swizzle_mode) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
   d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
   d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
   d |= 1ull << 46;
-  d |= 2ull << 61;
+  d |= static_cast<uint64_t>(swizzle_mode & 7u) << 61;
   return d;
 }
 

@@ -169,6 +169,19 @@ GEMM_API const char *gemm_status_string(gemm_status_t status);
  */
 GEMM_API gemm_status_t gemm_check_device_error(uint32_t *word);
 
+/*
+ * Diagnostic of the failure path: enqueues one warp that waits, with the same
+ * bounded mbarrier wait as the GEMM kernels, on a barrier nothing arrives on.
+ * After limit_us microseconds (1 .. 1000000) the wait gives up, records a
+ * timeout (wait code 7) in the device error word and the kernel returns; the
+ * context stays usable and gemm_check_device_error() then reports
+ * GEMM_ERR_TIMEOUT. Nothing faults, traps or hangs. Returns
+ * GEMM_ERR_INVALID_VALUE for a limit outside the range, else the launch status.
+ * Source: none on the pages (their error handling aborts the process); this is
+ * the library's own failure detection.
+ */
+GEMM_API gemm_status_t gemm_selftest_wait_timeout(uint32_t limit_us, cudaStream_t stream);
+
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 GEMM_API int gemm_version(void);
 
