@@ -54,37 +54,59 @@ namespace {
 #ifndef DGR_TC_STAGES
 #define DGR_TC_STAGES 4
 #endif
+#ifndef DGR_TC_STAGES_PAIR
+#define DGR_TC_STAGES_PAIR 6
+#endif
 #ifndef DGR_TC_GROUP_M
 #define DGR_TC_GROUP_M 16
 #endif
+#ifndef DGR_TC_GROUP_M_PAIR
+#define DGR_TC_GROUP_M_PAIR 8
+#endif
+#ifndef DGR_TC_PAIR
+#define DGR_TC_PAIR 1
+#endif
 
-constexpr int kBM = 128;
-constexpr int kBN = 256;
 // k-block: 64 16-bit values (one 128-byte swizzle row of A) or 32 (64-byte rows).
 constexpr int kBK = DGR_TC_BK;
 static_assert(kBK == 64 || kBK == 32, "k-block of 32 or 64 values");
-constexpr int kStages = DGR_TC_STAGES;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr int kGroupM = DGR_TC_GROUP_M;
 // int mode: k-blocks per exact fp32 chunk (1024 values of k)
 constexpr int kChunkKB = 1024 / kBK;
 constexpr uint32_t kTmemCols = 512;  // two 256-column fp32 accumulators
+constexpr int kBN = 256;             // tile columns (MMA N)
+constexpr int kBM = 128;             // tile rows held by one CTA (TMEM lanes)
 
 // A rows are kBK * 2 bytes long: 128-byte swizzle for 64 values, 64-byte for 32.
 constexpr uint32_t kARowBytes = kBK * 2;
 constexpr uint32_t kASwizzleMode = kBK == 64 ? 2u : 4u;   // descriptor encoding
 constexpr uint32_t kAAtomBytes = 8 * kARowBytes;          // 8-row swizzle atom
-constexpr uint32_t kABytes = kBM * kBK * 2;               // 16 or 8 KiB
 constexpr uint32_t kBBoxBytes = 64 * kBK * 2;             // one 64(N) x kBK box
-constexpr uint32_t kBBytes = kBK * kBN * 2;               // 32 or 16 KiB
-constexpr uint32_t kStageBytes = kABytes + kBBytes;
 
+// Single CTA: 128 x 256 tile, the CTA stages all 256 columns of B.
+// CTA pair:   256 x 256 tile, each CTA stages its 128 rows of A and its 128
+//             columns of B; the leader's MMA (M = 256) reads both CTAs.
+template <bool kPair>
+struct Cfg {
+  static constexpr int kTileM = kPair ? 256 : 128;
+  static constexpr int kBNLoad = kPair ? 128 : 256;   // B columns staged per CTA
+  static constexpr int kStages = kPair ? DGR_TC_STAGES_PAIR : DGR_TC_STAGES;
+  // Tiles are visited in groups of kGroupM tile rows so that the CTAs resident
+  // at one time share A rows and B columns in L2.
+  static constexpr int kGroupM = kPair ? DGR_TC_GROUP_M_PAIR : DGR_TC_GROUP_M;
+  static constexpr uint32_t kABytes = kBM * kBK * 2;
+  static constexpr uint32_t kBBytes = kBK * kBNLoad * 2;
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;           // per CTA
+  static constexpr uint32_t kTxBytes = kStageBytes * (kPair ? 2 : 1);  // per full phase
+};
+
+template <bool kPair>
 struct __align__(1024) TcSmem {
-  uint8_t a[kStages][kABytes];
-  uint8_t b[kStages][kBBytes];
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint8_t a[Cfg<kPair>::kStages][Cfg<kPair>::kABytes];
+  uint8_t b[Cfg<kPair>::kStages][Cfg<kPair>::kBBytes];
+  uint64_t full[Cfg<kPair>::kStages];
+  uint64_t empty[Cfg<kPair>::kStages];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t drain;
@@ -105,6 +127,7 @@ struct TcArgs {
   uint32_t *err_word;
 };
 
+template <int kGroupM>
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &tm, int &tn) {
   const int per_group = kGroupM * tiles_n;
   const int g = t / per_group;
@@ -166,18 +189,26 @@ __device__ __forceinline__ void store_row_chunk(const TcArgs<kInt> &p, int row, 
   }
 }
 
-template <bool kInt>
+template <bool kInt, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const TcArgs<kInt> p) {
-  using Out = typename TcArgs<kInt>::Out;
+  using Cf = Cfg<kPair>;
+  constexpr int kStages = Cf::kStages;
   extern __shared__ uint8_t smem_raw[];
-  // Swizzled TMA destinations need 1024-byte alignment.
-  TcSmem &sm = *reinterpret_cast<TcSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~uintptr_t(1023));
+  // Swizzled TMA destinations need 1024-byte alignment. The offset is the same
+  // in both CTAs of a pair, which the pair MMA relies on.
+  TcSmem<kPair> &sm = *reinterpret_cast<TcSmem<kPair> *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   volatile int *abort = &sm.abort;
+
+  uint32_t rank = 0;  // rank within the CTA pair; rank 0 issues the MMAs
+  if constexpr (kPair) rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int unit = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int units = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -186,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sm.tmem_full[i]), 1);
-      mbar_init(smem_u32(&sm.tmem_empty[i]), kEpiWarps);
+      mbar_init(smem_u32(&sm.tmem_empty[i]), kEpiWarps * (kPair ? 2 : 1));
     }
     mbar_init(smem_u32(&sm.drain), 1);
     sm.abort = 0;
@@ -195,11 +226,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(smem_u32(&sm.tmem_base), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before_sync();
-  __syncthreads();
+  if constexpr (kPair) {
+    cluster_sync();  // the leader's barriers exist before the peer signals them
+  } else {
+    __syncthreads();
+  }
   tc_fence_after_sync();
   const uint32_t tmem_base = sm.tmem_base;
 
@@ -211,26 +251,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
-      uint32_t issued = 0;             // stages with a load issued
-      uint32_t issued_parity = 0;      // parity of the last load issued per stage
+      uint32_t issued = 0;         // stages with a load issued
+      uint32_t issued_parity = 0;  // parity of the last load issued per stage
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+      for (int t = unit; ok && t < num_tiles; t += units) {
         int tm, tn;
-        tile_coords(t, p.tiles_m, p.tiles_n, tm, tn);
-        const int m0 = tm * kBM, n0 = tn * kBN;
+        tile_coords<Cf::kGroupM>(t, p.tiles_m, p.tiles_n, tm, tn);
+        const int m0 = tm * Cf::kTileM + static_cast<int>(rank) * kBM;
+        const int nb = tn * kBN + static_cast<int>(rank) * Cf::kBNLoad;
         for (int kb = 0; kb < KB; ++kb) {
-          const uint32_t empty_bar = smem_u32(&sm.empty[stage]);
-          if (!mbar_wait_bounded(empty_bar, phase ^ 1u, abort, p.err_word, kWaitEmpty)) {
+          if (!mbar_wait_bounded(smem_u32(&sm.empty[stage]), phase ^ 1u, abort, p.err_word,
+                                 kWaitEmpty)) {
             ok = false;
             break;
           }
           const uint32_t full_bar = smem_u32(&sm.full[stage]);
-          mbar_arrive_expect_tx(full_bar, kStageBytes);
-          tma_load_2d(smem_u32(sm.a[stage]), &tmA, full_bar, kb * kBK, m0);
+          if (leader) mbar_arrive_expect_tx(full_bar, Cf::kTxBytes);
+          if constexpr (kPair) {
+            const uint32_t full_leader = mapa_shared(full_bar, 0);
+            tma_load_2d_pair(smem_u32(sm.a[stage]), &tmA, full_leader, kb * kBK, m0);
 #pragma unroll
-          for (int j = 0; j < kBN / 64; ++j)
-            tma_load_2d(smem_u32(sm.b[stage] + j * kBBoxBytes), &tmB, full_bar, n0 + 64 * j,
-                        kb * kBK);
+            for (int j = 0; j < Cf::kBNLoad / 64; ++j)
+              tma_load_2d_pair(smem_u32(sm.b[stage] + j * kBBoxBytes), &tmB, full_leader,
+                               nb + 64 * j, kb * kBK);
+          } else {
+            tma_load_2d(smem_u32(sm.a[stage]), &tmA, full_bar, kb * kBK, m0);
+#pragma unroll
+            for (int j = 0; j < Cf::kBNLoad / 64; ++j)
+              tma_load_2d(smem_u32(sm.b[stage] + j * kBBoxBytes), &tmB, full_bar, nb + 64 * j,
+                          kb * kBK);
+          }
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) {
@@ -239,24 +289,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // Never leave with a copy still writing into shared memory.
-      for (int s = 0; s < kStages; ++s)
-        if (issued & (1u << s)) drain_wait(smem_u32(&sm.full[s]), (issued_parity >> s) & 1u, p.err_word);
+      // Never leave with a copy still writing into shared memory. The leader's
+      // full barriers count both CTAs' bytes; the peer CTA is held at the final
+      // cluster barrier until the leader has drained.
+      if (leader)
+        for (int s = 0; s < kStages; ++s)
+          if (issued & (1u << s))
+            drain_wait(smem_u32(&sm.full[s]), (issued_parity >> s) & 1u, p.err_word);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       uint32_t stage = 0, phase = 0, chunk = 0;
       bool ok = true;
       bool any = false;
-      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+      for (int t = unit; ok && t < num_tiles; t += units) {
         for (int kb0 = 0; ok && kb0 < KB; kb0 += chunk_kb) {
           const int kb1 = min(KB, kb0 + chunk_kb);
           const uint32_t buf = chunk & 1u, use = (chunk >> 1) & 1u;
           ++chunk;
-          if (!mbar_wait_bounded(smem_u32(&sm.tmem_empty[buf]), use ^ 1u, abort, p.err_word,
-                                 kWaitTmemEmpty)) {
+          bool got;
+          if constexpr (kPair) {
+            got = mbar_wait_bounded_cluster(smem_u32(&sm.tmem_empty[buf]), use ^ 1u, abort,
+                                            p.err_word, kWaitTmemEmpty);
+          } else {
+            got = mbar_wait_bounded(smem_u32(&sm.tmem_empty[buf]), use ^ 1u, abort, p.err_word,
+                                    kWaitTmemEmpty);
+          }
+          if (!got) {
             ok = false;
             break;
           }
@@ -280,22 +341,40 @@ __global__ void __launch_bounds__(kThreads, 1)
               // B: N-major, 128-byte swizzle; 16 rows of k = 16 * 128 B further.
               // LBO = one 64-column box, SBO = 1 KiB between groups of 8 k-rows.
               const uint64_t bdesc = smem_desc(b_addr + kk * 2048, kBBoxBytes, 1024, 2u);
-              tc_mma_f16(d_tmem, adesc, bdesc, p.idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+              const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
+              if constexpr (kPair) {
+                tc_mma_f16_pair(d_tmem, adesc, bdesc, p.idesc, acc);
+              } else {
+                tc_mma_f16(d_tmem, adesc, bdesc, p.idesc, acc);
+              }
             }
             any = true;
-            tc_commit(smem_u32(&sm.empty[stage]));
+            // This stage's shared memory is free again in both CTAs.
+            if constexpr (kPair) {
+              tc_commit_pair_mc(smem_u32(&sm.empty[stage]), 0x3);
+            } else {
+              tc_commit(smem_u32(&sm.empty[stage]));
+            }
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1u;
             }
           }
           if (!ok) break;
-          tc_commit(smem_u32(&sm.tmem_full[buf]));
+          if constexpr (kPair) {
+            tc_commit_pair_mc(smem_u32(&sm.tmem_full[buf]), 0x3);
+          } else {
+            tc_commit(smem_u32(&sm.tmem_full[buf]));
+          }
         }
       }
       // Never leave with an MMA still reading shared memory or writing TMEM.
       if (any) {
-        tc_commit(smem_u32(&sm.drain));
+        if constexpr (kPair) {
+          tc_commit_pair_mc(smem_u32(&sm.drain), 0x1);
+        } else {
+          tc_commit(smem_u32(&sm.drain));
+        }
         drain_wait(smem_u32(&sm.drain), 0, p.err_word);
       }
     }
@@ -303,15 +382,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int e = warp - 2;
-    const int quarter = warp & 3;          // TMEM lanes this warp may access
-    const int col_half = e >> 2;           // which 128 columns of the tile
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int col_half = e >> 2;   // which 128 columns of the tile
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t chunk = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+    for (int t = unit; ok && t < num_tiles; t += units) {
       int tm, tn;
-      tile_coords(t, p.tiles_m, p.tiles_n, tm, tn);
-      const int row = tm * kBM + quarter * 32 + lane;
+      tile_coords<Cf::kGroupM>(t, p.tiles_m, p.tiles_n, tm, tn);
+      const int row = tm * Cf::kTileM + static_cast<int>(rank) * kBM + quarter * 32 + lane;
       const int col0 = tn * kBN + col_half * 128;
       uint32_t acc[kInt ? 128 : 1];  // int mode: running int32 sums (wrap-around)
       if constexpr (kInt) {
@@ -352,7 +431,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sm.tmem_empty[buf]));
+        if (lane == 0) {
+          if constexpr (kPair) {
+            mbar_arrive_cluster(mapa_shared(smem_u32(&sm.tmem_empty[buf]), 0));
+          } else {
+            mbar_arrive(smem_u32(&sm.tmem_empty[buf]));
+          }
+        }
       }
       if constexpr (kInt) {
         if (ok && row < p.M) {
@@ -369,10 +454,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   tc_fence_before_sync();
-  __syncthreads();
+  if constexpr (kPair) {
+    cluster_sync();  // both CTAs done: no MMA, copy or arrival targets either CTA
+  } else {
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (kPair) {
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    } else {
+      tmem_dealloc(tmem_base, kTmemCols);
+    }
   }
 }
 
@@ -415,6 +508,39 @@ bool make_tmap(CUtensorMap *tm, CUtensorMapDataType dt, const void *base, int64_
   return r == CUDA_SUCCESS;
 }
 
+// Co-resident CTA pairs for a pair kernel on this device (0 if pairs are not
+// available), queried once per device and kernel.
+template <bool kInt>
+int pair_capacity(const DeviceInfo &dev, size_t smem) {
+  static std::mutex mu;
+  static int cache[64];
+  static bool known[64] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev.device < 0 || dev.device >= 64) return 0;
+  if (known[dev.device]) return cache[dev.device];
+  auto kern = gemm_tc_kernel<kInt, true>;
+  int n = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * static_cast<unsigned>(dev.sm_count / 2), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  cache[dev.device] = n;
+  known[dev.device] = true;
+  return n;
+}
+
 template <bool kInt>
 cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf16, int M, int N,
                       int K, typename TcArgs<kInt>::Out alpha, const void *A, int64_t lda,
@@ -431,15 +557,41 @@ cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf1
   p.beta = beta;
   p.C = C;
   p.ldc = ldc;
-  p.tiles_m = (M + kBM - 1) / kBM;
   p.tiles_n = (N + kBN - 1) / kBN;
   p.c_vec_ok = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0);
-  p.idesc = idesc_f16(is_bf16, false, true, kBM, kBN);
   p.err_word = dev.err_word;
+
+  const size_t smem_pair = sizeof(TcSmem<true>) + 1024;
+  const int pairs = DGR_TC_PAIR ? pair_capacity<kInt>(dev, smem_pair) : 0;
+  if (pairs > 0) {
+    p.tiles_m = (M + Cfg<true>::kTileM - 1) / Cfg<true>::kTileM;
+    p.idesc = idesc_f16(is_bf16, false, true, Cfg<true>::kTileM, kBN);
+    const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+    if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const int units = static_cast<int>(tiles < pairs ? tiles : pairs);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * static_cast<unsigned>(units), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem_pair;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<kInt, true>, tmA, tmB, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
+
+  p.tiles_m = (M + kBM - 1) / kBM;
+  p.idesc = idesc_f16(is_bf16, false, true, Cfg<false>::kTileM, kBN);
   const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
-  const size_t smem = sizeof(TcSmem) + 1024;
-  auto kern = gemm_tc_kernel<kInt>;
+  const size_t smem = sizeof(TcSmem<false>) + 1024;
+  auto kern = gemm_tc_kernel<kInt, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
