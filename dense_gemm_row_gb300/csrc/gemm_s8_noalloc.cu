@@ -20,10 +20,13 @@ namespace {
 
 // 64 MiB: enough for the widened operands of M = N = K = 4096.
 constexpr size_t kScratchBytes = size_t(64) << 20;
+// After the operands: 4 KiB of flags for the kernel's split-k tail (zeroed by
+// each call before use).
+constexpr size_t kFlagBytes = 4096;
 
 // The scratch array. Every GPU that loads this module keeps it until the
 // process exits. All calls on a device share it.
-static __device__ __align__(256) unsigned char g_s8_scratch[kScratchBytes];
+static __device__ __align__(256) unsigned char g_s8_scratch[kScratchBytes + kFlagBytes];
 
 constexpr int kMaxDevices = 64;
 
@@ -71,6 +74,9 @@ extern "C" gemm_status_t gemm_s8_noalloc(int64_t M, int64_t N, int64_t K, int32_
     cudaGetLastError();
     return GEMM_ERR_DEVICE;
   }
-  return static_cast<gemm_status_t>(dgr::abi_from_cuda(dgr::launch_gemm_s8_scratch(
-      *dev, int(M), int(N), int(K), alpha, A, lda, B, ldb, beta, C, ldc, scratch, stream)));
+  uint32_t *flags =
+      reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(scratch) + dgr::kScratchBytes);
+  return static_cast<gemm_status_t>(dgr::abi_from_cuda(
+      dgr::launch_gemm_s8_scratch(*dev, int(M), int(N), int(K), alpha, A, lda, B, ldb, beta, C,
+                                  ldc, scratch, flags, dgr::kFlagBytes / 4, stream)));
 }

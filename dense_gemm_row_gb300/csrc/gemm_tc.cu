@@ -101,10 +101,15 @@ struct Cfg {
   static constexpr uint32_t kTxBytes = kStageBytes * (kPair ? 2 : 1);  // per full phase
 };
 
+// Epilogue staging: one 32 x 32 x 4-byte block of C per epilogue warp, in the
+// 128-byte-swizzled layout of the C tensor map's box.
+constexpr uint32_t kStageCBytes = 32 * 128;
+
 template <bool kPair>
 struct __align__(1024) TcSmem {
   uint8_t a[Cfg<kPair>::kStages][Cfg<kPair>::kABytes];
   uint8_t b[Cfg<kPair>::kStages][Cfg<kPair>::kBBytes];
+  uint8_t stage_c[kEpiWarps][kStageCBytes];
   uint64_t full[Cfg<kPair>::kStages];
   uint64_t empty[Cfg<kPair>::kStages];
   uint64_t tmem_full[2];
@@ -123,9 +128,81 @@ struct TcArgs {
   int64_t ldc;
   int tiles_m, tiles_n;
   int c_vec_ok;  // C 16-byte aligned and ldc % 4 == 0
+  int c_tma;     // the epilogue writes C through the C tensor map (needs c_vec_ok)
   uint32_t idesc;
   uint32_t *err_word;
+  // Work split: the first dp_tiles tiles (a multiple of the number of units)
+  // are computed whole, round-robin; each of the remaining tail_tiles tiles
+  // is split along k into `split` parts, one per unit. Part j > 0 adds its
+  // partial product into C after part j - 1 has stored (tail flags, one per
+  // tail tile and CTA of a pair, zero at launch).
+  int dp_tiles, tail_tiles, split;
+  uint32_t *tail_flags;
 };
+
+// One item of a unit's work list: a tile and a range of its k-blocks.
+struct WorkItem {
+  int tile, kb0, kb1, part, parts;
+};
+
+// Item n of unit u's work list (false past its end). kb_unit is the k
+// granularity of split points: 1 k-block, or one exact 1024-k chunk in int
+// mode.
+__device__ __forceinline__ bool get_work(int u, int n, int units, int dp_tiles, int tail_tiles,
+                                         int split, int KB, int kb_unit, WorkItem &w) {
+  const int dp_per_unit = dp_tiles / units;
+  if (n < dp_per_unit) {
+    w.tile = u + n * units;
+    w.kb0 = 0;
+    w.kb1 = KB;
+    w.part = 0;
+    w.parts = 1;
+    return true;
+  }
+  if (n == dp_per_unit && u < tail_tiles * split) {
+    w.tile = dp_tiles + u / split;
+    w.part = u % split;
+    w.parts = split;
+    const int nunits = (KB + kb_unit - 1) / kb_unit;
+    w.kb0 = min(KB, (w.part * nunits / split) * kb_unit);
+    w.kb1 = min(KB, ((w.part + 1) * nunits / split) * kb_unit);
+    return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait until *flag >= value (another unit's part has been stored).
+__device__ __forceinline__ bool wait_flag(const uint32_t *flag, uint32_t value,
+                                          volatile int *abort, uint32_t *err_word) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (ld_acquire_gpu(flag) >= value) return true;
+    __nanosleep(128);  // keep the polling off the L2 the other units are streaming from
+    if ((it & 63u) == 63u) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs || it >= kWaitMaxPolls) {
+        *abort = 1;
+        record_timeout(err_word, kWaitFlag);
+        return false;
+      }
+    }
+  }
+}
+
+// Barrier among the epilogue warps only (named barrier 1).
+__device__ __forceinline__ void epilogue_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+}
 
 template <int kGroupM>
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &tm, int &tn) {
@@ -158,19 +235,21 @@ __device__ __forceinline__ int32_t scale_add(int32_t alpha, int32_t acc, int32_t
   return static_cast<int32_t>(r);
 }
 
+// C[row, col .. col+31] = alpha * v + beta * C (the C term only when use_c).
+// C is read through L2 (another SM may have just written it).
 template <bool kInt>
 __device__ __forceinline__ void store_row_chunk(const TcArgs<kInt> &p, int row, int col,
-                                                const typename TcArgs<kInt>::Out (&v)[32]) {
+                                                const typename TcArgs<kInt>::Out (&v)[32],
+                                                typename TcArgs<kInt>::Out beta, bool use_c) {
   using Out = typename TcArgs<kInt>::Out;
   Out *crow = p.C + static_cast<int64_t>(row) * p.ldc;
-  const Out alpha = p.alpha, beta = p.beta;
-  const bool use_c = beta != Out(0);
+  const Out alpha = p.alpha;
   if (p.c_vec_ok && col + 31 < p.N) {
     using Vec = typename std::conditional<kInt, int4, float4>::type;
 #pragma unroll
     for (int j = 0; j < 32; j += 4) {
       Vec c = {};
-      if (use_c) c = *reinterpret_cast<const Vec *>(crow + col + j);
+      if (use_c) c = __ldcg(reinterpret_cast<const Vec *>(crow + col + j));
       Vec o;
       o.x = scale_add(alpha, v[j], beta, c.x, use_c);
       o.y = scale_add(alpha, v[j + 1], beta, c.y, use_c);
@@ -182,18 +261,45 @@ __device__ __forceinline__ void store_row_chunk(const TcArgs<kInt> &p, int row, 
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       if (col + j < p.N) {
-        const Out c = use_c ? crow[col + j] : Out(0);
+        const Out c = use_c ? __ldcg(crow + col + j) : Out(0);
         crow[col + j] = scale_add(alpha, v[j], beta, c, use_c);
       }
     }
   }
 }
 
+// Writes one 32 x 32 block of C (rows y .. y+31, columns x .. x+31; the lane's
+// row is y + lane) from registers: stages it in the warp's swizzled buffer and
+// issues one TMA store, or one TMA reduce-add when `addto` (C += block).
+// Elements outside C are dropped by the tensor map's bounds.
+__device__ __forceinline__ void tma_write_block(uint32_t stage, const void *tmC, int x, int y,
+                                                int M, int N, const uint32_t (&w)[32],
+                                                bool addto, int lane) {
+  if (lane == 0) bulk_wait_read_all();  // the previous block has left the buffer
+  __syncwarp();
+  const uint32_t row = stage + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    st_shared_v4(row + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), w[4 * j], w[4 * j + 1],
+                 w[4 * j + 2], w[4 * j + 3]);
+  fence_proxy_async_shared();
+  __syncwarp();
+  if (lane == 0 && x < N && y < M) {  // a block wholly outside C issues nothing
+    if (addto) {
+      tma_reduce_add_2d(tmC, x, y, stage);
+    } else {
+      tma_store_2d(tmC, x, y, stage);
+    }
+    bulk_commit();
+  }
+}
+
 template <bool kInt, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const TcArgs<kInt> p) {
+                   const __grid_constant__ CUtensorMap tmC, const TcArgs<kInt> p) {
   using Cf = Cfg<kPair>;
+  using Out = typename TcArgs<kInt>::Out;
   constexpr int kStages = Cf::kStages;
   extern __shared__ uint8_t smem_raw[];
   // Swizzled TMA destinations need 1024-byte alignment. The offset is the same
@@ -224,6 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    if (p.c_tma) prefetch_tmap(&tmC);
   }
   if (warp == 1) {
     if constexpr (kPair) {
@@ -243,9 +350,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = sm.tmem_base;
 
-  const int num_tiles = p.tiles_m * p.tiles_n;
   const int KB = (p.K + kBK - 1) / kBK;
+  // int mode: exact fp32 chunks of 1024 k; float mode: one chunk per item
   const int chunk_kb = kInt ? kChunkKB : KB;
+  const int kb_unit = kInt ? kChunkKB : 1;
+  WorkItem wi;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -254,12 +363,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t issued = 0;         // stages with a load issued
       uint32_t issued_parity = 0;  // parity of the last load issued per stage
       bool ok = true;
-      for (int t = unit; ok && t < num_tiles; t += units) {
+      for (int n = 0; ok && get_work(unit, n, units, p.dp_tiles, p.tail_tiles, p.split, KB,
+                                     kb_unit, wi);
+           ++n) {
         int tm, tn;
-        tile_coords<Cf::kGroupM>(t, p.tiles_m, p.tiles_n, tm, tn);
+        tile_coords<Cf::kGroupM>(wi.tile, p.tiles_m, p.tiles_n, tm, tn);
         const int m0 = tm * Cf::kTileM + static_cast<int>(rank) * kBM;
         const int nb = tn * kBN + static_cast<int>(rank) * Cf::kBNLoad;
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = wi.kb0; kb < wi.kb1; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&sm.empty[stage]), phase ^ 1u, abort, p.err_word,
                                  kWaitEmpty)) {
             ok = false;
@@ -304,9 +415,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0, chunk = 0;
       bool ok = true;
       bool any = false;
-      for (int t = unit; ok && t < num_tiles; t += units) {
-        for (int kb0 = 0; ok && kb0 < KB; kb0 += chunk_kb) {
-          const int kb1 = min(KB, kb0 + chunk_kb);
+      for (int n = 0; ok && get_work(unit, n, units, p.dp_tiles, p.tail_tiles, p.split, KB,
+                                     kb_unit, wi);
+           ++n) {
+        for (int kb0 = wi.kb0; ok && kb0 < wi.kb1; kb0 += chunk_kb) {
+          const int kb1 = min(wi.kb1, kb0 + chunk_kb);
           const uint32_t buf = chunk & 1u, use = (chunk >> 1) & 1u;
           ++chunk;
           bool got;
@@ -381,34 +494,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
+    // Every epilogue warp walks the same work list and meets the same named
+    // barriers, whatever happens to its waits, so none can be left behind.
     const int e = warp - 2;
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int col_half = e >> 2;   // which 128 columns of the tile
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const bool flag_thread = (e == 0 && lane == 0);
     uint32_t chunk = 0;
-    bool ok = true;
-    for (int t = unit; ok && t < num_tiles; t += units) {
+    for (int n = 0;
+         get_work(unit, n, units, p.dp_tiles, p.tail_tiles, p.split, KB, kb_unit, wi); ++n) {
       int tm, tn;
-      tile_coords<Cf::kGroupM>(t, p.tiles_m, p.tiles_n, tm, tn);
+      tile_coords<Cf::kGroupM>(wi.tile, p.tiles_m, p.tiles_n, tm, tn);
       const int row = tm * Cf::kTileM + static_cast<int>(rank) * kBM + quarter * 32 + lane;
       const int col0 = tn * kBN + col_half * 128;
+      // Part 0 (or a whole tile) applies beta to the old C; a later part adds
+      // its partial product to what the previous part stored.
+      const bool addto = wi.part > 0;
+      const Out beta = addto ? Out(1) : p.beta;
+      const bool use_c = addto || p.beta != Out(0);
+      uint32_t *flag = nullptr;
+      if (wi.parts > 1)
+        flag = p.tail_flags + (wi.tile - p.dp_tiles) * 2 + static_cast<int>(rank);
+      if (addto) {
+        if (flag_thread) wait_flag(flag, static_cast<uint32_t>(wi.part), abort, p.err_word);
+        epilogue_sync();
+      }
       uint32_t acc[kInt ? 128 : 1];  // int mode: running int32 sums (wrap-around)
       if constexpr (kInt) {
 #pragma unroll
         for (int j = 0; j < 128; ++j) acc[j] = 0;
       }
-      for (int kb0 = 0; kb0 < KB; kb0 += chunk_kb) {
+      for (int kb0 = wi.kb0; kb0 < wi.kb1; kb0 += chunk_kb) {
         const uint32_t buf = chunk & 1u, use = (chunk >> 1) & 1u;
         ++chunk;
-        int got = 1;
+        int got = 0;
         if (lane == 0)
           got = mbar_wait_bounded(smem_u32(&sm.tmem_full[buf]), use, abort, p.err_word,
                                   kWaitTmemFull);
         got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) {
-          ok = false;
-          break;
-        }
+        if (!got) break;
         tc_fence_after_sync();
         const uint32_t taddr = tmem_base + lane_base + buf * kBN + col_half * 128;
 #pragma unroll
@@ -420,12 +545,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j)
               acc[c + j] += static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[j])));
+          } else if (p.c_tma) {
+            if (!*abort) {
+              uint32_t w[32];
+              const bool read_c = use_c && !addto && row < p.M;
+              const float *crow = p.C + static_cast<int64_t>(row) * p.ldc + col0 + c;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float c0 = (read_c && col0 + c + j < p.N) ? __ldcg(crow + j) : 0.f;
+                w[j] = __float_as_uint(
+                    scale_add(p.alpha, __uint_as_float(r[j]), beta, c0, read_c));
+              }
+              tma_write_block(smem_u32(sm.stage_c[e]), &tmC, col0 + c, row - lane, p.M, p.N, w,
+                              addto, lane);
+            }
           } else {
-            if (row < p.M) {
+            if (row < p.M && !*abort) {
               float v[32];
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-              store_row_chunk<kInt>(p, row, col0 + c, v);
+              store_row_chunk<kInt>(p, row, col0 + c, v, beta, use_c);
             }
           }
         }
@@ -440,17 +579,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if constexpr (kInt) {
-        if (ok && row < p.M) {
+        if (p.c_tma) {
+          if (!*abort) {
+            const bool read_c = use_c && !addto && row < p.M;
+            const int32_t *crow = p.C + static_cast<int64_t>(row) * p.ldc + col0;
+#pragma unroll
+            for (int c = 0; c < 128; c += 32) {
+              uint32_t w[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const int32_t c0 = (read_c && col0 + c + j < p.N) ? __ldcg(crow + c + j) : 0;
+                w[j] = static_cast<uint32_t>(
+                    scale_add(p.alpha, static_cast<int32_t>(acc[c + j]), beta, c0, read_c));
+              }
+              tma_write_block(smem_u32(sm.stage_c[e]), &tmC, col0 + c, row - lane, p.M, p.N, w,
+                              addto, lane);
+            }
+          }
+        } else if (row < p.M && !*abort) {
 #pragma unroll
           for (int c = 0; c < 128; c += 32) {
             int32_t v[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = static_cast<int32_t>(acc[c + j]);
-            store_row_chunk<kInt>(p, row, col0 + c, v);
+            store_row_chunk<kInt>(p, row, col0 + c, v, beta, use_c);
           }
         }
       }
+      if (flag) {
+        // Publish this part: every epilogue warp's stores complete, then the flag.
+        if (p.c_tma && lane == 0) bulk_wait_all();
+        __syncwarp();
+        epilogue_sync();
+        if (flag_thread && !*abort) {
+          __threadfence();
+          st_release_gpu(flag, static_cast<uint32_t>(wi.part + 1));
+        }
+      }
     }
+    // Never leave with a TMA store still reading the staging buffer.
+    if (p.c_tma && lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before_sync();
@@ -508,6 +677,23 @@ bool make_tmap(CUtensorMap *tm, CUtensorMapDataType dt, const void *base, int64_
   return r == CUDA_SUCCESS;
 }
 
+// C (row-major rows x cols, 4-byte elements, row stride ld) in boxes of 32 x 32
+// elements with 128-byte swizzle, for the epilogue's TMA stores and reduces.
+bool make_tmap_c(CUtensorMap *tm, bool is_int, const void *base, int64_t rows, int64_t cols,
+                 int64_t ld) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(tm, is_int ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                   2, const_cast<void *>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Co-resident CTA pairs for a pair kernel on this device (0 if pairs are not
 // available), queried once per device and kernel.
 template <bool kInt>
@@ -541,11 +727,69 @@ int pair_capacity(const DeviceInfo &dev, size_t smem) {
   return n;
 }
 
+// Library-owned stream-ordered memory pool of a device (scratch for the int8
+// path and the split-k tail flags); freed blocks stay mapped for reuse.
+cudaError_t device_pool(const DeviceInfo &dev, cudaMemPool_t *out) {
+  static std::mutex mu;
+  static cudaMemPool_t pools[64] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+  if (!pools[dev.device]) {
+    cudaMemPoolProps props;
+    std::memset(&props, 0, sizeof props);
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev.device;
+    cudaMemPool_t pl;
+    cudaError_t e = cudaMemPoolCreate(&pl, &props);
+    if (e != cudaSuccess) return e;
+    uint64_t keep = ~0ull;  // keep freed memory mapped for the next call
+    cudaMemPoolSetAttribute(pl, cudaMemPoolAttrReleaseThreshold, &keep);
+    pools[dev.device] = pl;
+  }
+  *out = pools[dev.device];
+  return cudaSuccess;
+}
+
+#ifndef DGR_TC_MAX_SPLIT
+#define DGR_TC_MAX_SPLIT 4
+#endif
+constexpr int kMaxSplit = DGR_TC_MAX_SPLIT;  // parts per tail tile (each adds one pass over C)
+
+// Splits T tiles of KB k-blocks over at most `cap` units: whole tiles
+// round-robin, then the leftover tiles split along k (at most max_split
+// parts, in steps of kb_unit k-blocks) so that every unit gets one part (see
+// TcArgs).
+void plan_work(int64_t T, int KB, int kb_unit, int cap, int max_split, int &units, int &dp_tiles,
+               int &tail_tiles, int &split) {
+  const int nunits = (KB + kb_unit - 1) / kb_unit;
+  int U = cap;
+  int64_t W = T / U, R = T - W * U;
+  int S = 1;
+  if (R > 0) {
+    S = static_cast<int>(U / R);
+    if (S > max_split) S = max_split;
+    if (S > nunits) S = nunits;
+    if (S < 1) S = 1;
+  }
+  if (S == 1) {
+    if (T < U) U = static_cast<int>(T);
+    W = T / U;
+    R = T - W * U;
+  }
+  units = U;
+  dp_tiles = static_cast<int>(W * U);
+  tail_tiles = static_cast<int>(R);
+  split = S;
+}
+
 template <bool kInt>
 cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf16, int M, int N,
                       int K, typename TcArgs<kInt>::Out alpha, const void *A, int64_t lda,
                       const void *B, int64_t ldb, typename TcArgs<kInt>::Out beta,
-                      typename TcArgs<kInt>::Out *C, int64_t ldc, cudaStream_t stream) {
+                      typename TcArgs<kInt>::Out *C, int64_t ldc, cudaStream_t stream,
+                      uint32_t *flags_ws, size_t flags_words) {
   CUtensorMap tmA, tmB;
   if (!make_tmap(&tmA, dt, A, M, K, lda, kBM, kBK)) return cudaErrorInvalidValue;
   if (!make_tmap(&tmB, dt, B, K, N, ldb, kBK, 64)) return cudaErrorInvalidValue;
@@ -560,15 +804,58 @@ cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf1
   p.tiles_n = (N + kBN - 1) / kBN;
   p.c_vec_ok = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0);
   p.err_word = dev.err_word;
+  p.tail_flags = nullptr;
+  // TMA stores of C need a 16-byte aligned base and row stride; otherwise the
+  // epilogue writes C with plain guarded stores.
+  CUtensorMap tmC;
+  std::memset(&tmC, 0, sizeof tmC);
+  p.c_tma = p.c_vec_ok && make_tmap_c(&tmC, kInt, C, M, N, ldc);
 
+  static_assert(sizeof(TcSmem<true>) + 1024 <= 232448, "pair kernel shared memory");
+  static_assert(sizeof(TcSmem<false>) + 1024 <= 232448, "single-CTA kernel shared memory");
   const size_t smem_pair = sizeof(TcSmem<true>) + 1024;
   const int pairs = DGR_TC_PAIR ? pair_capacity<kInt>(dev, smem_pair) : 0;
-  if (pairs > 0) {
-    p.tiles_m = (M + Cfg<true>::kTileM - 1) / Cfg<true>::kTileM;
-    p.idesc = idesc_f16(is_bf16, false, true, Cfg<true>::kTileM, kBN);
-    const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
-    if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
-    const int units = static_cast<int>(tiles < pairs ? tiles : pairs);
+  const bool use_pairs = pairs > 0;
+  const int tile_m = use_pairs ? Cfg<true>::kTileM : Cfg<false>::kTileM;
+  p.tiles_m = (M + tile_m - 1) / tile_m;
+  p.idesc = idesc_f16(is_bf16, false, true, tile_m, kBN);
+  const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const int KB = (K + kBK - 1) / kBK;
+  const int cap = use_pairs ? pairs : dev.sm_count;
+  const int kb_unit = kInt ? kChunkKB : 1;
+  int units = 0;
+  plan_work(tiles, KB, kb_unit, cap, kMaxSplit, units, p.dp_tiles, p.tail_tiles, p.split);
+
+  // Tail flags: zeroed per call; from the caller's buffer or the pool.
+  void *pool_flags = nullptr;
+  if (p.split > 1) {
+    const size_t need = static_cast<size_t>(p.tail_tiles) * 2;
+    if (flags_ws != nullptr) {
+      if (flags_words >= need) {
+        p.tail_flags = flags_ws;
+      } else {  // the caller's buffer is too small: whole tiles only
+        plan_work(tiles, KB, kb_unit, cap, 1, units, p.dp_tiles, p.tail_tiles, p.split);
+      }
+    } else {
+      cudaMemPool_t pool;
+      cudaError_t e = device_pool(dev, &pool);
+      if (e != cudaSuccess) return e;
+      e = cudaMallocFromPoolAsync(&pool_flags, need * 4, pool, stream);
+      if (e != cudaSuccess) return e;
+      p.tail_flags = static_cast<uint32_t *>(pool_flags);
+    }
+    if (p.split > 1) {
+      cudaError_t e = cudaMemsetAsync(p.tail_flags, 0, need * 4, stream);
+      if (e != cudaSuccess) {
+        if (pool_flags) cudaFreeAsync(pool_flags, stream);
+        return e;
+      }
+    }
+  }
+
+  cudaError_t e;
+  if (use_pairs) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * static_cast<unsigned>(units), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -581,23 +868,23 @@ cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf1
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<kInt, true>, tmA, tmB, p);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<kInt, true>, tmA, tmB, tmC, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
+  } else {
+    const size_t smem = sizeof(TcSmem<false>) + 1024;
+    auto kern = gemm_tc_kernel<kInt, false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e == cudaSuccess) {
+      kern<<<units, kThreads, smem, stream>>>(tmA, tmB, tmC, p);
+      e = cudaGetLastError();
+    }
   }
-
-  p.tiles_m = (M + kBM - 1) / kBM;
-  p.idesc = idesc_f16(is_bf16, false, true, Cfg<false>::kTileM, kBN);
-  const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
-  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
-  const size_t smem = sizeof(TcSmem<false>) + 1024;
-  auto kern = gemm_tc_kernel<kInt, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  const int grid = static_cast<int>(tiles < dev.sm_count ? tiles : dev.sm_count);
-  kern<<<grid, kThreads, smem, stream>>>(tmA, tmB, p);
-  return cudaGetLastError();
+  if (pool_flags) {
+    cudaError_t f = cudaFreeAsync(pool_flags, stream);
+    if (e == cudaSuccess) e = f;
+  }
+  return e;
 }
 
 // int8 -> fp16, exact (|x| <= 128). dst has row stride ldd (multiple of 8) and
@@ -657,7 +944,7 @@ cudaError_t launch_gemm_tc_f16(const DeviceInfo &dev, bool is_bf16, int M, int N
   const CUtensorMapDataType dt =
       is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   return launch_tc<false>(dev, dt, is_bf16, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
-                          stream);
+                          stream, nullptr, 0);
 }
 
 // The int8 path widens A and B to fp16 in stream-ordered scratch memory from a
@@ -672,27 +959,10 @@ cudaError_t launch_gemm_s8(const DeviceInfo &dev, int M, int N, int K, int32_t a
   const size_t a_off = (a_bytes + 255) / 256 * 256;
   const size_t total = a_off + static_cast<size_t>(K) * ldb16 * 2;
 
-  static std::mutex mu;
-  static cudaMemPool_t pools[64] = {};
   cudaMemPool_t pool = nullptr;
   {
-    std::lock_guard<std::mutex> lock(mu);
-    if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
-    if (!pools[dev.device]) {
-      cudaMemPoolProps props;
-      std::memset(&props, 0, sizeof props);
-      props.allocType = cudaMemAllocationTypePinned;
-      props.handleTypes = cudaMemHandleTypeNone;
-      props.location.type = cudaMemLocationTypeDevice;
-      props.location.id = dev.device;
-      cudaMemPool_t pl;
-      cudaError_t e = cudaMemPoolCreate(&pl, &props);
-      if (e != cudaSuccess) return e;
-      uint64_t keep = ~0ull;  // keep freed scratch mapped for the next call
-      cudaMemPoolSetAttribute(pl, cudaMemPoolAttrReleaseThreshold, &keep);
-      pools[dev.device] = pl;
-    }
-    pool = pools[dev.device];
+    cudaError_t e = device_pool(dev, &pool);
+    if (e != cudaSuccess) return e;
   }
   void *scratch = nullptr;
   cudaError_t e = cudaMallocFromPoolAsync(&scratch, total, pool, stream);
@@ -703,7 +973,7 @@ cudaError_t launch_gemm_s8(const DeviceInfo &dev, int M, int N, int K, int32_t a
   if (e == cudaSuccess) e = widen_s8(dev, B, ldb, b16, ldb16, K, N, stream);
   if (e == cudaSuccess)
     e = launch_tc<true>(dev, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, false, M, N, K, alpha, a16, lda16,
-                        b16, ldb16, beta, C, ldc, stream);
+                        b16, ldb16, beta, C, ldc, stream, nullptr, 0);
   cudaError_t f = cudaFreeAsync(scratch, stream);
   return e != cudaSuccess ? e : f;
 }
@@ -723,7 +993,7 @@ size_t s8_scratch_bytes(int M, int N, int K) {
 cudaError_t launch_gemm_s8_scratch(const DeviceInfo &dev, int M, int N, int K, int32_t alpha,
                                    const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
                                    int32_t beta, int32_t *C, int64_t ldc, void *scratch,
-                                   cudaStream_t stream) {
+                                   uint32_t *flags, size_t flags_words, cudaStream_t stream) {
   const int64_t lda16 = (static_cast<int64_t>(K) + 7) / 8 * 8;
   const int64_t ldb16 = (static_cast<int64_t>(N) + 7) / 8 * 8;
   const size_t a_off = (static_cast<size_t>(M) * lda16 * 2 + 255) / 256 * 256;
@@ -733,7 +1003,7 @@ cudaError_t launch_gemm_s8_scratch(const DeviceInfo &dev, int M, int N, int K, i
   if (e == cudaSuccess) e = widen_s8(dev, B, ldb, b16, ldb16, K, N, stream);
   if (e == cudaSuccess)
     e = launch_tc<true>(dev, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, false, M, N, K, alpha, a16, lda16,
-                        b16, ldb16, beta, C, ldc, stream);
+                        b16, ldb16, beta, C, ldc, stream, flags, flags_words);
   return e;
 }
 

@@ -13,7 +13,7 @@ namespace dgr {
 // code of the first wait that gave up.
 constexpr uint32_t kErrTimeoutBit = 1u;
 constexpr uint32_t kWaitFull = 1, kWaitEmpty = 2, kWaitTmemFull = 3, kWaitTmemEmpty = 4,
-                   kWaitDrain = 5, kWaitTest = 7;
+                   kWaitDrain = 5, kWaitFlag = 6, kWaitTest = 7;
 
 // Per-device facts gathered once by the ABI layer.
 struct DeviceInfo {
@@ -39,12 +39,14 @@ cudaError_t launch_gemm_s8(const DeviceInfo &dev, int M, int N, int K, int32_t a
                            int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream);
 
 // Bytes of scratch the int8 path needs, and the int8 path on caller-provided
-// scratch (256-byte aligned, at least s8_scratch_bytes(M, N, K) bytes).
+// scratch (256-byte aligned, at least s8_scratch_bytes(M, N, K) bytes) and
+// caller-provided split-k tail flags (flags_words 32-bit words, zeroed by the
+// call with cudaMemsetAsync; a buffer too small for the split turns it off).
 size_t s8_scratch_bytes(int M, int N, int K);
 cudaError_t launch_gemm_s8_scratch(const DeviceInfo &dev, int M, int N, int K, int32_t alpha,
                                    const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
                                    int32_t beta, int32_t *C, int64_t ldc, void *scratch,
-                                   cudaStream_t stream);
+                                   uint32_t *flags, size_t flags_words, cudaStream_t stream);
 
 // K == 0: C = beta * C (C = 0 when beta == 0), M x N window only.
 cudaError_t launch_scale_f32(int M, int N, float beta, float *C, int64_t ldc,
