@@ -805,11 +805,14 @@ cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf1
   p.c_vec_ok = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0);
   p.err_word = dev.err_word;
   p.tail_flags = nullptr;
-  // TMA stores of C need a 16-byte aligned base and row stride; otherwise the
-  // epilogue writes C with plain guarded stores.
+  // TMA stores of C need a 16-byte aligned base and row stride, and rows whose
+  // length is a whole number of 16-byte units: a store box is clipped at the
+  // right edge of C only in 16-byte units, so with N % 4 != 0 it would also
+  // write the first columns of the row padding. Otherwise the epilogue writes
+  // C with plain guarded stores.
   CUtensorMap tmC;
   std::memset(&tmC, 0, sizeof tmC);
-  p.c_tma = p.c_vec_ok && make_tmap_c(&tmC, kInt, C, M, N, ldc);
+  p.c_tma = p.c_vec_ok && (N % 4 == 0) && make_tmap_c(&tmC, kInt, C, M, N, ldc);
 
   static_assert(sizeof(TcSmem<true>) + 1024 <= 232448, "pair kernel shared memory");
   static_assert(sizeof(TcSmem<false>) + 1024 <= 232448, "single-CTA kernel shared memory");

@@ -7,7 +7,8 @@ import torch
 
 CANARY_F32 = -12345.678
 CANARY_I32 = -1234567
-GUARD = 257  # elements of canary before and after the C window
+GUARD_ALIGNED = 256    # canary elements before the C window: keeps C 16-byte aligned
+GUARD_UNALIGNED = 257  # ... or moves C off every 16-byte boundary
 
 
 def dev_copy(t: torch.Tensor, poison) -> torch.Tensor:
@@ -24,14 +25,18 @@ class Banded:
     """An M x N output with row stride ldc, embedded in a flat buffer with a band
     of canary values before, after, and in every row's padding."""
 
-    def __init__(self, C0: torch.Tensor, ldc: int | None = None):
+    def __init__(self, C0: torch.Tensor, ldc: int | None = None, aligned: bool = True):
+        """aligned: C starts on a 16-byte boundary (the tensor-core epilogue then
+        writes through TMA when ldc is a multiple of 4); otherwise it starts 4
+        bytes past one, which forces the plain-store epilogue."""
         M, N = C0.shape
         self.M, self.N = M, N
         self.ldc = max(N, 1) if ldc is None else ldc
+        self.guard = GUARD_ALIGNED if aligned else GUARD_UNALIGNED
         self.canary = CANARY_I32 if C0.dtype == torch.int32 else CANARY_F32
-        self.flat = torch.full((GUARD + M * self.ldc + GUARD,), self.canary, dtype=C0.dtype,
-                               device="cuda")
-        self.C = self.flat[GUARD:GUARD + M * self.ldc].view(M, self.ldc)[:, :N]
+        self.flat = torch.full((self.guard + M * self.ldc + GUARD_UNALIGNED,), self.canary,
+                               dtype=C0.dtype, device="cuda")
+        self.C = self.flat[self.guard:self.guard + M * self.ldc].view(M, self.ldc)[:, :N]
         self.C.copy_(C0)
 
     def result(self) -> torch.Tensor:
@@ -40,7 +45,7 @@ class Banded:
     def check_canaries(self):
         flat = self.flat.cpu()
         mask = torch.ones_like(flat, dtype=torch.bool)
-        window = mask[GUARD:GUARD + self.M * self.ldc].view(self.M, self.ldc)
+        window = mask[self.guard:self.guard + self.M * self.ldc].view(self.M, self.ldc)
         window[:, :self.N] = False
         outside = flat[mask]
         if flat.dtype.is_floating_point:

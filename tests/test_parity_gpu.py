@@ -30,10 +30,10 @@ def poison_of(dtype):
     return w.INT8_POISON if dtype == torch.int8 else float("nan")
 
 
-def run_gpu(gemm_mod, p: w.Problem, ldc=None) -> tuple[torch.Tensor, Banded]:
+def run_gpu(gemm_mod, p: w.Problem, ldc=None, aligned=True) -> tuple[torch.Tensor, Banded]:
     A = dev_copy(p.A, poison_of(p.A.dtype))
     B = dev_copy(p.B, poison_of(p.B.dtype))
-    out = Banded(p.C0.contiguous(), ldc)
+    out = Banded(p.C0.contiguous(), ldc, aligned)
     gemm_mod.gemm(A, B, out.C, p.alpha, p.beta)
     torch.cuda.synchronize()
     return out.result(), out
@@ -104,9 +104,12 @@ def ld_for(dtype, cols):
     return None
 
 
+@pytest.mark.parametrize("c_layout", ["c_aligned", "c_unaligned"])
 @pytest.mark.parametrize("dtype", ALL_DTYPES, ids=str)
 @pytest.mark.parametrize("shape", edge_shapes(24, 3), ids=lambda s: "x".join(map(str, s)))
-def test_edge_sweep(gemm_mod, oracle_mod, dtype, shape):
+def test_edge_sweep(gemm_mod, oracle_mod, dtype, shape, c_layout):
+    """Aligned C: 16-byte aligned base and ldc % 4 == 0 (tensor-core epilogue
+    through TMA stores / reduce-adds). Unaligned C: plain guarded stores."""
     M, N, K = shape
     if dtype == torch.int8:
         p = w.problem(M, N, K, dtype, "int8", 100 + M + 7 * N + 13 * K, alpha=3, beta=-2,
@@ -114,13 +117,16 @@ def test_edge_sweep(gemm_mod, oracle_mod, dtype, shape):
     else:
         p = w.problem(M, N, K, dtype, "uniform_pm1", 100 + M + 7 * N + 13 * K, alpha=1.5,
                       beta=-0.5, c_dist="uniform_pm1", lda=ld_for(dtype, K), ldb=ld_for(dtype, N))
-    got, out = run_gpu(gemm_mod, p, ldc=N + 3)
+    aligned = c_layout == "c_aligned"
+    ldc = (N + 4) // 4 * 4 + 4 if aligned else N + 3
+    got, out = run_gpu(gemm_mod, p, ldc=ldc, aligned=aligned)
     assert_parity(got, oracle_of(oracle_mod, p), exact=(dtype == torch.int8))
     out.check_canaries()
 
 
+@pytest.mark.parametrize("c_layout", ["c_aligned", "c_unaligned"])
 @pytest.mark.parametrize("dtype", ALL_DTYPES, ids=str)
-def test_many_tiles_ragged_tail(gemm_mod, oracle_mod, dtype):
+def test_many_tiles_ragged_tail(gemm_mod, oracle_mod, dtype, c_layout):
     """Several tiles in each direction plus a ragged tail in M, N and K."""
     M, N, K = 397, 611, 1111
     if dtype == torch.int8:
@@ -129,7 +135,8 @@ def test_many_tiles_ragged_tail(gemm_mod, oracle_mod, dtype):
     else:
         p = w.problem(M, N, K, dtype, "normal", 41, alpha=0.5, beta=2.0, c_dist="normal",
                       lda=1120, ldb=616)
-    got, out = run_gpu(gemm_mod, p, ldc=650)
+    aligned = c_layout == "c_aligned"
+    got, out = run_gpu(gemm_mod, p, ldc=652 if aligned else 651, aligned=aligned)
     assert_parity(got, oracle_of(oracle_mod, p), exact=(dtype == torch.int8))
     out.check_canaries()
 
@@ -187,7 +194,7 @@ def test_alpha_zero_and_k_zero(gemm_mod, oracle_mod, dtype):
             # float64 oracle bit for bit.
             p = w.problem(M, N, K, dtype, "normal", 71, alpha=float(alpha), beta=-2.0,
                           c_dist="normal", lda=ld_for(dtype, max(K, 1)), ldb=ld_for(dtype, N))
-        got, out = run_gpu(gemm_mod, p, ldc=N + 5)
+        got, out = run_gpu(gemm_mod, p, ldc=N + 3)
         ref = oracle_of(oracle_mod, p)
         # alpha*acc + beta*C with alpha = 0 or an empty sum is exactly beta*C.
         assert_parity(got, ref, exact=True)
@@ -238,3 +245,28 @@ def test_streams_are_respected(gemm_mod, oracle_mod):
         gemm_mod.gemm_bf16(512, 512, 512, 1.0, A, 512, B, 512, 0.0, C, 512, s)
     s.synchronize()
     assert rel_frobenius(C.cpu().numpy(), oracle_of(oracle_mod, p)) <= TOL
+
+
+# ------------------------------------------------------ work split across SMs
+
+@pytest.mark.parametrize("dtype", ALL_DTYPES, ids=str)
+@pytest.mark.parametrize("shape", [(4096, 4096, 1024), (2304, 6400, 2048), (300, 4100, 3072),
+                                   (16, 8192, 4096), (520, 130, 9000)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_split_tail_shapes(gemm_mod, oracle_mod, dtype, shape):
+    """Shapes whose tile count leaves a partial last wave (so leftover tiles are
+    split along k between SMs, later parts adding into C), with beta != 0 so
+    that part 0's beta*C and the later parts' additions both matter. Checked on
+    sampled rows, in both C layouts."""
+    M, N, K = shape
+    for aligned in (True, False):
+        if dtype == torch.int8:
+            p = w.problem(M, N, K, dtype, "int8", 131 + M, alpha=-3, beta=7, c_dist="int")
+        else:
+            p = w.problem(M, N, K, dtype, "normal", 131 + M, alpha=0.75, beta=-1.25,
+                          c_dist="normal", lda=ld_for(dtype, K), ldb=ld_for(dtype, N))
+        ldc = (N + 3) // 4 * 4 if aligned else N + 1
+        got, out = run_gpu(gemm_mod, p, ldc=ldc, aligned=aligned)
+        rows = sample_rows(M, 24, seed=M)
+        assert_parity(got[rows], oracle_of(oracle_mod, p, rows), exact=(dtype == torch.int8))
+        out.check_canaries()
