@@ -333,6 +333,22 @@ def run_reference(args, world, rank):
     return 0
 
 
+def aggregate_ranks(torch, dist, ms, flops_per_step, steps, device):
+    """Whole-job throughput over the ranks: every rank ran `steps` steps of
+    `flops_per_step` in `ms` milliseconds of its own; the job's time is the
+    slowest rank's. Returns (max ms over ranks, TFLOP/s of all ranks together).
+    Without a process group this is the single-GPU figure."""
+    world = 1
+    ms_max = float(ms)
+    if dist is not None:
+        world = dist.get_world_size()
+        t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    value = world * flops_per_step * steps / (ms_max / 1e3) / 1e12
+    return ms_max, value
+
+
 # ------------------------------------------------------------ other workloads
 
 def measure_extra(binding, torch, w, name, peaks, sm_count, stream, gpu_id):
@@ -463,14 +479,9 @@ def main():
     clocks = sampler.summary(t0, t1)
     binding.check_device_error()
 
-    ms_max = ms
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
-    step_ms = ms_max / args.steps
     flops = flops_of(M, N, K)
-    value = world * flops * args.steps / (ms_max / 1e3) / 1e12
+    ms_max, value = aggregate_ranks(torch, dist, ms, flops, args.steps, "cuda")
+    step_ms = ms_max / args.steps
 
     if rank != 0:
         if dist is not None:
