@@ -4,8 +4,10 @@
 // and dispatch to the kernels. Nothing here allocates or frees user memory,
 // prints, or aborts.
 #include <cstdint>
+#include <map>
 #include <mutex>
 #include <type_traits>
+#include <utility>
 
 #include <cuda_runtime.h>
 
@@ -113,6 +115,18 @@ cudaError_t launch_scale(int M, int N, T beta, T *C, int64_t ldc, cudaStream_t s
 }
 
 }  // namespace
+
+cudaError_t set_max_dynamic_smem(const void *kernel, int bytes, int device) {
+  static std::mutex mu;
+  static std::map<std::pair<const void *, int>, int> done;  // -> bytes already set
+  std::lock_guard<std::mutex> lock(mu);
+  auto key = std::make_pair(kernel, device);
+  auto it = done.find(key);
+  if (it != done.end() && it->second >= bytes) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[key] = bytes;
+  return e;
+}
 
 int abi_check_args(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
                    int64_t ldb, const void *C, int64_t ldc, bool *nothing_to_do) {

@@ -727,6 +727,8 @@ int pair_capacity(const DeviceInfo &dev, size_t smem) {
   return n;
 }
 
+}  // namespace
+
 // Library-owned stream-ordered memory pool of a device (scratch for the int8
 // path and the split-k tail flags); freed blocks stay mapped for reuse.
 cudaError_t device_pool(const DeviceInfo &dev, cudaMemPool_t *out) {
@@ -751,6 +753,8 @@ cudaError_t device_pool(const DeviceInfo &dev, cudaMemPool_t *out) {
   *out = pools[dev.device];
   return cudaSuccess;
 }
+
+namespace {
 
 #ifndef DGR_TC_MAX_SPLIT
 #define DGR_TC_MAX_SPLIT 4
@@ -790,6 +794,17 @@ cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf1
                       const void *B, int64_t ldb, typename TcArgs<kInt>::Out beta,
                       typename TcArgs<kInt>::Out *C, int64_t ldc, cudaStream_t stream,
                       uint32_t *flags_ws, size_t flags_words) {
+  // Short, wide problems: the transposed-role kernel streams B at HBM speed
+  // instead of multiplying a mostly-zero 256-row tile.
+  if (M <= kSkinnyMaxM) {
+    if constexpr (kInt) {
+      return launch_tc_skinny_int(dev, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream,
+                                  flags_ws, flags_words);
+    } else {
+      return launch_tc_skinny_float(dev, is_bf16, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                                    stream);
+    }
+  }
   CUtensorMap tmA, tmB;
   if (!make_tmap(&tmA, dt, A, M, K, lda, kBM, kBK)) return cudaErrorInvalidValue;
   if (!make_tmap(&tmB, dt, B, K, N, ldb, kBK, 64)) return cudaErrorInvalidValue;
@@ -876,8 +891,8 @@ cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf1
   } else {
     const size_t smem = sizeof(TcSmem<false>) + 1024;
     auto kern = gemm_tc_kernel<kInt, false>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
+    e = set_max_dynamic_smem(reinterpret_cast<const void *>(kern), static_cast<int>(smem),
+                             dev.device);
     if (e == cudaSuccess) {
       kern<<<units, kThreads, smem, stream>>>(tmA, tmB, tmC, p);
       e = cudaGetLastError();

@@ -48,6 +48,30 @@ cudaError_t launch_gemm_s8_scratch(const DeviceInfo &dev, int M, int N, int K, i
                                    int32_t beta, int32_t *C, int64_t ldc, void *scratch,
                                    uint32_t *flags, size_t flags_words, cudaStream_t stream);
 
+// Short, wide problems (M <= kSkinnyMaxM) on the tensor cores, computed as
+// C^T = B^T A^T so that N fills the MMA rows (gemm_tc_skinny.cu). 16-bit inputs
+// with the same layout rule as launch_gemm_tc_f16; the int version takes the
+// fp16-widened operands of the int8 path and optional caller-provided flags.
+// Measured on GB300 (N = K = 8192): faster than the 256-row CTA-pair tiles up to
+// M = 32 (M = 1: 34 vs 50 us), slower at M = 64.
+constexpr int kSkinnyMaxM = 32;
+cudaError_t launch_tc_skinny_float(const DeviceInfo &dev, bool is_bf16, int M, int N, int K,
+                                   float alpha, const void *A, int64_t lda, const void *B,
+                                   int64_t ldb, float beta, float *C, int64_t ldc,
+                                   cudaStream_t stream);
+cudaError_t launch_tc_skinny_int(const DeviceInfo &dev, int M, int N, int K, int32_t alpha,
+                                 const void *A16, int64_t lda, const void *B16, int64_t ldb,
+                                 int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream,
+                                 uint32_t *flags, size_t flags_words);
+
+// Raises a kernel's dynamic shared-memory limit on the current device, once
+// per (kernel, device); later calls only look the pair up.
+cudaError_t set_max_dynamic_smem(const void *kernel, int bytes, int device);
+
+// The library's stream-ordered memory pool on a device (created on first use;
+// freed blocks stay mapped for reuse).
+cudaError_t device_pool(const DeviceInfo &dev, cudaMemPool_t *out);
+
 // K == 0: C = beta * C (C = 0 when beta == 0), M x N window only.
 cudaError_t launch_scale_f32(int M, int N, float beta, float *C, int64_t ldc,
                              cudaStream_t stream);

@@ -246,12 +246,11 @@ __global__ void __launch_bounds__(kThreads, 2) sgemm_simt_kernel(const SimtArgs 
 }
 
 template <int BK, int STAGES, bool VEC_B>
-cudaError_t launch_variant(const SimtArgs &a, cudaStream_t stream) {
+cudaError_t launch_variant(const SimtArgs &a, int device, cudaStream_t stream) {
   constexpr size_t smem = sizeof(SimtSmem<BK, STAGES>);
   auto kern = sgemm_simt_kernel<BK, STAGES, VEC_B>;
-  // Idempotent; cheap after the first call on a device.
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void *>(kern),
+                                       static_cast<int>(smem), device);
   if (e != cudaSuccess) return e;
   const int64_t blocks = static_cast<int64_t>(a.tiles_m) * a.tiles_n;
   kern<<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(a);
@@ -263,7 +262,6 @@ cudaError_t launch_variant(const SimtArgs &a, cudaStream_t stream) {
 cudaError_t launch_sgemm_simt(const DeviceInfo &dev, int M, int N, int K, float alpha,
                               const float *A, int64_t lda, const float *B, int64_t ldb,
                               float beta, float *C, int64_t ldc, cudaStream_t stream) {
-  (void)dev;
   SimtArgs a;
   a.M = M;
   a.N = N;
@@ -288,8 +286,8 @@ cudaError_t launch_sgemm_simt(const DeviceInfo &dev, int M, int N, int K, float 
 #define DGR_SIMT_STAGES 2
 #endif
   constexpr int kBK = DGR_SIMT_BK, kStages = DGR_SIMT_STAGES;
-  return vec_b ? launch_variant<kBK, kStages, true>(a, stream)
-               : launch_variant<kBK, kStages, false>(a, stream);
+  return vec_b ? launch_variant<kBK, kStages, true>(a, dev.device, stream)
+               : launch_variant<kBK, kStages, false>(a, dev.device, stream);
 }
 
 }  // namespace dgr

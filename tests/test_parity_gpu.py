@@ -270,3 +270,24 @@ def test_split_tail_shapes(gemm_mod, oracle_mod, dtype, shape):
         rows = sample_rows(M, 24, seed=M)
         assert_parity(got[rows], oracle_of(oracle_mod, p, rows), exact=(dtype == torch.int8))
         out.check_canaries()
+
+
+# ---------------------------------------------------------- short, wide shapes
+
+@pytest.mark.parametrize("dtype", ALL_DTYPES, ids=str)
+@pytest.mark.parametrize("M", [1, 5, 16, 17, 32, 33])
+def test_skinny_shapes(gemm_mod, oracle_mod, dtype, M):
+    """Few rows of A (the transposed-role kernel for M <= 32, the tiled kernel
+    above), a ragged N and a K that is split across SMs, with beta != 0; every
+    output checked."""
+    N, K = 2056, 3000
+    for aligned in (True, False):
+        if dtype == torch.int8:
+            p = w.problem(M, N, K, dtype, "int8", 211 + M, alpha=5, beta=-3, c_dist="int")
+        else:
+            p = w.problem(M, N, K, dtype, "normal", 211 + M, alpha=-0.5, beta=1.5,
+                          c_dist="normal", lda=ld_for(dtype, K), ldb=ld_for(dtype, N))
+        ldc = N if aligned else N + 1
+        got, out = run_gpu(gemm_mod, p, ldc=ldc, aligned=aligned)
+        assert_parity(got, oracle_of(oracle_mod, p), exact=(dtype == torch.int8))
+        out.check_canaries()
