@@ -165,6 +165,9 @@ gemm_status_t gemm_f32(int64_t M, int64_t N, int64_t K, float alpha, const float
   const DeviceInfo *dev = nullptr;
   if ((st = current_device(&dev)) != GEMM_OK) return st;
   if (K == 0) return from_cuda(dgr::launch_scale_f32(int(M), int(N), beta, C, ldc, stream));
+  if (dgr::small_m_supported(int(M), A, lda, B, ldb, 4))  // few rows: stream B once
+    return from_cuda(dgr::launch_small_m_f32(*dev, int(M), int(N), int(K), alpha, A, lda, B, ldb,
+                                             beta, C, ldc, stream));
   return from_cuda(dgr::launch_sgemm_simt(*dev, int(M), int(N), int(K), alpha, A, lda, B, ldb,
                                           beta, C, ldc, stream));
 }
@@ -209,6 +212,9 @@ gemm_status_t gemm_s8(int64_t M, int64_t N, int64_t K, int32_t alpha, const int8
   const DeviceInfo *dev = nullptr;
   if ((st = current_device(&dev)) != GEMM_OK) return st;
   if (K == 0) return from_cuda(dgr::launch_scale_s32(int(M), int(N), beta, C, ldc, stream));
+  if (dgr::small_m_supported(int(M), A, lda, B, ldb, 1))  // few rows: int8 B read once, dp4a
+    return from_cuda(dgr::launch_small_m_s8(*dev, int(M), int(N), int(K), alpha, A, lda, B, ldb,
+                                            beta, C, ldc, stream));
   return from_cuda(dgr::launch_gemm_s8(*dev, int(M), int(N), int(K), alpha, A, lda, B, ldb, beta,
                                        C, ldc, stream));
 }

@@ -68,6 +68,19 @@ cudaError_t launch_tc_skinny_int(const DeviceInfo &dev, int M, int N, int K, int
 // per (kernel, device); later calls only look the pair up.
 cudaError_t set_max_dynamic_smem(const void *kernel, int bytes, int device);
 
+// fp32 and int8 GEMM for M <= 32 (gemm_small_m.cu): streams B once with TMA,
+// 4 columns x all rows per thread (packed fp32 FMA / dp4a). Usable when
+// small_m_supported(): A and B 16-byte aligned with row strides that are whole
+// multiples of 16 bytes (esize = element size in bytes).
+bool small_m_supported(int M, const void *A, int64_t lda, const void *B, int64_t ldb,
+                       int esize);
+cudaError_t launch_small_m_f32(const DeviceInfo &dev, int M, int N, int K, float alpha,
+                               const float *A, int64_t lda, const float *B, int64_t ldb,
+                               float beta, float *C, int64_t ldc, cudaStream_t stream);
+cudaError_t launch_small_m_s8(const DeviceInfo &dev, int M, int N, int K, int32_t alpha,
+                              const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
+                              int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream);
+
 // The library's stream-ordered memory pool on a device (created on first use;
 // freed blocks stay mapped for reuse).
 cudaError_t device_pool(const DeviceInfo &dev, cudaMemPool_t *out);

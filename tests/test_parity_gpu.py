@@ -277,11 +277,13 @@ def test_split_tail_shapes(gemm_mod, oracle_mod, dtype, shape):
 @pytest.mark.parametrize("dtype", ALL_DTYPES, ids=str)
 @pytest.mark.parametrize("M", [1, 5, 16, 17, 32, 33])
 def test_skinny_shapes(gemm_mod, oracle_mod, dtype, M):
-    """Few rows of A (the transposed-role kernel for M <= 32, the tiled kernel
-    above), a ragged N and a K that is split across SMs, with beta != 0; every
-    output checked."""
-    N, K = 2056, 3000
-    for aligned in (True, False):
+    """Few rows of A (for M <= 32: the transposed-role tensor-core kernel, and
+    for fp32 / int8 the small-M kernel when A and B rows are 16-byte multiples;
+    the tiled kernels above), a ragged N and a K that is split across SMs, with
+    beta != 0; every output checked. K = 3008 keeps int8 rows 16-byte multiples,
+    K = 3000 does not (fallback paths)."""
+    N = 2056
+    for aligned, K in ((True, 3008), (False, 3000), (True, 3000)):
         if dtype == torch.int8:
             p = w.problem(M, N, K, dtype, "int8", 211 + M, alpha=5, beta=-3, c_dist="int")
         else:
