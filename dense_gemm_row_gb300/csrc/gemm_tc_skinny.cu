@@ -15,9 +15,11 @@
 //     time: full 128-byte segments.
 // Every CTA computes one slice of work: a 128-column block of C over one part
 // of the k range. When there are fewer column blocks than SMs, k is split into
-// `split` parts; part 0 stores alpha*p0 + beta*C and part j, after waiting for
-// part j-1's flag, adds alpha*p_j, in order, so the result is deterministic
-// (and exact in the int8 mode, whose split points fall on 1024-k chunks).
+// `split` parts: every part stores its partial sums in a workspace and counts
+// itself done on its column block; the part that finishes last adds the
+// partials in part order and writes alpha * sum + beta * C. The result is
+// deterministic (and exact in the int8 mode, whose split points fall on
+// 1024-k chunks), and no part waits for another.
 //
 // Sources: as gemm_tc.cu (C = alpha*A*B + beta*C, "Sgemm [128,128,8]"; half /
 // bfloat16 x half / bfloat16 -> float and signed char -> int, C++ warp matrix
@@ -72,8 +74,10 @@ struct SkArgs {
   Out alpha, beta;
   Out *C;
   int64_t ldc;
-  int split;         // parts of k per column block
-  uint32_t *flags;   // one per column block when split > 1, zero at launch
+  int split;           // parts of k per column block
+  uint32_t *counters;  // parts done, one per column block (split > 1), zero at launch
+  Out *ws;             // partial sums [split][M][ws_ld] (split > 1)
+  int64_t ws_ld;       // column blocks * 128
   uint32_t idesc;
   uint32_t *err_word;
 };
@@ -92,33 +96,6 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
         "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
       : "memory");
-}
-
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ bool wait_flag(const uint32_t *flag, uint32_t value,
-                                          volatile int *abort, uint32_t *err_word) {
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 0;; ++it) {
-    if (ld_acquire_gpu(flag) >= value) return true;
-    __nanosleep(128);
-    if ((it & 63u) == 63u) {
-      if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs || it >= kWaitMaxPolls) {
-        *abort = 1;
-        record_timeout(err_word, kWaitFlag);
-        return false;
-      }
-    }
-  }
 }
 
 __device__ __forceinline__ void epilogue_sync() {
@@ -262,9 +239,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int n = n0 + quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const bool flag_thread = (warp == 2 && lane == 0);
-    const bool addto = part > 0;
-    uint32_t *flag = p.split > 1 ? p.flags + blk : nullptr;
     uint32_t acc[kInt ? kMaxM : 1];
     if constexpr (kInt) {
 #pragma unroll
@@ -282,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       got = __shfl_sync(0xffffffffu, got, 0);
       if (!got) break;
       tc_fence_after_sync();
-      const uint32_t taddr = tmem_base + lane_base + buf * kBufCols;
+      const uint32_t taddr = tmem_base + lane_base + buf * 64;
 #pragma unroll
       for (int c = 0; c < kMaxM; c += 16) {
         if (c < p.mp) {
@@ -303,33 +277,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm.tmem_empty[buf]));
     }
-    if (addto) {
-      if (flag_thread) wait_flag(flag, static_cast<uint32_t>(part), abort, p.err_word);
-      epilogue_sync();
-    }
-    if (n < p.N && !*abort && kb1 > kb0) {
-      const Out beta = addto ? Out(1) : p.beta;
-      const bool use_c = addto || p.beta != Out(0);
-#pragma unroll
-      for (int m = 0; m < kMaxM; ++m) {
-        if (m < p.M) {
-          Out *cp = p.C + static_cast<int64_t>(m) * p.ldc + n;
-          const Out c = use_c ? __ldcg(cp) : Out(0);
-          Out v;
-          if constexpr (kInt) {
-            v = static_cast<int32_t>(acc[m]);
-          } else {
-            v = facc[m];
-          }
-          *cp = axpby(p.alpha, v, beta, c, use_c);
-        }
+    auto value = [&](int m) -> Out {
+      if constexpr (kInt) {
+        return static_cast<int32_t>(acc[m]);
+      } else {
+        return facc[m];
       }
-    }
-    if (flag) {
+    };
+    const bool use_c = p.beta != Out(0);
+    if (p.split == 1) {
+      if (n < p.N && !*abort && kb1 > kb0) {
+#pragma unroll
+        for (int m = 0; m < kMaxM; ++m)
+          if (m < p.M) {
+            Out *cp = p.C + static_cast<int64_t>(m) * p.ldc + n;
+            *cp = axpby(p.alpha, value(m), p.beta, use_c ? *cp : Out(0), use_c);
+          }
+      }
+    } else {
+      // Store this part's partial sums, count the part done; the last part of
+      // the column block adds all parts in order.
+#pragma unroll
+      for (int m = 0; m < kMaxM; ++m)
+        if (m < p.M) p.ws[(static_cast<int64_t>(part) * p.M + m) * p.ws_ld + n] = value(m);
+      __threadfence();
       epilogue_sync();
-      if (flag_thread && !*abort) {
+      __shared__ int last;
+      if (warp == 2 && lane == 0)
+        last = (atomicAdd(p.counters + blk, 1u) == static_cast<uint32_t>(p.split - 1));
+      epilogue_sync();
+      if (last) {
         __threadfence();
-        st_release_gpu(flag, static_cast<uint32_t>(part + 1));
+        if (n < p.N) {
+#pragma unroll 1
+          for (int m = 0; m < p.M; ++m) {
+            Out sum = Out(0);
+            for (int q = 0; q < p.split; ++q) {
+              const Out v = __ldcg(p.ws + (static_cast<int64_t>(q) * p.M + m) * p.ws_ld + n);
+              if constexpr (kInt) {
+                sum = static_cast<int32_t>(static_cast<uint32_t>(sum) + static_cast<uint32_t>(v));
+              } else {
+                sum += v;
+              }
+            }
+            Out *cp = p.C + static_cast<int64_t>(m) * p.ldc + n;
+            *cp = axpby(p.alpha, sum, p.beta, use_c ? *cp : Out(0), use_c);
+          }
+        }
       }
     }
   }
@@ -394,7 +388,6 @@ cudaError_t launch(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf16, 
   p.ldc = ldc;
   p.idesc = idesc_f16(is_bf16, /*a_mn_major=*/true, /*b_mn_major=*/false, kBN, p.mp);
   p.err_word = dev.err_word;
-  p.flags = nullptr;
   CUtensorMap tmA, tmB;
   if (!tmap16(&tmA, dt, A, M, K, lda, static_cast<uint32_t>(p.mp))) return cudaErrorInvalidValue;
   if (!tmap16(&tmB, dt, B, K, N, ldb, kBK)) return cudaErrorInvalidValue;
@@ -409,27 +402,30 @@ cudaError_t launch(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf16, 
   if (split > nunits) split = nunits;
   if (split < 1) split = 1;
 
-  void *pool_flags = nullptr;
+  // split > 1 needs a workspace for the partial sums (from the pool); a caller
+  // that provides its own memory gets whole column blocks instead.
+  if (flags_ws != nullptr) split = 1;
+  (void)flags_words;
+  void *pool_ws = nullptr;
+  p.counters = nullptr;
+  p.ws = nullptr;
+  p.ws_ld = static_cast<int64_t>(blocks) * kBN;
   if (split > 1) {
-    const size_t need = static_cast<size_t>(blocks);
-    if (flags_ws != nullptr && flags_words >= need) {
-      p.flags = flags_ws;
-    } else if (flags_ws != nullptr) {
-      split = 1;
-    } else {
-      cudaMemPool_t pool;
-      cudaError_t e = device_pool(dev, &pool);
-      if (e != cudaSuccess) return e;
-      e = cudaMallocFromPoolAsync(&pool_flags, need * 4, pool, stream);
-      if (e != cudaSuccess) return e;
-      p.flags = static_cast<uint32_t *>(pool_flags);
-    }
-    if (split > 1) {
-      cudaError_t e = cudaMemsetAsync(p.flags, 0, need * 4, stream);
-      if (e != cudaSuccess) {
-        if (pool_flags) cudaFreeAsync(pool_flags, stream);
-        return e;
-      }
+    cudaMemPool_t pool;
+    cudaError_t e = device_pool(dev, &pool);
+    if (e != cudaSuccess) return e;
+    const size_t ws_bytes =
+        static_cast<size_t>(split) * M * p.ws_ld * sizeof(typename SkArgs<kInt>::Out);
+    const size_t cnt_off = (ws_bytes + 255) / 256 * 256;
+    e = cudaMallocFromPoolAsync(&pool_ws, cnt_off + static_cast<size_t>(blocks) * 4, pool,
+                                stream);
+    if (e != cudaSuccess) return e;
+    p.ws = static_cast<typename SkArgs<kInt>::Out *>(pool_ws);
+    p.counters = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(pool_ws) + cnt_off);
+    e = cudaMemsetAsync(p.counters, 0, static_cast<size_t>(blocks) * 4, stream);
+    if (e != cudaSuccess) {
+      cudaFreeAsync(pool_ws, stream);
+      return e;
     }
   }
   p.split = split;
@@ -443,8 +439,8 @@ cudaError_t launch(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf16, 
     kern<<<static_cast<unsigned>(blocks * split), kThreads, smem, stream>>>(tmA, tmB, p);
     e = cudaGetLastError();
   }
-  if (pool_flags) {
-    cudaError_t f = cudaFreeAsync(pool_flags, stream);
+  if (pool_ws) {
+    cudaError_t f = cudaFreeAsync(pool_ws, stream);
     if (e == cudaSuccess) e = f;
   }
   return e;
