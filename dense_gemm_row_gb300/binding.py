@@ -14,6 +14,13 @@ Two layers:
 * ``gemm(A, B, C, alpha, beta)`` takes 2-D CUDA tensors with unit column stride
   (row stride = leading dimension), picks the entry point from A's dtype and
   runs on torch's current stream.
+
+The extended entry points (strided-batched GEMM with transposed operands) have
+the same two layers: ``gemm_f32_ex / gemm_bf16_ex / gemm_f16_ex / gemm_s8_ex(
+opA, opB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc,
+strideC, batch, stream=None)`` (opX: OP_N or OP_T) and ``gemm_batched(A, B, C,
+alpha, beta, trans_a=False, trans_b=False)`` for 3-D tensors (a 2-D operand,
+or one expanded along the batch with stride 0, is shared by every entry).
 """
 from __future__ import annotations
 
@@ -34,9 +41,11 @@ STATUS = {
 }
 
 # Every function include/dense_gemm_row.h declares.
-EXPORTED = ("gemm_f32", "gemm_bf16", "gemm_f16", "gemm_s8", "gemm_s8_noalloc",
-            "gemm_status_string", "gemm_check_device_error", "gemm_selftest_wait_timeout",
-            "gemm_version")
+EXPORTED = ("gemm_f32", "gemm_bf16", "gemm_f16", "gemm_s8", "gemm_f32_ex", "gemm_bf16_ex",
+            "gemm_f16_ex", "gemm_s8_ex", "gemm_s8_noalloc", "gemm_status_string",
+            "gemm_check_device_error", "gemm_selftest_wait_timeout", "gemm_version")
+
+OP_N, OP_T = 0, 1  # gemm_op_t
 
 
 class GemmError(RuntimeError):
@@ -60,6 +69,13 @@ def _load():
     for name in ("gemm_s8", "gemm_s8_noalloc"):
         fn = getattr(lib, name)
         fn.argtypes = [i64, i64, i64, i32, vp, i64, vp, i64, i32, vp, i64, vp]
+        fn.restype = ctypes.c_int
+    op = ctypes.c_int
+    for name, sc in (("gemm_f32_ex", f32), ("gemm_bf16_ex", f32), ("gemm_f16_ex", f32),
+                     ("gemm_s8_ex", i32)):
+        fn = getattr(lib, name)
+        fn.argtypes = [op, op, i64, i64, i64, sc, vp, i64, i64, vp, i64, i64, sc, vp, i64, i64,
+                       i64, vp]
         fn.restype = ctypes.c_int
     lib.gemm_status_string.argtypes = [ctypes.c_int]
     lib.gemm_status_string.restype = ctypes.c_char_p
@@ -125,6 +141,24 @@ def gemm_s8_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
                                _addr(C), ldc, _stream(stream)), "gemm_s8_noalloc")
 
 
+def _ex(name, cast):
+    def call(opA, opB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc, strideC,
+             batch, stream=None):
+        _check(getattr(lib, name)(int(opA), int(opB), M, N, K, cast(alpha), _addr(A), lda,
+                                  strideA, _addr(B), ldb, strideB, cast(beta), _addr(C), ldc,
+                                  strideC, batch, _stream(stream)), name)
+    call.__name__ = name
+    call.__doc__ = (f"{name}: strided-batched C_b = alpha*op(A_b)*op(B_b) + beta*C_b "
+                    "(include/dense_gemm_row.h).")
+    return call
+
+
+gemm_f32_ex = _ex("gemm_f32_ex", float)
+gemm_bf16_ex = _ex("gemm_bf16_ex", float)
+gemm_f16_ex = _ex("gemm_f16_ex", float)
+gemm_s8_ex = _ex("gemm_s8_ex", int)
+
+
 def check_device_error() -> int:
     """Reads and clears the device error word; raises GemmError(GEMM_ERR_TIMEOUT)
     if a kernel gave up a bounded wait. Returns the raw word otherwise (0)."""
@@ -162,4 +196,55 @@ def gemm(A, B, C, alpha=1.0, beta=0.0, stream=None):
     if C.dtype != c_dtype:
         raise TypeError(f"gemm: C must be {c_dtype} for {A.dtype} inputs")
     fn(M, N, K, alpha, A, _ld(A, "A"), B, _ld(B, "B"), beta, C, _ld(C, "C"), stream)
+    return C
+
+
+def _mat(t, name):
+    """(matrix stride, row stride) of a 2-D or 3-D operand with unit column
+    stride; a 2-D operand is one matrix shared by every batch entry."""
+    if t.dim() not in (2, 3):
+        raise ValueError(f"{name} must be 2-D or 3-D")
+    rows, cols = t.shape[-2], t.shape[-1]
+    if rows > 0 and cols > 1 and t.stride(-1) != 1:
+        raise ValueError(f"{name} needs unit column stride (row-major)")
+    ld = max(int(t.stride(-2)), int(cols), 1)
+    mstride = int(t.stride(0)) if t.dim() == 3 and t.shape[0] > 1 else 0
+    return mstride, ld
+
+
+def gemm_batched(A, B, C, alpha=1.0, beta=0.0, trans_a=False, trans_b=False, stream=None):
+    """C[b] = alpha * op(A[b]) * op(B[b]) + beta * C[b] for CUDA tensors.
+
+    C is (batch, M, N). A is (batch, M, K), or (batch, K, M) with trans_a; B is
+    (batch, K, N), or (batch, N, K) with trans_b. A 2-D A or B (or one expanded
+    along the batch, stride 0) is shared by every entry. Rows must have unit
+    column stride; row and matrix strides are passed through. dtypes as gemm()."""
+    import torch
+    if C.dim() != 3:
+        raise ValueError("gemm_batched: C must be 3-D (batch, M, N)")
+    batch, M, N = C.shape
+    K = A.shape[-2] if trans_a else A.shape[-1]
+    a_rows = A.shape[-1] if trans_a else A.shape[-2]
+    b_k = B.shape[-1] if trans_b else B.shape[-2]
+    b_n = B.shape[-2] if trans_b else B.shape[-1]
+    if a_rows != M or b_k != K or b_n != N:
+        raise ValueError("gemm_batched: shapes do not chain")
+    for t, name in ((A, "A"), (B, "B")):
+        if t.dim() == 3 and t.shape[0] not in (1, batch):
+            raise ValueError(f"gemm_batched: {name} has {t.shape[0]} matrices, C {batch}")
+    if A.dtype != B.dtype:
+        raise TypeError("gemm_batched: A and B must share a dtype")
+    fns = {torch.float32: (gemm_f32_ex, torch.float32),
+           torch.bfloat16: (gemm_bf16_ex, torch.float32),
+           torch.float16: (gemm_f16_ex, torch.float32), torch.int8: (gemm_s8_ex, torch.int32)}
+    if A.dtype not in fns:
+        raise TypeError(f"gemm_batched: unsupported dtype {A.dtype}")
+    fn, c_dtype = fns[A.dtype]
+    if C.dtype != c_dtype:
+        raise TypeError(f"gemm_batched: C must be {c_dtype} for {A.dtype} inputs")
+    sa, lda = _mat(A, "A")
+    sb, ldb = _mat(B, "B")
+    sc, ldc = _mat(C, "C")
+    fn(OP_T if trans_a else OP_N, OP_T if trans_b else OP_N, M, N, K, alpha, A, lda, sa, B, ldb,
+       sb, beta, C, ldc, sc, batch, stream)
     return C

@@ -89,12 +89,15 @@ gemm_status_t from_cuda(cudaError_t e) {
 // ------------------------------------------------------------ K == 0 kernels
 
 template <typename T>
-__global__ void scale_kernel(int M, int N, T beta, T *C, int64_t ldc) {
-  const int64_t total = static_cast<int64_t>(M) * N;
+__global__ void scale_kernel(int M, int N, T beta, T *C, int64_t ldc, int batch,
+                             int64_t stride) {
+  const int64_t per = static_cast<int64_t>(M) * N;
+  const int64_t total = per * batch;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t r = i / N, c = i - r * N;
-    T *p = C + r * ldc + c;
+    const int64_t b = i / per, j = i - b * per;
+    const int64_t r = j / N, c = j - r * N;
+    T *p = C + b * stride + r * ldc + c;
     if (beta == T(0)) {
       *p = T(0);
     } else if constexpr (std::is_integral<T>::value) {  // int32 wrap-around
@@ -106,12 +109,48 @@ __global__ void scale_kernel(int M, int N, T beta, T *C, int64_t ldc) {
 }
 
 template <typename T>
-cudaError_t launch_scale(int M, int N, T beta, T *C, int64_t ldc, cudaStream_t stream) {
-  const int64_t total = static_cast<int64_t>(M) * N;
+cudaError_t launch_scale(int M, int N, T beta, T *C, int64_t ldc, cudaStream_t stream,
+                         int batch = 1, int64_t stride = 0) {
+  const int64_t total = static_cast<int64_t>(M) * N * batch;
   int64_t blocks = (total + 255) / 256;
   if (blocks > 4096) blocks = 4096;
-  scale_kernel<T><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(M, N, beta, C, ldc);
+  scale_kernel<T><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(M, N, beta, C, ldc, batch,
+                                                                     stride);
   return cudaGetLastError();
+}
+
+// Argument checks of the extended entry points: operand forms, sizes, the
+// stored operands' row strides, batch count and strides. Returns GEMM_OK when
+// the call should proceed; sets *nothing_to_do when there is no output.
+gemm_status_t check_ex(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N, int64_t K,
+                       const void *A, int64_t lda, int64_t strideA, const void *B, int64_t ldb,
+                       int64_t strideB, const void *C, int64_t ldc, int64_t strideC,
+                       int64_t batch, bool *nothing_to_do) {
+  *nothing_to_do = false;
+  if ((opA != GEMM_OP_N && opA != GEMM_OP_T) || (opB != GEMM_OP_N && opB != GEMM_OP_T))
+    return GEMM_ERR_INVALID_VALUE;
+  if (batch < 0 || batch > kMaxDim) return GEMM_ERR_INVALID_VALUE;
+  if (strideA < 0 || strideB < 0 || strideC < 0) return GEMM_ERR_INVALID_VALUE;
+  // Stored row lengths: A's rows hold K (op N) or M (op T) values, B's N or K.
+  const int64_t a_row = opA == GEMM_OP_N ? K : M;
+  const int64_t b_row = opB == GEMM_OP_N ? N : K;
+  if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_VALUE;
+  if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_INVALID_VALUE;
+  if (batch == 0 || M == 0 || N == 0) {
+    *nothing_to_do = true;
+    return GEMM_OK;
+  }
+  if (ldc < N || C == nullptr) return GEMM_ERR_INVALID_VALUE;
+  if (K > 0) {
+    if (lda < a_row || A == nullptr) return GEMM_ERR_INVALID_VALUE;
+    if (ldb < b_row || B == nullptr) return GEMM_ERR_INVALID_VALUE;
+  }
+  if (batch > 1) {
+    // The C matrices must not overlap: strideC >= (M - 1) * ldc + N.
+    if (M > 1 && ldc > (INT64_MAX - N) / (M - 1)) return GEMM_ERR_INVALID_VALUE;
+    if (strideC < (M - 1) * ldc + N) return GEMM_ERR_INVALID_VALUE;
+  }
+  return GEMM_OK;
 }
 
 }  // namespace
@@ -126,6 +165,15 @@ cudaError_t set_max_dynamic_smem(const void *kernel, int bytes, int device) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess) done[key] = bytes;
   return e;
+}
+
+cudaError_t launch_scale_batched_f32(int M, int N, float beta, float *C, int64_t ldc, int batch,
+                                     int64_t stride, cudaStream_t stream) {
+  return launch_scale<float>(M, N, beta, C, ldc, stream, batch, stride);
+}
+cudaError_t launch_scale_batched_s32(int M, int N, int32_t beta, int32_t *C, int64_t ldc,
+                                     int batch, int64_t stride, cudaStream_t stream) {
+  return launch_scale<int32_t>(M, N, beta, C, ldc, stream, batch, stride);
 }
 
 int abi_check_args(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
@@ -149,7 +197,9 @@ cudaError_t launch_scale_s32(int M, int N, int32_t beta, int32_t *C, int64_t ldc
 
 }  // namespace dgr
 
+using dgr::BatchOps;
 using dgr::check_args;
+using dgr::check_ex;
 using dgr::current_device;
 using dgr::DeviceInfo;
 using dgr::from_cuda;
@@ -217,6 +267,101 @@ gemm_status_t gemm_s8(int64_t M, int64_t N, int64_t K, int32_t alpha, const int8
                                             beta, C, ldc, stream));
   return from_cuda(dgr::launch_gemm_s8(*dev, int(M), int(N), int(K), alpha, A, lda, B, ldb, beta,
                                        C, ldc, stream));
+}
+
+static BatchOps make_ops(gemm_op_t opA, gemm_op_t opB, int64_t strideA, int64_t strideB,
+                         int64_t strideC, int64_t batch) {
+  BatchOps ops;
+  ops.a_t = opA == GEMM_OP_T;
+  ops.b_t = opB == GEMM_OP_T;
+  ops.batch = static_cast<int>(batch);
+  ops.stride_a = strideA;
+  ops.stride_b = strideB;
+  ops.stride_c = strideC;
+  return ops;
+}
+
+gemm_status_t gemm_f32_ex(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N, int64_t K,
+                          float alpha, const float *A, int64_t lda, int64_t strideA,
+                          const float *B, int64_t ldb, int64_t strideB, float beta, float *C,
+                          int64_t ldc, int64_t strideC, int64_t batch, cudaStream_t stream) {
+  bool skip = false;
+  gemm_status_t st = check_ex(opA, opB, M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc,
+                              strideC, batch, &skip);
+  if (st != GEMM_OK || skip) return st;
+  const BatchOps ops = make_ops(opA, opB, strideA, strideB, strideC, batch);
+  if (ops.plain()) return gemm_f32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+  const DeviceInfo *dev = nullptr;
+  if ((st = current_device(&dev)) != GEMM_OK) return st;
+  if (K == 0)
+    return from_cuda(dgr::launch_scale_batched_f32(int(M), int(N), beta, C, ldc, ops.batch,
+                                                   strideC, stream));
+  return from_cuda(dgr::launch_sgemm_simt_ex(*dev, ops, int(M), int(N), int(K), alpha, A, lda, B,
+                                             ldb, beta, C, ldc, stream));
+}
+
+static gemm_status_t gemm_half_ex(bool is_bf16, gemm_op_t opA, gemm_op_t opB, int64_t M,
+                                  int64_t N, int64_t K, float alpha, const uint16_t *A,
+                                  int64_t lda, int64_t strideA, const uint16_t *B, int64_t ldb,
+                                  int64_t strideB, float beta, float *C, int64_t ldc,
+                                  int64_t strideC, int64_t batch, cudaStream_t stream) {
+  bool skip = false;
+  gemm_status_t st = check_ex(opA, opB, M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc,
+                              strideC, batch, &skip);
+  if (st != GEMM_OK || skip) return st;
+  const BatchOps ops = make_ops(opA, opB, strideA, strideB, strideC, batch);
+  if (ops.plain()) return gemm_half(is_bf16, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+  if (K > 0) {
+    // TMA: 16-byte aligned bases, row strides and matrix strides.
+    if ((reinterpret_cast<uintptr_t>(A) & 15u) || (reinterpret_cast<uintptr_t>(B) & 15u) ||
+        (lda % 8) || (ldb % 8))
+      return GEMM_ERR_UNSUPPORTED_LAYOUT;
+    if (batch > 1 && ((strideA % 8) || (strideB % 8))) return GEMM_ERR_UNSUPPORTED_LAYOUT;
+  }
+  const DeviceInfo *dev = nullptr;
+  if ((st = current_device(&dev)) != GEMM_OK) return st;
+  if (K == 0)
+    return from_cuda(dgr::launch_scale_batched_f32(int(M), int(N), beta, C, ldc, ops.batch,
+                                                   strideC, stream));
+  return from_cuda(dgr::launch_gemm_tc_f16_ex(*dev, is_bf16, ops, int(M), int(N), int(K), alpha,
+                                              A, lda, B, ldb, beta, C, ldc, stream));
+}
+
+gemm_status_t gemm_bf16_ex(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N, int64_t K,
+                           float alpha, const gemm_bf16_t *A, int64_t lda, int64_t strideA,
+                           const gemm_bf16_t *B, int64_t ldb, int64_t strideB, float beta,
+                           float *C, int64_t ldc, int64_t strideC, int64_t batch,
+                           cudaStream_t stream) {
+  return gemm_half_ex(true, opA, opB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C,
+                      ldc, strideC, batch, stream);
+}
+
+gemm_status_t gemm_f16_ex(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N, int64_t K,
+                          float alpha, const gemm_f16_t *A, int64_t lda, int64_t strideA,
+                          const gemm_f16_t *B, int64_t ldb, int64_t strideB, float beta,
+                          float *C, int64_t ldc, int64_t strideC, int64_t batch,
+                          cudaStream_t stream) {
+  return gemm_half_ex(false, opA, opB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C,
+                      ldc, strideC, batch, stream);
+}
+
+gemm_status_t gemm_s8_ex(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N, int64_t K,
+                         int32_t alpha, const int8_t *A, int64_t lda, int64_t strideA,
+                         const int8_t *B, int64_t ldb, int64_t strideB, int32_t beta, int32_t *C,
+                         int64_t ldc, int64_t strideC, int64_t batch, cudaStream_t stream) {
+  bool skip = false;
+  gemm_status_t st = check_ex(opA, opB, M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc,
+                              strideC, batch, &skip);
+  if (st != GEMM_OK || skip) return st;
+  const BatchOps ops = make_ops(opA, opB, strideA, strideB, strideC, batch);
+  if (ops.plain()) return gemm_s8(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+  const DeviceInfo *dev = nullptr;
+  if ((st = current_device(&dev)) != GEMM_OK) return st;
+  if (K == 0)
+    return from_cuda(dgr::launch_scale_batched_s32(int(M), int(N), beta, C, ldc, ops.batch,
+                                                   strideC, stream));
+  return from_cuda(dgr::launch_gemm_s8_ex(*dev, ops, int(M), int(N), int(K), alpha, A, lda, B,
+                                          ldb, beta, C, ldc, stream));
 }
 
 const char *gemm_status_string(gemm_status_t status) {

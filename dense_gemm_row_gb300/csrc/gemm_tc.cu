@@ -1,7 +1,15 @@
 // gemm_tc.cu -- tensor-core GEMM for sm_103a: tcgen05.mma with the
 // accumulator in tensor memory (TMEM), operands staged by TMA.
 //
-//     C = alpha * A * B + beta * C       A: M x K, B: K x N, C: M x N, row-major
+//     C = alpha * op(A) * op(B) + beta * C      op(A): M x K, op(B): K x N,
+//                                                C: M x N, all row-major
+//
+// op(X) is X as stored or its transpose, and the problem may be a stack of
+// `batch` such GEMMs at fixed element strides (strided-batched GEMM). Neither
+// costs anything on this path: a transposed operand is staged by TMA in the
+// other major order and the MMA's descriptors say so; the batch index is the
+// third coordinate of every tensor map and one more dimension of the tile
+// list.
 //
 // 16-bit inputs (bf16 or fp16), fp32 accumulation, and either
 //   * fp32 output (gemm_bf16 / gemm_f16), or
@@ -22,7 +30,10 @@
 //   warp 0      one thread issues TMA loads of A (128 x 64, K-major, 128-byte
 //               swizzle) and B (64 x 256 as four 64 x 64 boxes, N-major,
 //               128-byte swizzle) into a kStages-deep ring guarded by
-//               full/empty mbarriers.
+//               full/empty mbarriers. A stored transposed (K x M) arrives as
+//               two 64(M) x 64(K) M-major boxes; B stored transposed (N x K)
+//               as one 256(N) x 64(K) K-major box. Every layout fills the same
+//               bytes per stage.
 //   warp 1      allocates 512 TMEM columns; one thread issues
 //               tcgen05.mma.cta_group::1.kind::f16 (M=128, N=256, K=16) into
 //               one of two 256-column accumulators and commits each stage's
@@ -82,7 +93,7 @@ constexpr int kBM = 128;             // tile rows held by one CTA (TMEM lanes)
 constexpr uint32_t kARowBytes = kBK * 2;
 constexpr uint32_t kASwizzleMode = kBK == 64 ? 2u : 4u;   // descriptor encoding
 constexpr uint32_t kAAtomBytes = 8 * kARowBytes;          // 8-row swizzle atom
-constexpr uint32_t kBBoxBytes = 64 * kBK * 2;             // one 64(N) x kBK box
+constexpr uint32_t kMNBoxBytes = 64 * kBK * 2;            // any 64(M or N) x kBK MN-major box
 
 // Single CTA: 128 x 256 tile, the CTA stages all 256 columns of B.
 // CTA pair:   256 x 256 tile, each CTA stages its 128 rows of A and its 128
@@ -127,6 +138,9 @@ struct TcArgs {
   Out *C;
   int64_t ldc;
   int tiles_m, tiles_n;
+  int tiles_per_batch;   // tiles_m * tiles_n; tile t is tile t % this of matrix t / this
+  int a_batched, b_batched;  // the operand's tensor map has one matrix per batch entry
+  int64_t stride_c;      // elements between consecutive C matrices
   int c_vec_ok;  // C 16-byte aligned and ldc % 4 == 0
   int c_tma;     // the epilogue writes C through the C tensor map (needs c_vec_ok)
   uint32_t idesc;
@@ -215,6 +229,16 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
   tn = r / rows;
 }
 
+// Tile t of a batched problem: batch entry bt, tile (tm, tn) within it. The
+// tiles of one matrix are contiguous in t, so the resident CTAs work on one or
+// two matrices at a time and the grouped raster's L2 reuse holds within each.
+template <int kGroupM, bool kInt>
+__device__ __forceinline__ void batch_tile_coords(int t, const TcArgs<kInt> &p, int &bt, int &tm,
+                                                  int &tn) {
+  bt = t / p.tiles_per_batch;
+  tile_coords<kGroupM>(t - bt * p.tiles_per_batch, p.tiles_m, p.tiles_n, tm, tn);
+}
+
 // Waits without looking at the abort flag (used to drain in-flight work).
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint32_t *err_word) {
   volatile int never = 0;
@@ -238,11 +262,12 @@ __device__ __forceinline__ int32_t scale_add(int32_t alpha, int32_t acc, int32_t
 // C[row, col .. col+31] = alpha * v + beta * C (the C term only when use_c).
 // C is read through L2 (another SM may have just written it).
 template <bool kInt>
-__device__ __forceinline__ void store_row_chunk(const TcArgs<kInt> &p, int row, int col,
+__device__ __forceinline__ void store_row_chunk(const TcArgs<kInt> &p,
+                                                typename TcArgs<kInt>::Out *C, int row, int col,
                                                 const typename TcArgs<kInt>::Out (&v)[32],
                                                 typename TcArgs<kInt>::Out beta, bool use_c) {
   using Out = typename TcArgs<kInt>::Out;
-  Out *crow = p.C + static_cast<int64_t>(row) * p.ldc;
+  Out *crow = C + static_cast<int64_t>(row) * p.ldc;
   const Out alpha = p.alpha;
   if (p.c_vec_ok && col + 31 < p.N) {
     using Vec = typename std::conditional<kInt, int4, float4>::type;
@@ -268,12 +293,12 @@ __device__ __forceinline__ void store_row_chunk(const TcArgs<kInt> &p, int row, 
   }
 }
 
-// Writes one 32 x 32 block of C (rows y .. y+31, columns x .. x+31; the lane's
-// row is y + lane) from registers: stages it in the warp's swizzled buffer and
-// issues one TMA store, or one TMA reduce-add when `addto` (C += block).
-// Elements outside C are dropped by the tensor map's bounds.
+// Writes one 32 x 32 block of C matrix z (rows y .. y+31, columns x .. x+31;
+// the lane's row is y + lane) from registers: stages it in the warp's swizzled
+// buffer and issues one TMA store, or one TMA reduce-add when `addto`
+// (C += block). Elements outside C are dropped by the tensor map's bounds.
 __device__ __forceinline__ void tma_write_block(uint32_t stage, const void *tmC, int x, int y,
-                                                int M, int N, const uint32_t (&w)[32],
+                                                int z, int M, int N, const uint32_t (&w)[32],
                                                 bool addto, int lane) {
   if (lane == 0) bulk_wait_read_all();  // the previous block has left the buffer
   __syncwarp();
@@ -286,15 +311,16 @@ __device__ __forceinline__ void tma_write_block(uint32_t stage, const void *tmC,
   __syncwarp();
   if (lane == 0 && x < N && y < M) {  // a block wholly outside C issues nothing
     if (addto) {
-      tma_reduce_add_2d(tmC, x, y, stage);
+      tma_reduce_add_3d(tmC, x, y, z, stage);
     } else {
-      tma_store_2d(tmC, x, y, stage);
+      tma_store_3d(tmC, x, y, z, stage);
     }
     bulk_commit();
   }
 }
 
-template <bool kInt, bool kPair>
+// kAT / kBT: A stored K x M / B stored N x K (used transposed).
+template <bool kInt, bool kPair, bool kAT, bool kBT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcArgs<kInt> p) {
@@ -366,10 +392,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int n = 0; ok && get_work(unit, n, units, p.dp_tiles, p.tail_tiles, p.split, KB,
                                      kb_unit, wi);
            ++n) {
-        int tm, tn;
-        tile_coords<Cf::kGroupM>(wi.tile, p.tiles_m, p.tiles_n, tm, tn);
+        int bt, tm, tn;
+        batch_tile_coords<Cf::kGroupM>(wi.tile, p, bt, tm, tn);
         const int m0 = tm * Cf::kTileM + static_cast<int>(rank) * kBM;
         const int nb = tn * kBN + static_cast<int>(rank) * Cf::kBNLoad;
+        const int za = p.a_batched ? bt : 0, zb = p.b_batched ? bt : 0;
         for (int kb = wi.kb0; kb < wi.kb1; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&sm.empty[stage]), phase ^ 1u, abort, p.err_word,
                                  kWaitEmpty)) {
@@ -378,19 +405,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t full_bar = smem_u32(&sm.full[stage]);
           if (leader) mbar_arrive_expect_tx(full_bar, Cf::kTxBytes);
-          if constexpr (kPair) {
-            const uint32_t full_leader = mapa_shared(full_bar, 0);
-            tma_load_2d_pair(smem_u32(sm.a[stage]), &tmA, full_leader, kb * kBK, m0);
-#pragma unroll
-            for (int j = 0; j < Cf::kBNLoad / 64; ++j)
-              tma_load_2d_pair(smem_u32(sm.b[stage] + j * kBBoxBytes), &tmB, full_leader,
-                               nb + 64 * j, kb * kBK);
+          // A pair's loads signal the leader's barrier; a single CTA's its own.
+          const uint32_t bar = kPair ? mapa_shared(full_bar, 0) : full_bar;
+          auto load = [&](uint32_t dst, const CUtensorMap *tm, int x, int y, int z) {
+            if constexpr (kPair) {
+              tma_load_3d_pair(dst, tm, bar, x, y, z);
+            } else {
+              tma_load_3d(dst, tm, bar, x, y, z);
+            }
+          };
+          const int k0 = kb * kBK;
+          if constexpr (!kAT) {
+            load(smem_u32(sm.a[stage]), &tmA, k0, m0, za);  // 128 rows x kBK, K-major
           } else {
-            tma_load_2d(smem_u32(sm.a[stage]), &tmA, full_bar, kb * kBK, m0);
 #pragma unroll
-            for (int j = 0; j < Cf::kBNLoad / 64; ++j)
-              tma_load_2d(smem_u32(sm.b[stage] + j * kBBoxBytes), &tmB, full_bar, nb + 64 * j,
-                          kb * kBK);
+            for (int j = 0; j < kBM / 64; ++j)  // kBK rows of k x 64 values of m, twice
+              load(smem_u32(sm.a[stage] + j * kMNBoxBytes), &tmA, m0 + 64 * j, k0, za);
+          }
+          if constexpr (!kBT) {
+#pragma unroll
+            for (int j = 0; j < Cf::kBNLoad / 64; ++j)  // kBK rows of k x 64 values of n
+              load(smem_u32(sm.b[stage] + j * kMNBoxBytes), &tmB, nb + 64 * j, k0, zb);
+          } else {
+            load(smem_u32(sm.b[stage]), &tmB, k0, nb, zb);  // kBNLoad rows x kBK, K-major
           }
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -447,13 +484,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t b_addr = smem_u32(sm.b[stage]);
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk) {
-              // A: K-major swizzled rows; 16 values of k = 32 B further along the
-              // row; SBO = one 8-row swizzle atom.
+              // K-major operand: swizzled rows of kBK values; 16 values of k =
+              // 32 B further along the row; SBO = one 8-row swizzle atom.
+              // MN-major operand: 128-byte swizzled rows of 64 values of m or n,
+              // one row per k; 16 values of k = 16 * 128 B further; LBO = one
+              // 64-value box, SBO = 1 KiB between groups of 8 k-rows.
               const uint64_t adesc =
-                  smem_desc(a_addr + kk * 32, 16, kAAtomBytes, kASwizzleMode);
-              // B: N-major, 128-byte swizzle; 16 rows of k = 16 * 128 B further.
-              // LBO = one 64-column box, SBO = 1 KiB between groups of 8 k-rows.
-              const uint64_t bdesc = smem_desc(b_addr + kk * 2048, kBBoxBytes, 1024, 2u);
+                  kAT ? smem_desc(a_addr + kk * 2048, kMNBoxBytes, 1024, 2u)
+                      : smem_desc(a_addr + kk * 32, 16, kAAtomBytes, kASwizzleMode);
+              const uint64_t bdesc =
+                  kBT ? smem_desc(b_addr + kk * 32, 16, kAAtomBytes, kASwizzleMode)
+                      : smem_desc(b_addr + kk * 2048, kMNBoxBytes, 1024, 2u);
               const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
               if constexpr (kPair) {
                 tc_mma_f16_pair(d_tmem, adesc, bdesc, p.idesc, acc);
@@ -504,8 +545,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t chunk = 0;
     for (int n = 0;
          get_work(unit, n, units, p.dp_tiles, p.tail_tiles, p.split, KB, kb_unit, wi); ++n) {
-      int tm, tn;
-      tile_coords<Cf::kGroupM>(wi.tile, p.tiles_m, p.tiles_n, tm, tn);
+      int bt, tm, tn;
+      batch_tile_coords<Cf::kGroupM>(wi.tile, p, bt, tm, tn);
+      Out *const Cb = p.C + static_cast<int64_t>(bt) * p.stride_c;
       const int row = tm * Cf::kTileM + static_cast<int>(rank) * kBM + quarter * 32 + lane;
       const int col0 = tn * kBN + col_half * 128;
       // Part 0 (or a whole tile) applies beta to the old C; a later part adds
@@ -549,22 +591,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!*abort) {
               uint32_t w[32];
               const bool read_c = use_c && !addto && row < p.M;
-              const float *crow = p.C + static_cast<int64_t>(row) * p.ldc + col0 + c;
+              const float *crow = Cb + static_cast<int64_t>(row) * p.ldc + col0 + c;
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
                 const float c0 = (read_c && col0 + c + j < p.N) ? __ldcg(crow + j) : 0.f;
                 w[j] = __float_as_uint(
                     scale_add(p.alpha, __uint_as_float(r[j]), beta, c0, read_c));
               }
-              tma_write_block(smem_u32(sm.stage_c[e]), &tmC, col0 + c, row - lane, p.M, p.N, w,
-                              addto, lane);
+              tma_write_block(smem_u32(sm.stage_c[e]), &tmC, col0 + c, row - lane, bt, p.M, p.N,
+                              w, addto, lane);
             }
           } else {
             if (row < p.M && !*abort) {
               float v[32];
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-              store_row_chunk<kInt>(p, row, col0 + c, v, beta, use_c);
+              store_row_chunk<kInt>(p, Cb, row, col0 + c, v, beta, use_c);
             }
           }
         }
@@ -582,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.c_tma) {
           if (!*abort) {
             const bool read_c = use_c && !addto && row < p.M;
-            const int32_t *crow = p.C + static_cast<int64_t>(row) * p.ldc + col0;
+            const int32_t *crow = Cb + static_cast<int64_t>(row) * p.ldc + col0;
 #pragma unroll
             for (int c = 0; c < 128; c += 32) {
               uint32_t w[32];
@@ -592,8 +634,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 w[j] = static_cast<uint32_t>(
                     scale_add(p.alpha, static_cast<int32_t>(acc[c + j]), beta, c0, read_c));
               }
-              tma_write_block(smem_u32(sm.stage_c[e]), &tmC, col0 + c, row - lane, p.M, p.N, w,
-                              addto, lane);
+              tma_write_block(smem_u32(sm.stage_c[e]), &tmC, col0 + c, row - lane, bt, p.M, p.N,
+                              w, addto, lane);
             }
           }
         } else if (row < p.M && !*abort) {
@@ -602,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int32_t v[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = static_cast<int32_t>(acc[c + j]);
-            store_row_chunk<kInt>(p, row, col0 + c, v, beta, use_c);
+            store_row_chunk<kInt>(p, Cb, row, col0 + c, v, beta, use_c);
           }
         }
       }
@@ -659,39 +701,63 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// Row-major rows x cols matrix of 16-bit elements, row stride ld (elements),
-// boxes of box_rows x box_cols elements; the swizzle spans one box row
-// (box_cols * 2 bytes: 128 or 64).
+// Stride in bytes between the matrices of a stack: the caller's stride, or,
+// for a single matrix, any legal value (the third coordinate is always 0).
+cuuint64_t matrix_stride_bytes(int64_t count, int64_t stride, int64_t rows, int64_t ld,
+                               int esize) {
+  if (count > 1) return static_cast<cuuint64_t>(stride) * esize;
+  return (static_cast<cuuint64_t>(rows) * ld * esize + 15) / 16 * 16;
+}
+
+// A stack of `count` row-major rows x cols matrices of 16-bit elements, row
+// stride ld and matrix stride `stride` (elements), in boxes of box_rows x
+// box_cols elements; the swizzle spans one box row (box_cols * 2 bytes: 128
+// or 64).
 bool make_tmap(CUtensorMap *tm, CUtensorMapDataType dt, const void *base, int64_t rows,
-               int64_t cols, int64_t ld, uint32_t box_rows, uint32_t box_cols) {
+               int64_t cols, int64_t ld, int64_t count, int64_t stride, uint32_t box_rows,
+               uint32_t box_cols) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-  cuuint32_t box[2] = {box_cols, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(tm, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(count)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2,
+                           matrix_stride_bytes(count, stride, rows, ld, 2)};
+  cuuint32_t box[3] = {box_cols, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(tm, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE,
                    box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-// C (row-major rows x cols, 4-byte elements, row stride ld) in boxes of 32 x 32
-// elements with 128-byte swizzle, for the epilogue's TMA stores and reduces.
+// C (a stack of `count` row-major rows x cols matrices, 4-byte elements, row
+// stride ld, matrix stride `stride`) in boxes of 32 x 32 elements with 128-byte
+// swizzle, for the epilogue's TMA stores and reduces.
 bool make_tmap_c(CUtensorMap *tm, bool is_int, const void *base, int64_t rows, int64_t cols,
-                 int64_t ld) {
+                 int64_t ld, int64_t count, int64_t stride) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
-  cuuint32_t box[2] = {32, 32};
-  cuuint32_t estr[2] = {1, 1};
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(count)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 4,
+                           matrix_stride_bytes(count, stride, rows, ld, 4)};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(tm, is_int ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                   2, const_cast<void *>(base), dims, strides, box, estr,
+                   3, const_cast<void *>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// The kernel for an operand form.
+template <bool kInt, bool kPair>
+auto tc_kernel_for(bool a_t, bool b_t) -> decltype(&gemm_tc_kernel<kInt, kPair, false, false>) {
+  if (a_t)
+    return b_t ? gemm_tc_kernel<kInt, kPair, true, true> : gemm_tc_kernel<kInt, kPair, true, false>;
+  return b_t ? gemm_tc_kernel<kInt, kPair, false, true>
+             : gemm_tc_kernel<kInt, kPair, false, false>;
 }
 
 // Co-resident CTA pairs for a pair kernel on this device (0 if pairs are not
@@ -704,7 +770,7 @@ int pair_capacity(const DeviceInfo &dev, size_t smem) {
   std::lock_guard<std::mutex> lock(mu);
   if (dev.device < 0 || dev.device >= 64) return 0;
   if (known[dev.device]) return cache[dev.device];
-  auto kern = gemm_tc_kernel<kInt, true>;
+  auto kern = gemm_tc_kernel<kInt, true, false, false>;
   int n = 0;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) == cudaSuccess) {
@@ -789,14 +855,15 @@ void plan_work(int64_t T, int KB, int kb_unit, int cap, int max_split, int &unit
 }
 
 template <bool kInt>
-cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf16, int M, int N,
-                      int K, typename TcArgs<kInt>::Out alpha, const void *A, int64_t lda,
+cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf16,
+                      const BatchOps &ops, int M, int N, int K,
+                      typename TcArgs<kInt>::Out alpha, const void *A, int64_t lda,
                       const void *B, int64_t ldb, typename TcArgs<kInt>::Out beta,
                       typename TcArgs<kInt>::Out *C, int64_t ldc, cudaStream_t stream,
                       uint32_t *flags_ws, size_t flags_words) {
   // Short, wide problems: the transposed-role kernel streams B at HBM speed
   // instead of multiplying a mostly-zero 256-row tile.
-  if (M <= kSkinnyMaxM) {
+  if (M <= kSkinnyMaxM && ops.plain()) {
     if constexpr (kInt) {
       return launch_tc_skinny_int(dev, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream,
                                   flags_ws, flags_words);
@@ -805,9 +872,39 @@ cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf1
                                     stream);
     }
   }
+  static_assert(sizeof(TcSmem<true>) + 1024 <= 232448, "pair kernel shared memory");
+  static_assert(sizeof(TcSmem<false>) + 1024 <= 232448, "single-CTA kernel shared memory");
+  const size_t smem_pair = sizeof(TcSmem<true>) + 1024;
+  const int pairs = DGR_TC_PAIR ? pair_capacity<kInt>(dev, smem_pair) : 0;
+  const bool use_pairs = pairs > 0;
+  const int tile_m = use_pairs ? Cfg<true>::kTileM : Cfg<false>::kTileM;
+  const uint32_t bn_load = use_pairs ? Cfg<true>::kBNLoad : Cfg<false>::kBNLoad;
+
+  // Operand tensor maps: one matrix, or one per batch entry.
+  const int64_t batch = ops.batch;
+  const int64_t na = (batch > 1 && ops.stride_a != 0) ? batch : 1;
+  const int64_t nb = (batch > 1 && ops.stride_b != 0) ? batch : 1;
   CUtensorMap tmA, tmB;
-  if (!make_tmap(&tmA, dt, A, M, K, lda, kBM, kBK)) return cudaErrorInvalidValue;
-  if (!make_tmap(&tmB, dt, B, K, N, ldb, kBK, 64)) return cudaErrorInvalidValue;
+  const bool maps_ok =
+      (ops.a_t ? make_tmap(&tmA, dt, A, K, M, lda, na, ops.stride_a, kBK, 64)
+               : make_tmap(&tmA, dt, A, M, K, lda, na, ops.stride_a, kBM, kBK)) &&
+      (ops.b_t ? make_tmap(&tmB, dt, B, N, K, ldb, nb, ops.stride_b, bn_load, kBK)
+               : make_tmap(&tmB, dt, B, K, N, ldb, nb, ops.stride_b, kBK, 64));
+  if (!maps_ok) {
+    if (na == 1 && nb == 1) return cudaErrorInvalidValue;
+    // A stride the tensor-map encoder does not take (matrices that overlap):
+    // one launch per batch entry, each on a single matrix.
+    BatchOps one = ops;
+    one.batch = 1;
+    for (int64_t b = 0; b < batch; ++b) {
+      const void *Ab = static_cast<const uint16_t *>(A) + b * ops.stride_a;
+      const void *Bb = static_cast<const uint16_t *>(B) + b * ops.stride_b;
+      cudaError_t e = launch_tc<kInt>(dev, dt, is_bf16, one, M, N, K, alpha, Ab, lda, Bb, ldb,
+                                      beta, C + b * ops.stride_c, ldc, stream, nullptr, 0);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
   TcArgs<kInt> p;
   p.M = M;
   p.N = N;
@@ -816,29 +913,29 @@ cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf1
   p.beta = beta;
   p.C = C;
   p.ldc = ldc;
+  p.tiles_m = (M + tile_m - 1) / tile_m;
   p.tiles_n = (N + kBN - 1) / kBN;
+  p.tiles_per_batch = p.tiles_m * p.tiles_n;
+  p.a_batched = na > 1;
+  p.b_batched = nb > 1;
+  p.stride_c = batch > 1 ? ops.stride_c : 0;
   p.c_vec_ok = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0);
   p.err_word = dev.err_word;
   p.tail_flags = nullptr;
   // TMA stores of C need a 16-byte aligned base and row stride, and rows whose
   // length is a whole number of 16-byte units: a store box is clipped at the
   // right edge of C only in 16-byte units, so with N % 4 != 0 it would also
-  // write the first columns of the row padding. Otherwise the epilogue writes
-  // C with plain guarded stores.
+  // write the first columns of the row padding. A stack of C matrices also
+  // needs a matrix stride of whole 16-byte units. Otherwise the epilogue
+  // writes C with plain guarded stores.
   CUtensorMap tmC;
   std::memset(&tmC, 0, sizeof tmC);
-  p.c_tma = p.c_vec_ok && (N % 4 == 0) && make_tmap_c(&tmC, kInt, C, M, N, ldc);
-
-  static_assert(sizeof(TcSmem<true>) + 1024 <= 232448, "pair kernel shared memory");
-  static_assert(sizeof(TcSmem<false>) + 1024 <= 232448, "single-CTA kernel shared memory");
-  const size_t smem_pair = sizeof(TcSmem<true>) + 1024;
-  const int pairs = DGR_TC_PAIR ? pair_capacity<kInt>(dev, smem_pair) : 0;
-  const bool use_pairs = pairs > 0;
-  const int tile_m = use_pairs ? Cfg<true>::kTileM : Cfg<false>::kTileM;
-  p.tiles_m = (M + tile_m - 1) / tile_m;
-  p.idesc = idesc_f16(is_bf16, false, true, tile_m, kBN);
-  const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
-  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  p.c_tma = p.c_vec_ok && (N % 4 == 0) && (batch == 1 || ops.stride_c % 4 == 0) &&
+            make_tmap_c(&tmC, kInt, C, M, N, ldc, batch, ops.stride_c);
+  p.idesc = idesc_f16(is_bf16, ops.a_t, !ops.b_t, tile_m, kBN);
+  const int64_t tiles = static_cast<int64_t>(p.tiles_per_batch) * batch;
+  if (static_cast<int64_t>(p.tiles_m) * p.tiles_n > 0x7fffffffLL || tiles > 0x7fffffffLL)
+    return cudaErrorInvalidValue;
   const int KB = (K + kBK - 1) / kBK;
   const int cap = use_pairs ? pairs : dev.sm_count;
   const int kb_unit = kInt ? kChunkKB : 1;
@@ -886,11 +983,15 @@ cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf1
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<kInt, true>, tmA, tmB, tmC, p);
+    auto kern = tc_kernel_for<kInt, true>(ops.a_t, ops.b_t);
+    // Every form has the same shared memory; raise the limit for this one.
+    e = set_max_dynamic_smem(reinterpret_cast<const void *>(kern), static_cast<int>(smem_pair),
+                             dev.device);
+    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, p);
     if (e == cudaSuccess) e = cudaGetLastError();
   } else {
     const size_t smem = sizeof(TcSmem<false>) + 1024;
-    auto kern = gemm_tc_kernel<kInt, false>;
+    auto kern = tc_kernel_for<kInt, false>(ops.a_t, ops.b_t);
     e = set_max_dynamic_smem(reinterpret_cast<const void *>(kern), static_cast<int>(smem),
                              dev.device);
     if (e == cudaSuccess) {
@@ -905,20 +1006,24 @@ cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf1
   return e;
 }
 
-// int8 -> fp16, exact (|x| <= 128). dst has row stride ldd (multiple of 8) and
-// its padding columns [cols, ldd) are written with zeros. Each thread widens 16
-// consecutive elements of a row: one 16-byte load when the source row is
-// 16-byte aligned and the chunk is inside the matrix, byte loads otherwise,
-// and one or two 16-byte stores.
-__global__ void widen_s8_kernel(const int8_t *__restrict__ src, int64_t lds, __half *dst,
-                                int64_t ldd, int rows, int cols, int vec_ok) {
+// int8 -> fp16, exact (|x| <= 128), for a stack of `count` rows x cols
+// matrices (source matrix stride src_stride; destination matrices packed at
+// rows * ldd). dst has row stride ldd (multiple of 8) and its padding columns
+// [cols, ldd) are written with zeros. Each thread widens 16 consecutive
+// elements of a row: one 16-byte load when the source row is 16-byte aligned
+// and the chunk is inside the matrix, byte loads otherwise, and one or two
+// 16-byte stores.
+__global__ void widen_s8_kernel(const int8_t *__restrict__ src, int64_t lds, int64_t src_stride,
+                                __half *dst, int64_t ldd, int rows, int cols, int count,
+                                int vec_ok) {
   const int64_t chunks_per_row = (ldd + 15) / 16;
-  const int64_t total = static_cast<int64_t>(rows) * chunks_per_row;
+  const int64_t total = static_cast<int64_t>(rows) * count * chunks_per_row;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t r = i / chunks_per_row;
+    const int64_t r = i / chunks_per_row;  // row of the whole stack
     const int c0 = static_cast<int>((i - r * chunks_per_row) * 16);
-    const int8_t *s = src + r * lds;
+    const int64_t m = r / rows;            // matrix of the stack
+    const int8_t *s = src + m * src_stride + (r - m * rows) * lds;
     __align__(16) __half h[16];
     if (vec_ok && c0 + 16 <= cols) {
       const int4 v = *reinterpret_cast<const int4 *>(s + c0);
@@ -940,16 +1045,18 @@ __global__ void widen_s8_kernel(const int8_t *__restrict__ src, int64_t lds, __h
 }
 
 cudaError_t widen_s8(const DeviceInfo &dev, const int8_t *src, int64_t lds, __half *dst,
-                     int64_t ldd, int rows, int cols, cudaStream_t stream) {
-  const int64_t total = static_cast<int64_t>(rows) * ((ldd + 15) / 16);
+                     int64_t ldd, int rows, int cols, cudaStream_t stream, int count = 1,
+                     int64_t src_stride = 0) {
+  const int64_t total = static_cast<int64_t>(rows) * count * ((ldd + 15) / 16);
   const int threads = 256;
   int64_t blocks = (total + threads - 1) / threads;
   const int64_t cap = static_cast<int64_t>(dev.sm_count) * 16;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  const int vec_ok = (reinterpret_cast<uintptr_t>(src) % 16 == 0) && (lds % 16 == 0);
-  widen_s8_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(src, lds, dst, ldd,
-                                                                        rows, cols, vec_ok);
+  const int vec_ok = (reinterpret_cast<uintptr_t>(src) % 16 == 0) && (lds % 16 == 0) &&
+                     (count == 1 || src_stride % 16 == 0);
+  widen_s8_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+      src, lds, src_stride, dst, ldd, rows, cols, count, vec_ok);
   return cudaGetLastError();
 }
 
@@ -961,7 +1068,17 @@ cudaError_t launch_gemm_tc_f16(const DeviceInfo &dev, bool is_bf16, int M, int N
                                cudaStream_t stream) {
   const CUtensorMapDataType dt =
       is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  return launch_tc<false>(dev, dt, is_bf16, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+  return launch_tc<false>(dev, dt, is_bf16, BatchOps(), M, N, K, alpha, A, lda, B, ldb, beta, C,
+                          ldc, stream, nullptr, 0);
+}
+
+cudaError_t launch_gemm_tc_f16_ex(const DeviceInfo &dev, bool is_bf16, const BatchOps &ops, int M,
+                                  int N, int K, float alpha, const void *A, int64_t lda,
+                                  const void *B, int64_t ldb, float beta, float *C, int64_t ldc,
+                                  cudaStream_t stream) {
+  const CUtensorMapDataType dt =
+      is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return launch_tc<false>(dev, dt, is_bf16, ops, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
                           stream, nullptr, 0);
 }
 
@@ -990,12 +1107,54 @@ cudaError_t launch_gemm_s8(const DeviceInfo &dev, int M, int N, int K, int32_t a
   e = widen_s8(dev, A, lda, a16, lda16, M, K, stream);
   if (e == cudaSuccess) e = widen_s8(dev, B, ldb, b16, ldb16, K, N, stream);
   if (e == cudaSuccess)
-    e = launch_tc<true>(dev, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, false, M, N, K, alpha, a16, lda16,
-                        b16, ldb16, beta, C, ldc, stream, nullptr, 0);
+    e = launch_tc<true>(dev, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, false, BatchOps(), M, N, K, alpha,
+                        a16, lda16, b16, ldb16, beta, C, ldc, stream, nullptr, 0);
   cudaError_t f = cudaFreeAsync(scratch, stream);
   return e != cudaSuccess ? e : f;
 }
 
+// Batched / transposed int8: each operand is widened in its stored layout
+// (one matrix, or one per batch entry, packed), then the tensor-core kernel
+// reads the fp16 copies with the same transposes and strides.
+cudaError_t launch_gemm_s8_ex(const DeviceInfo &dev, const BatchOps &ops, int M, int N, int K,
+                              int32_t alpha, const int8_t *A, int64_t lda, const int8_t *B,
+                              int64_t ldb, int32_t beta, int32_t *C, int64_t ldc,
+                              cudaStream_t stream) {
+  // Stored shapes: A is M x K or K x M, B is K x N or N x K.
+  const int a_rows = ops.a_t ? K : M, a_cols = ops.a_t ? M : K;
+  const int b_rows = ops.b_t ? N : K, b_cols = ops.b_t ? K : N;
+  const int na = (ops.batch > 1 && ops.stride_a != 0) ? ops.batch : 1;
+  const int nb = (ops.batch > 1 && ops.stride_b != 0) ? ops.batch : 1;
+  const int64_t lda16 = (static_cast<int64_t>(a_cols) + 7) / 8 * 8;
+  const int64_t ldb16 = (static_cast<int64_t>(b_cols) + 7) / 8 * 8;
+  const int64_t a_mat = a_rows * lda16, b_mat = b_rows * ldb16;  // packed strides (elements)
+  const size_t a_bytes = static_cast<size_t>(na) * a_mat * 2;
+  const size_t a_off = (a_bytes + 255) / 256 * 256;
+  const size_t total = a_off + static_cast<size_t>(nb) * b_mat * 2;
+
+  cudaMemPool_t pool = nullptr;
+  {
+    cudaError_t e = device_pool(dev, &pool);
+    if (e != cudaSuccess) return e;
+  }
+  void *scratch = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&scratch, total, pool, stream);
+  if (e != cudaSuccess) return e;
+  __half *a16 = static_cast<__half *>(scratch);
+  __half *b16 = reinterpret_cast<__half *>(static_cast<uint8_t *>(scratch) + a_off);
+  e = widen_s8(dev, A, lda, a16, lda16, a_rows, a_cols, stream, na, ops.stride_a);
+  if (e == cudaSuccess)
+    e = widen_s8(dev, B, ldb, b16, ldb16, b_rows, b_cols, stream, nb, ops.stride_b);
+  if (e == cudaSuccess) {
+    BatchOps wide = ops;
+    wide.stride_a = na > 1 ? a_mat : 0;
+    wide.stride_b = nb > 1 ? b_mat : 0;
+    e = launch_tc<true>(dev, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, false, wide, M, N, K, alpha, a16,
+                        lda16, b16, ldb16, beta, C, ldc, stream, nullptr, 0);
+  }
+  cudaError_t f = cudaFreeAsync(scratch, stream);
+  return e != cudaSuccess ? e : f;
+}
 
 // The int8 path with scratch memory supplied by the caller instead of drawn
 // from the library's pool: widen A and B into `scratch` (which must hold
@@ -1020,8 +1179,8 @@ cudaError_t launch_gemm_s8_scratch(const DeviceInfo &dev, int M, int N, int K, i
   cudaError_t e = widen_s8(dev, A, lda, a16, lda16, M, K, stream);
   if (e == cudaSuccess) e = widen_s8(dev, B, ldb, b16, ldb16, K, N, stream);
   if (e == cudaSuccess)
-    e = launch_tc<true>(dev, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, false, M, N, K, alpha, a16, lda16,
-                        b16, ldb16, beta, C, ldc, stream, flags, flags_words);
+    e = launch_tc<true>(dev, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, false, BatchOps(), M, N, K, alpha,
+                        a16, lda16, b16, ldb16, beta, C, ldc, stream, flags, flags_words);
   return e;
 }
 

@@ -22,6 +22,17 @@ struct DeviceInfo {
   uint32_t *err_word = nullptr;  // device address of this device's error word
 };
 
+// Operand forms and batching of the extended entry points (gemm_*_ex):
+// C_b = alpha * op(A_b) * op(B_b) + beta * C_b for b < batch, X_b = X + b *
+// stride_x elements. A stride of 0 (or batch == 1) means one shared matrix.
+struct BatchOps {
+  bool a_t = false;  // A stored K x M (row-major), used transposed
+  bool b_t = false;  // B stored N x K (row-major), used transposed
+  int batch = 1;
+  int64_t stride_a = 0, stride_b = 0, stride_c = 0;  // elements
+  bool plain() const { return !a_t && !b_t && batch == 1; }
+};
+
 // All sizes are already validated: M, N >= 1, K >= 1, each < 2^31, ld >= row length.
 cudaError_t launch_sgemm_simt(const DeviceInfo &dev, int M, int N, int K, float alpha,
                               const float *A, int64_t lda, const float *B, int64_t ldb,
@@ -33,6 +44,22 @@ cudaError_t launch_gemm_tc_f16(const DeviceInfo &dev, bool is_bf16, int M, int N
                                float alpha, const void *A, int64_t lda, const void *B,
                                int64_t ldb, float beta, float *C, int64_t ldc,
                                cudaStream_t stream);
+
+// The same with transposed operands and batches (A and B stored as BatchOps
+// says; the layout rule above applies to the stored matrices, and non-zero
+// strides of A and B are multiples of 8 elements).
+cudaError_t launch_gemm_tc_f16_ex(const DeviceInfo &dev, bool is_bf16, const BatchOps &ops, int M,
+                                  int N, int K, float alpha, const void *A, int64_t lda,
+                                  const void *B, int64_t ldb, float beta, float *C, int64_t ldc,
+                                  cudaStream_t stream);
+cudaError_t launch_gemm_s8_ex(const DeviceInfo &dev, const BatchOps &ops, int M, int N, int K,
+                              int32_t alpha, const int8_t *A, int64_t lda, const int8_t *B,
+                              int64_t ldb, int32_t beta, int32_t *C, int64_t ldc,
+                              cudaStream_t stream);
+cudaError_t launch_sgemm_simt_ex(const DeviceInfo &dev, const BatchOps &ops, int M, int N, int K,
+                                 float alpha, const float *A, int64_t lda, const float *B,
+                                 int64_t ldb, float beta, float *C, int64_t ldc,
+                                 cudaStream_t stream);
 
 cudaError_t launch_gemm_s8(const DeviceInfo &dev, int M, int N, int K, int32_t alpha,
                            const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
@@ -90,6 +117,11 @@ cudaError_t launch_scale_f32(int M, int N, float beta, float *C, int64_t ldc,
                              cudaStream_t stream);
 cudaError_t launch_scale_s32(int M, int N, int32_t beta, int32_t *C, int64_t ldc,
                              cudaStream_t stream);
+// The same over a stack of `batch` C matrices, `stride` elements apart.
+cudaError_t launch_scale_batched_f32(int M, int N, float beta, float *C, int64_t ldc, int batch,
+                                     int64_t stride, cudaStream_t stream);
+cudaError_t launch_scale_batched_s32(int M, int N, int32_t beta, int32_t *C, int64_t ldc,
+                                     int batch, int64_t stride, cudaStream_t stream);
 
 // Accessors to the ABI layer's shared host logic (defined in abi.cu). The
 // status values are those of gemm_status_t.

@@ -141,6 +141,32 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint
 
 // 2-D tiled bulk tensor store shared -> global (elements outside the tensor
 // are not written), and the same with an element-wise add into global memory.
+// Three-dimensional forms (x, y, z): the batched GEMM's operands and output
+// are stacks of row-major matrices, z the matrix index.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint32_t bar, int c0,
+                                            int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];\n" ::"r"(dst),
+      "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const void *tmap, int c0, int c1, int c2,
+                                             uint32_t src) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];\n" ::
+          "l"(tmap),
+      "r"(c0), "r"(c1), "r"(c2), "r"(src)
+      : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_3d(const void *tmap, int c0, int c1, int c2,
+                                                  uint32_t src) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%1, %2, %3}], [%4];\n" ::"l"(tmap),
+      "r"(c0), "r"(c1), "r"(c2), "r"(src)
+      : "memory");
+}
 __device__ __forceinline__ void tma_store_2d(const void *tmap, int c0, int c1, uint32_t src) {
   asm volatile(
       "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];\n" ::"l"(
@@ -355,6 +381,14 @@ __device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t cta_mas
 
 // TMA load into this CTA's shared memory whose completion is signalled on an
 // mbarrier that may live in the peer CTA (shared::cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void *tmap,
+                                                 uint32_t cluster_bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile"
+      ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];\n" ::"r"(dst),
+      "l"(tmap), "r"(cluster_bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *tmap,
                                                  uint32_t cluster_bar, int c0, int c1) {
   asm volatile(

@@ -33,6 +33,12 @@
 //    here a chunk is only used when that is safe.
 //  * Epilogue: alpha*acc + beta*C with 16-byte accesses where aligned, scalar
 //    guarded accesses at the edges. C is not read when beta == 0.
+//  * Transposed operands and batches (the extended entry point): the shared
+//    tiles keep their layouts (A k-major, B n-major), only the copies change.
+//    A stored K x M is copied straight (16-byte chunks when aligned); B stored
+//    N x K is copied with the same conflict-free transposing pattern as A
+//    (its tile then also has a padded row stride of 132). The batch entry is
+//    blockIdx.y.
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -69,6 +75,7 @@ struct SimtArgs {
   int64_t ldb;
   float *C;
   int64_t ldc;
+  int64_t stride_a, stride_b, stride_c;  // elements between batch entries (blockIdx.y)
   int tiles_m, tiles_n;
   int c_vec_ok;  // C 16-byte aligned and ldc % 4 == 0
 };
@@ -78,10 +85,10 @@ struct SimtArgs {
 // banks, and every 4-float group stays 16-byte aligned for the fragment loads.
 constexpr int kAStride = kBM + 4;
 
-template <int BK, int STAGES>
+template <int BK, int STAGES, int BStride>
 struct SimtSmem {
   float a[STAGES][BK][kAStride];  // A tile, transposed: a[s][k][m]
-  float b[STAGES][BK][kBN];       // B tile: b[s][k][n]
+  float b[STAGES][BK][BStride];   // B tile: b[s][k][n]
 };
 
 // Linear CTA index -> (tile_m, tile_n): groups of kGroupM tile rows are walked
@@ -96,62 +103,95 @@ __device__ __forceinline__ void tile_coords(int bid, int tiles_m, int tiles_n, i
   tn = r / rows;
 }
 
-template <int BK, bool VEC_B>
-__device__ __forceinline__ void load_tile(const SimtArgs &p, float (*sa)[kAStride],
-                                          float (*sb)[kBN], int m0, int n0, int k0, int tid) {
-  // A: one warp instruction copies 4 rows x 8 consecutive k (lane = 8*row + k),
-  // i.e. four 32-byte global segments, into the transposed tile. The BK/2
-  // instructions of a thread walk (row group, k half) pairs of its warp.
-  {
-    static_assert(BK % 8 == 0, "A staging copies k in groups of 8");
-    constexpr int kGroupsK = BK / 8;
-    const int warp = tid >> 5, lane = tid & 31;
-    const int r_lo = lane >> 3, k_lo = lane & 7;
+// Copies a 4 x 8 (rows x k) block per warp instruction from a row-major matrix
+// whose rows run along k into the k-major tile dst[k][row] (row stride 132):
+// lane = 8 * row + k, so one warp reads four 32-byte segments and its 32
+// stores hit 32 distinct banks. rows_valid / k_valid bound the source.
+template <int BK>
+__device__ __forceinline__ void copy_transposing(const float *src, int64_t ld, float (*dst)[kAStride],
+                                                 int r0, int k0, int rows_valid, int k_valid,
+                                                 int tid) {
+  static_assert(BK % 8 == 0, "transposing copies take k in groups of 8");
+  constexpr int kGroupsK = BK / 8;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int r_lo = lane >> 3, k_lo = lane & 7;
 #pragma unroll
-    for (int i = 0; i < BK / 2; ++i) {
-      const int pair = warp * (BK / 2) + i;        // 0 .. 4*BK-1
-      const int m = (pair / kGroupsK) * 4 + r_lo;   // 32 groups of 4 rows
-      const int k = (pair % kGroupsK) * 8 + k_lo;   // groups of 8 k
-      const int gm = m0 + m, gk = k0 + k;
-      const bool ok = gm < p.M && gk < p.K;
-      const float *src = ok ? p.A + static_cast<int64_t>(gm) * p.lda + gk : p.A;
-      cp_async_4(smem_u32(&sa[k][m]), src, ok ? 4u : 0u);
-    }
+  for (int i = 0; i < BK / 2; ++i) {
+    const int pair = warp * (BK / 2) + i;        // 0 .. 4*BK-1
+    const int r = (pair / kGroupsK) * 4 + r_lo;   // 32 groups of 4 rows
+    const int k = (pair % kGroupsK) * 8 + k_lo;   // groups of 8 k
+    const int gr = r0 + r, gk = k0 + k;
+    const bool ok = gr < rows_valid && gk < k_valid;
+    const float *p = ok ? src + static_cast<int64_t>(gr) * ld + gk : src;
+    cp_async_4(smem_u32(&dst[k][r]), p, ok ? 4u : 0u);
   }
-  // B: row-major BK x 128 tile.
-  if constexpr (VEC_B) {
-    constexpr int kChunks = BK * kBN / 4 / kThreads;
+}
+
+// Copies rows k0 .. k0+BK-1, columns c0 .. c0+127 of a row-major matrix whose
+// rows run along k straight into dst[k][col]: 16-byte chunks when VEC (every
+// chunk then lies wholly inside or outside the matrix), 4-byte elements
+// otherwise.
+template <int BK, bool VEC, int Stride>
+__device__ __forceinline__ void copy_straight(const float *src, int64_t ld, float (*dst)[Stride],
+                                              int k0, int c0, int k_valid, int c_valid, int tid) {
+  if constexpr (VEC) {
+    constexpr int kChunks = BK * 128 / 4 / kThreads;
 #pragma unroll
     for (int i = 0; i < kChunks; ++i) {
       const int c = tid + i * kThreads;
       const int row = c >> 5;
       const int col = (c & 31) * 4;
-      const int gk = k0 + row, gn = n0 + col;
-      const bool ok = gk < p.K && gn < p.N;
-      const float *src = ok ? p.B + static_cast<int64_t>(gk) * p.ldb + gn : p.B;
-      cp_async_16(smem_u32(&sb[row][col]), src, ok ? 16u : 0u);
+      const int gk = k0 + row, gc = c0 + col;
+      const bool ok = gk < k_valid && gc < c_valid;
+      const float *p = ok ? src + static_cast<int64_t>(gk) * ld + gc : src;
+      cp_async_16(smem_u32(&dst[row][col]), p, ok ? 16u : 0u);
     }
   } else {
-    constexpr int kPer = BK * kBN / kThreads;
+    constexpr int kPer = BK * 128 / kThreads;
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
       const int e = tid + i * kThreads;
       const int row = e >> 7;
-      const int col = e & (kBN - 1);
-      const int gk = k0 + row, gn = n0 + col;
-      const bool ok = gk < p.K && gn < p.N;
-      const float *src = ok ? p.B + static_cast<int64_t>(gk) * p.ldb + gn : p.B;
-      cp_async_4(smem_u32(&sb[row][col]), src, ok ? 4u : 0u);
+      const int col = e & 127;
+      const int gk = k0 + row, gc = c0 + col;
+      const bool ok = gk < k_valid && gc < c_valid;
+      const float *p = ok ? src + static_cast<int64_t>(gk) * ld + gc : src;
+      cp_async_4(smem_u32(&dst[row][col]), p, ok ? 4u : 0u);
     }
   }
 }
 
-template <int BK, int STAGES, bool VEC_B>
+// One BK-deep stage: the A tile (k-major, 128 rows of op(A)) and the B tile
+// (k rows x 128 columns of op(B)). A_T / B_T: the operand is stored
+// transposed; VEC_A / VEC_B: its straight copy may use 16-byte chunks.
+template <int BK, bool A_T, bool VEC_A, bool B_T, bool VEC_B, int BStride>
+__device__ __forceinline__ void load_tile(const SimtArgs &p, const float *A, const float *B,
+                                          float (*sa)[kAStride], float (*sb)[BStride], int m0,
+                                          int n0, int k0, int tid) {
+  if constexpr (A_T) {
+    copy_straight<BK, VEC_A, kAStride>(A, p.lda, sa, k0, m0, p.K, p.M, tid);  // stored K x M
+  } else {
+    copy_transposing<BK>(A, p.lda, sa, m0, k0, p.M, p.K, tid);  // stored M x K
+  }
+  if constexpr (B_T) {
+    copy_transposing<BK>(B, p.ldb, sb, n0, k0, p.N, p.K, tid);  // stored N x K
+  } else {
+    copy_straight<BK, VEC_B, BStride>(B, p.ldb, sb, k0, n0, p.K, p.N, tid);  // stored K x N
+  }
+}
+
+// BATCH: blockIdx.y selects the batch entry (otherwise a single problem, and
+// the operand addresses stay in the parameter bank instead of registers).
+template <int BK, int STAGES, bool A_T, bool VEC_A, bool B_T, bool VEC_B, bool BATCH>
 __global__ void __launch_bounds__(kThreads, 2) sgemm_simt_kernel(const SimtArgs p) {
+  constexpr int kBStride = B_T ? kAStride : kBN;
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  auto &sm = *reinterpret_cast<SimtSmem<BK, STAGES> *>(smem_raw);
+  auto &sm = *reinterpret_cast<SimtSmem<BK, STAGES, kBStride> *>(smem_raw);
 
   const int tid = threadIdx.x;
+  const float *A = BATCH ? p.A + blockIdx.y * p.stride_a : p.A;
+  const float *B = BATCH ? p.B + blockIdx.y * p.stride_b : p.B;
+  float *C = BATCH ? p.C + blockIdx.y * p.stride_c : p.C;
   int tm, tn;
   tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, tm, tn);
   const int m0 = tm * kBM, n0 = tn * kBN;
@@ -171,7 +211,9 @@ __global__ void __launch_bounds__(kThreads, 2) sgemm_simt_kernel(const SimtArgs 
   const int KT = (p.K + BK - 1) / BK;
 #pragma unroll
   for (int s = 0; s < STAGES - 1; ++s) {
-    if (s < KT) load_tile<BK, VEC_B>(p, sm.a[s], sm.b[s], m0, n0, s * BK, tid);
+    if (s < KT)
+      load_tile<BK, A_T, VEC_A, B_T, VEC_B, kBStride>(p, A, B, sm.a[s], sm.b[s], m0, n0, s * BK,
+                                                       tid);
     cp_async_commit();
   }
 
@@ -182,7 +224,8 @@ __global__ void __launch_bounds__(kThreads, 2) sgemm_simt_kernel(const SimtArgs 
       const int nt = kt + STAGES - 1;
       if (nt < KT) {
         const int s = nt % STAGES;
-        load_tile<BK, VEC_B>(p, sm.a[s], sm.b[s], m0, n0, nt * BK, tid);
+        load_tile<BK, A_T, VEC_A, B_T, VEC_B, kBStride>(p, A, B, sm.a[s], sm.b[s], m0, n0,
+                                                         nt * BK, tid);
       }
       cp_async_commit();
     }
@@ -217,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 2) sgemm_simt_kernel(const SimtArgs 
   for (int i = 0; i < 8; ++i) {
     const int row = m0 + rm + (i & 3) + (i >> 2) * 64;
     if (row >= p.M) continue;
-    float *crow = p.C + static_cast<int64_t>(row) * p.ldc;
+    float *crow = C + static_cast<int64_t>(row) * p.ldc;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int col = n0 + cn + h * 64;
@@ -245,23 +288,63 @@ __global__ void __launch_bounds__(kThreads, 2) sgemm_simt_kernel(const SimtArgs 
   }
 }
 
-template <int BK, int STAGES, bool VEC_B>
-cudaError_t launch_variant(const SimtArgs &a, int device, cudaStream_t stream) {
-  constexpr size_t smem = sizeof(SimtSmem<BK, STAGES>);
-  auto kern = sgemm_simt_kernel<BK, STAGES, VEC_B>;
+template <int BK, int STAGES, bool A_T, bool VEC_A, bool B_T, bool VEC_B, bool BATCH = true>
+cudaError_t launch_variant(const SimtArgs &a, int batch, int device, cudaStream_t stream) {
+  constexpr size_t smem = sizeof(SimtSmem<BK, STAGES, B_T ? kAStride : kBN>);
+  auto kern = sgemm_simt_kernel<BK, STAGES, A_T, VEC_A, B_T, VEC_B, BATCH>;
   cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void *>(kern),
                                        static_cast<int>(smem), device);
   if (e != cudaSuccess) return e;
   const int64_t blocks = static_cast<int64_t>(a.tiles_m) * a.tiles_n;
-  kern<<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(a);
-  return cudaGetLastError();
+  // The batch runs on gridDim.y, at most 65535 entries per launch.
+  constexpr int kMaxY = 65535;
+  for (int b0 = 0; b0 < batch; b0 += kMaxY) {
+    SimtArgs c = a;
+    c.A += b0 * a.stride_a;
+    c.B += b0 * a.stride_b;
+    c.C += b0 * a.stride_c;
+    const unsigned ny = static_cast<unsigned>(batch - b0 < kMaxY ? batch - b0 : kMaxY);
+    kern<<<dim3(static_cast<unsigned>(blocks), ny), kThreads, smem, stream>>>(c);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+#ifndef DGR_SIMT_BK
+#define DGR_SIMT_BK 32
+#endif
+#ifndef DGR_SIMT_STAGES
+#define DGR_SIMT_STAGES 2
+#endif
+constexpr int kSimtBK = DGR_SIMT_BK, kSimtStages = DGR_SIMT_STAGES;
+
+template <bool A_T, bool VEC_A>
+cudaError_t launch_b(const SimtArgs &a, bool b_t, bool vec_b, int batch, int device,
+                     cudaStream_t stream) {
+  if (b_t)
+    return launch_variant<kSimtBK, kSimtStages, A_T, VEC_A, true, false>(a, batch, device, stream);
+  return vec_b ? launch_variant<kSimtBK, kSimtStages, A_T, VEC_A, false, true>(a, batch, device,
+                                                                               stream)
+               : launch_variant<kSimtBK, kSimtStages, A_T, VEC_A, false, false>(a, batch, device,
+                                                                                stream);
+}
+
+// 16-byte chunks of a straight copy are safe when the stored matrix (and every
+// matrix of a stack) starts 16-byte aligned, its rows are whole 16-byte units
+// apart, and its row length `cols` is a multiple of 4 (a chunk never straddles
+// the right edge).
+bool vec_ok(const float *base, int64_t ld, int64_t cols, int batch, int64_t stride) {
+  return (reinterpret_cast<uintptr_t>(base) % 16 == 0) && (ld % 4 == 0) && (cols % 4 == 0) &&
+         (batch == 1 || stride % 4 == 0);
 }
 
 }  // namespace
 
-cudaError_t launch_sgemm_simt(const DeviceInfo &dev, int M, int N, int K, float alpha,
-                              const float *A, int64_t lda, const float *B, int64_t ldb,
-                              float beta, float *C, int64_t ldc, cudaStream_t stream) {
+cudaError_t launch_sgemm_simt_ex(const DeviceInfo &dev, const BatchOps &ops, int M, int N, int K,
+                                 float alpha, const float *A, int64_t lda, const float *B,
+                                 int64_t ldb, float beta, float *C, int64_t ldc,
+                                 cudaStream_t stream) {
   SimtArgs a;
   a.M = M;
   a.N = N;
@@ -274,20 +357,32 @@ cudaError_t launch_sgemm_simt(const DeviceInfo &dev, int M, int N, int K, float 
   a.ldb = ldb;
   a.C = C;
   a.ldc = ldc;
+  const int batch = ops.batch;
+  a.stride_a = batch > 1 ? ops.stride_a : 0;
+  a.stride_b = batch > 1 ? ops.stride_b : 0;
+  a.stride_c = batch > 1 ? ops.stride_c : 0;
   a.tiles_m = (M + kBM - 1) / kBM;
   a.tiles_n = (N + kBN - 1) / kBN;
-  a.c_vec_ok = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0);
+  a.c_vec_ok = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0) &&
+               (batch == 1 || a.stride_c % 4 == 0);
   if (static_cast<int64_t>(a.tiles_m) * a.tiles_n > 0x7fffffffLL) return cudaErrorInvalidValue;
-  const bool vec_b = (reinterpret_cast<uintptr_t>(B) % 16 == 0) && (ldb % 4 == 0) && (N % 4 == 0);
-#ifndef DGR_SIMT_BK
-#define DGR_SIMT_BK 32
-#endif
-#ifndef DGR_SIMT_STAGES
-#define DGR_SIMT_STAGES 2
-#endif
-  constexpr int kBK = DGR_SIMT_BK, kStages = DGR_SIMT_STAGES;
-  return vec_b ? launch_variant<kBK, kStages, true>(a, dev.device, stream)
-               : launch_variant<kBK, kStages, false>(a, dev.device, stream);
+  const bool vec_a = ops.a_t && vec_ok(A, lda, M, batch, a.stride_a);
+  const bool vec_b = !ops.b_t && vec_ok(B, ldb, N, batch, a.stride_b);
+  if (ops.plain())  // one problem, no transposes: the kernels without a batch index
+    return vec_b ? launch_variant<kSimtBK, kSimtStages, false, false, false, true, false>(
+                       a, 1, dev.device, stream)
+                 : launch_variant<kSimtBK, kSimtStages, false, false, false, false, false>(
+                       a, 1, dev.device, stream);
+  if (!ops.a_t) return launch_b<false, false>(a, ops.b_t, vec_b, batch, dev.device, stream);
+  return vec_a ? launch_b<true, true>(a, ops.b_t, vec_b, batch, dev.device, stream)
+               : launch_b<true, false>(a, ops.b_t, vec_b, batch, dev.device, stream);
+}
+
+cudaError_t launch_sgemm_simt(const DeviceInfo &dev, int M, int N, int K, float alpha,
+                              const float *A, int64_t lda, const float *B, int64_t ldb,
+                              float beta, float *C, int64_t ldc, cudaStream_t stream) {
+  return launch_sgemm_simt_ex(dev, BatchOps(), M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                              stream);
 }
 
 }  // namespace dgr

@@ -1,6 +1,7 @@
 """Time one C-ABI entry point on one problem shape.
 
     python -m dense_gemm_row_gb300.timing --dtype bf16 --shape 16,8192,8192 [--iters 20]
+        [--ops NN|NT|TN|TT] [--batch B]
 
 Draws seeded operands of the given shape (workloads.matrix: N(0,1) for floats,
 uniform -128..127 for int8; alpha = 1, beta = 0), runs the entry point a few
@@ -9,6 +10,10 @@ one stream and prints one JSON line: milliseconds per call, TFLOP/s (TOPS for
 int8) and the GB/s of the algorithmic bytes (A and B read once, C written
 once). Used for the per-shape measurements in profiles/ (run it under ncu with
 a small --iters).
+
+--ops and --batch time the extended entry points (gemm_*_ex): a stack of B
+problems, each operand stored as op says (T: the transpose is stored); the
+figures are then totals over the stack.
 """
 from __future__ import annotations
 
@@ -24,6 +29,8 @@ _DTYPES = {"f32": (torch.float32, torch.float32, binding.gemm_f32),
            "bf16": (torch.bfloat16, torch.float32, binding.gemm_bf16),
            "f16": (torch.float16, torch.float32, binding.gemm_f16),
            "s8": (torch.int8, torch.int32, binding.gemm_s8)}
+_EX = {"f32": binding.gemm_f32_ex, "bf16": binding.gemm_bf16_ex, "f16": binding.gemm_f16_ex,
+       "s8": binding.gemm_s8_ex}
 
 
 def main(argv=None) -> int:
@@ -33,32 +40,46 @@ def main(argv=None) -> int:
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--seed", type=int, default=1)
+    ap.add_argument("--ops", choices=["NN", "NT", "TN", "TT"], default="NN")
+    ap.add_argument("--batch", type=int, default=1)
     a = ap.parse_args(argv)
     M, N, K = (int(x) for x in a.shape.split(","))
     in_dt, out_dt, fn = _DTYPES[a.dtype]
     dist = "int8" if a.dtype == "s8" else "normal"
-    A = w.matrix(M, K, in_dt, dist, a.seed * 3).cuda()
-    B = w.matrix(K, N, in_dt, dist, a.seed * 3 + 1).cuda()
-    C = torch.zeros(M, N, dtype=out_dt, device="cuda")
+    a_t, b_t = a.ops[0] == "T", a.ops[1] == "T"
+    nb = a.batch
+    A = w.stack(nb, *((K, M) if a_t else (M, K)), in_dt, dist, a.seed * 3).flat.cuda()
+    B = w.stack(nb, *((N, K) if b_t else (K, N)), in_dt, dist, a.seed * 3 + 1000).flat.cuda()
+    C = torch.zeros(nb * M * N, dtype=out_dt, device="cuda")
     one, zero = (1, 0) if a.dtype == "s8" else (1.0, 0.0)
     stream = torch.cuda.current_stream()
-    args = (M, N, K, one, A, K, B, N, zero, C, N, stream)
+    if a.ops == "NN" and nb == 1:
+        def call():
+            fn(M, N, K, one, A, K, B, N, zero, C, N, stream)
+    else:
+        ex = _EX[a.dtype]
+        ops = (binding.OP_T if a_t else binding.OP_N, binding.OP_T if b_t else binding.OP_N)
+
+        def call():
+            ex(*ops, M, N, K, one, A, M if a_t else K, M * K, B, K if b_t else N, K * N, zero, C,
+               N, M * N, nb, stream)
     for _ in range(a.warmup):
-        fn(*args)
+        call()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(a.iters):
-        fn(*args)
+        call()
     e1.record(stream)
     torch.cuda.synchronize()
     binding.check_device_error()
     ms = e0.elapsed_time(e1) / a.iters
     nbytes = (A.numel() * A.element_size() + B.numel() * B.element_size()
               + C.numel() * C.element_size())
-    print(json.dumps({"dtype": a.dtype, "M": M, "N": N, "K": K, "iters": a.iters, "ms": ms,
-                      "tflops": 2.0 * M * N * K / (ms / 1e3) / 1e12,
+    print(json.dumps({"dtype": a.dtype, "M": M, "N": N, "K": K, "ops": a.ops, "batch": nb,
+                      "iters": a.iters, "ms": ms,
+                      "tflops": 2.0 * nb * M * N * K / (ms / 1e3) / 1e12,
                       "gbs": nbytes / (ms / 1e3) / 1e9}))
     return 0
 

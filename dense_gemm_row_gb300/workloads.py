@@ -78,6 +78,42 @@ def matrix(rows: int, cols: int, dtype: torch.dtype, dist: str, seed: int,
 
 
 @dataclass
+class Stack:
+    """`batch` row-major rows x cols matrices in one flat buffer: matrix b
+    starts at element b * stride, rows are ld apart. Everything outside the
+    matrices (row padding, gaps between matrices) holds the poison value."""
+    flat: torch.Tensor
+    batch: int
+    rows: int
+    cols: int
+    ld: int
+    stride: int
+
+    def mat(self, b: int) -> torch.Tensor:
+        """View of matrix b (rows x cols, row stride ld)."""
+        if self.rows == 0 or self.cols == 0:
+            return torch.empty((self.rows, self.cols), dtype=self.flat.dtype)
+        base = self.flat[b * self.stride:b * self.stride + (self.rows - 1) * self.ld + self.cols]
+        return base.as_strided((self.rows, self.cols), (self.ld, 1))
+
+
+def stack(batch: int, rows: int, cols: int, dtype: torch.dtype, dist: str, seed: int,
+          ld: int | None = None, gap: int = 0) -> Stack:
+    """A Stack of `batch` independent draws of matrix(rows, cols, dtype, dist,
+    seed + b), with row stride ld (>= cols) and matrix stride rows * ld + gap."""
+    ld = max(cols, 1) if ld is None else int(ld)
+    if ld < cols:
+        raise ValueError("ld must be >= cols")
+    stride = rows * ld + int(gap)
+    poison = INT8_POISON if dtype == torch.int8 else FLOAT_POISON
+    flat = torch.full((max(batch * stride, 1),), poison, dtype=dtype)
+    st = Stack(flat, batch, rows, cols, ld, stride)
+    for b in range(batch):
+        st.mat(b).copy_(matrix(rows, cols, dtype, dist, seed + b))
+    return st
+
+
+@dataclass
 class Problem:
     """Operands of one GEMM call: C = alpha*A*B + beta*C0."""
     name: str

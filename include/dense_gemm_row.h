@@ -123,6 +123,57 @@ GEMM_API gemm_status_t gemm_s8(int64_t M, int64_t N, int64_t K, int32_t alpha,
                       const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
                       int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream);
 
+/* Operand forms for the extended entry points. */
+typedef enum {
+    GEMM_OP_N = 0, /* the operand as stored (row-major) */
+    GEMM_OP_T = 1  /* the transpose of the stored row-major matrix */
+} gemm_op_t;
+
+/*
+ * Extended entry points: strided-batched GEMM with transposed operands.
+ *
+ *   for b in [0, batch):
+ *     C_b = alpha * op(A_b) * op(B_b) + beta * C_b
+ *   A_b = A + b*strideA, B_b = B + b*strideB, C_b = C + b*strideC (elements)
+ *
+ * op(A_b) is M x K: with GEMM_OP_N, A_b is stored M x K row-major (lda >= K);
+ * with GEMM_OP_T, A_b is stored K x M row-major (lda >= M) and transposed.
+ * op(B_b) is K x N: GEMM_OP_N stores K x N (ldb >= N); GEMM_OP_T stores N x K
+ * (ldb >= K). C_b is M x N row-major (ldc >= N). batch >= 1 (batch = 0 does
+ * nothing). The C_b must not overlap each other or any input: when batch > 1,
+ * strideC >= (M - 1) * ldc + N (else GEMM_ERR_INVALID_VALUE). Input strides
+ * may be any value >= 0, including 0 (one matrix shared by every batch entry);
+ * gemm_bf16_ex and gemm_f16_ex need them to be multiples of 8 elements (16
+ * bytes) when batch > 1 (else GEMM_ERR_UNSUPPORTED_LAYOUT).
+ * Everything else -- beta == 0 never reads C, K == 0, alignment rules, status
+ * codes, streams -- is as for the plain entry points, and a call with
+ * GEMM_OP_N, GEMM_OP_N and batch == 1 computes exactly what the plain call does.
+ * Sources: the plain entry points' definition applied to each batch entry; the
+ * batched (bmm) and transposed forms are the dlog page's PyTorch matmul
+ * survey (section 矩阵相乘的若干写法: mm, bmm, einsum) and the WMMA page's
+ * row_major / col_major operand layouts.
+ */
+GEMM_API gemm_status_t gemm_f32_ex(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N, int64_t K,
+                                   float alpha, const float *A, int64_t lda, int64_t strideA,
+                                   const float *B, int64_t ldb, int64_t strideB, float beta,
+                                   float *C, int64_t ldc, int64_t strideC, int64_t batch,
+                                   cudaStream_t stream);
+GEMM_API gemm_status_t gemm_bf16_ex(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N,
+                                    int64_t K, float alpha, const gemm_bf16_t *A, int64_t lda,
+                                    int64_t strideA, const gemm_bf16_t *B, int64_t ldb,
+                                    int64_t strideB, float beta, float *C, int64_t ldc,
+                                    int64_t strideC, int64_t batch, cudaStream_t stream);
+GEMM_API gemm_status_t gemm_f16_ex(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N, int64_t K,
+                                   float alpha, const gemm_f16_t *A, int64_t lda,
+                                   int64_t strideA, const gemm_f16_t *B, int64_t ldb,
+                                   int64_t strideB, float beta, float *C, int64_t ldc,
+                                   int64_t strideC, int64_t batch, cudaStream_t stream);
+GEMM_API gemm_status_t gemm_s8_ex(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N, int64_t K,
+                                  int32_t alpha, const int8_t *A, int64_t lda, int64_t strideA,
+                                  const int8_t *B, int64_t ldb, int64_t strideB, int32_t beta,
+                                  int32_t *C, int64_t ldc, int64_t strideC, int64_t batch,
+                                  cudaStream_t stream);
+
 /*
  * gemm_s8_noalloc -- gemm_s8 for callers that must not allocate device memory.
  * The pages have no counterpart of this entry point; it is part of this

@@ -93,3 +93,51 @@ def test_tensor_core_layout_rule(gemm_mod, fn):
     assert f(8, 8, 8, 1.0, FAKE, 8, FAKE + 8, 8, 0.0, FAKE, 8, None) == LAYOUT
     assert f(8, 8, 12, 1.0, FAKE, 12, FAKE, 8, 0.0, FAKE, 8, None) == LAYOUT
     assert f(8, 12, 8, 1.0, FAKE, 8, FAKE, 12, 0.0, FAKE, 12, None) == LAYOUT
+
+
+EX = ["gemm_f32_ex", "gemm_bf16_ex", "gemm_f16_ex", "gemm_s8_ex"]
+N_, T_ = 0, 1
+
+
+def call_ex(f, fn, opA=N_, opB=N_, M=8, N=8, K=8, A=FAKE, lda=8, sA=64, B=FAKE, ldb=8, sB=64,
+            C=FAKE, ldc=8, sC=64, batch=2):
+    a = 1 if fn == "gemm_s8_ex" else 1.0
+    return f(opA, opB, M, N, K, a, A, lda, sA, B, ldb, sB, a, C, ldc, sC, batch, None)
+
+
+@pytest.mark.parametrize("fn", EX)
+def test_extended_invalid_arguments_rejected_on_host(gemm_mod, fn):
+    f = getattr(gemm_mod.lib, fn)
+    assert call_ex(f, fn, opA=2) == INVALID               # not a gemm_op_t
+    assert call_ex(f, fn, opB=-1) == INVALID
+    assert call_ex(f, fn, batch=-1) == INVALID
+    assert call_ex(f, fn, batch=2**31) == INVALID
+    assert call_ex(f, fn, sA=-8) == INVALID               # negative strides
+    assert call_ex(f, fn, sB=-8) == INVALID
+    assert call_ex(f, fn, sC=-8) == INVALID
+    assert call_ex(f, fn, sC=8 * 7 + 7) == INVALID        # C matrices overlap: < (M-1)*ldc + N
+    # Stored row lengths follow the operand form: A^T rows hold M, B^T rows hold K.
+    assert call_ex(f, fn, opA=T_, M=16, lda=8) == INVALID
+    assert call_ex(f, fn, opB=T_, K=16, lda=16, ldb=8) == INVALID
+    assert call_ex(f, fn, opA=N_, K=16, lda=8) == INVALID
+    assert call_ex(f, fn, A=None) == INVALID
+    assert call_ex(f, fn, C=None) == INVALID
+
+
+@pytest.mark.parametrize("fn", EX)
+def test_extended_empty_is_a_no_op(gemm_mod, fn):
+    f = getattr(gemm_mod.lib, fn)
+    assert call_ex(f, fn, batch=0, A=None, B=None, C=None) == OK
+    assert call_ex(f, fn, M=0, A=None, B=None, C=None) == OK
+    assert call_ex(f, fn, N=0, A=None, B=None, C=None) == OK
+
+
+@pytest.mark.parametrize("fn", ["gemm_bf16_ex", "gemm_f16_ex"])
+def test_extended_tensor_core_layout_rule(gemm_mod, fn):
+    """Matrix strides of A and B in whole 16-byte units when batch > 1, on top
+    of the plain entry points' base and row-stride rule."""
+    f = getattr(gemm_mod.lib, fn)
+    assert call_ex(f, fn, sA=68) == LAYOUT
+    assert call_ex(f, fn, sB=12) == LAYOUT
+    assert call_ex(f, fn, A=FAKE + 2) == LAYOUT
+    assert call_ex(f, fn, opA=T_, lda=12, M=12, ldc=12, N=8, sC=256) == LAYOUT
