@@ -59,9 +59,22 @@ def load(path: str):
         fn = getattr(lib, name)
         fn.argtypes = [i64, i64, i64, f64, vp, i64, vp, i64, f64, vp, i64]
         fn.restype = ctypes.c_int
-    lib.oracle_gemm_s8.argtypes = [i64, i64, i64, ctypes.c_int32, vp, i64, vp, i64,
-                                   ctypes.c_int32, vp, i64]
-    lib.oracle_gemm_s8.restype = ctypes.c_int
+    for name in ("oracle_gemm_s8", "oracle_gemm_u8"):
+        fn = getattr(lib, name)
+        fn.argtypes = [i64, i64, i64, ctypes.c_int32, vp, i64, vp, i64, ctypes.c_int32, vp, i64]
+        fn.restype = ctypes.c_int
+    lib.oracle_gemm_tf32.argtypes = [i64, i64, i64, f64, vp, i64, vp, i64, f64, vp, i64]
+    lib.oracle_gemm_tf32.restype = ctypes.c_int
+    for name in ("oracle_gemm_f16_f16", "oracle_gemm_bf16_bf16"):
+        fn = getattr(lib, name)
+        fn.argtypes = [i64, i64, i64, f64, vp, i64, vp, i64, f64, vp, i64]
+        fn.restype = ctypes.c_int
+    lib.oracle_encode_f16.argtypes = [f64]
+    lib.oracle_encode_f16.restype = ctypes.c_uint16
+    lib.oracle_encode_bf16.argtypes = [f64]
+    lib.oracle_encode_bf16.restype = ctypes.c_uint16
+    lib.oracle_round_tf32.argtypes = [ctypes.c_float]
+    lib.oracle_round_tf32.restype = ctypes.c_float
     lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
     lib.oracle_decode_bf16.restype = f64
     lib.oracle_decode_f16.argtypes = [ctypes.c_uint16]
@@ -107,14 +120,17 @@ _FLOAT_DTYPES = {
 
 
 def gemm(A: torch.Tensor, B: torch.Tensor, alpha: float = 1.0, beta: float = 0.0,
-         C0: torch.Tensor | np.ndarray | None = None) -> np.ndarray:
+         C0: torch.Tensor | np.ndarray | None = None, tf32: bool = False) -> np.ndarray:
     """C = alpha*A*B + beta*C0 for float32/bfloat16/float16/float64 A and B.
 
     Returns the float64 result, not rounded to the inputs' type. ``C0`` (any
     float type, converted exactly to float64) is not read when beta == 0.
+    tf32=True (float32 A and B only): the inputs are first reduced to tf32.
     """
     if A.dtype != B.dtype or A.dtype not in _FLOAT_DTYPES:
         raise TypeError("oracle.gemm: A and B must share one float dtype")
+    if tf32 and A.dtype != torch.float32:
+        raise TypeError("oracle.gemm: tf32 takes float32 inputs")
     M, K = A.shape
     K2, N = B.shape
     if K != K2:
@@ -128,17 +144,40 @@ def gemm(A: torch.Tensor, B: torch.Tensor, alpha: float = 1.0, beta: float = 0.0
         C = np.array(c0, dtype=np.float64, order="C", copy=True)
         if C.shape != (M, N):
             raise ValueError("oracle.gemm: C0 has the wrong shape")
-    fn = getattr(_lib(), _FLOAT_DTYPES[A.dtype])
+    fn = getattr(_lib(), "oracle_gemm_tf32" if tf32 else _FLOAT_DTYPES[A.dtype])
     _check(fn(M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb, float(beta),
               C.ctypes.data, max(N, 1)))
     return C
 
 
+def gemm_out16(A: torch.Tensor, B: torch.Tensor, alpha: float = 1.0, beta: float = 0.0,
+               C0: torch.Tensor | None = None) -> torch.Tensor:
+    """16-bit A, B and C of one format (float16 or bfloat16): the exact result
+    rounded once to that format. Returns a CPU tensor of the inputs' dtype."""
+    if A.dtype != B.dtype or A.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError("oracle.gemm_out16: A and B must both be float16 or bfloat16")
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError("oracle.gemm_out16: inner dimensions differ")
+    lda, ldb = _ld(A, "A"), _ld(B, "B")
+    if C0 is None:
+        C = torch.zeros((M, N), dtype=A.dtype)
+    else:
+        if C0.dtype != A.dtype or tuple(C0.shape) != (M, N):
+            raise ValueError("oracle.gemm_out16: C0 must be M x N of the inputs' dtype")
+        C = C0.detach().cpu().contiguous().clone()
+    name = "oracle_gemm_bf16_bf16" if A.dtype == torch.bfloat16 else "oracle_gemm_f16_f16"
+    _check(getattr(_lib(), name)(M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb,
+                                 float(beta), C.data_ptr(), max(N, 1)))
+    return C
+
+
 def gemm_s8(A: torch.Tensor, B: torch.Tensor, alpha: int = 1, beta: int = 0,
             C0: torch.Tensor | np.ndarray | None = None) -> np.ndarray:
-    """int8 A and B, int64 accumulation, int32 wrap-around output."""
-    if A.dtype != torch.int8 or B.dtype != torch.int8:
-        raise TypeError("oracle.gemm_s8: A and B must be int8")
+    """int8 (or uint8) A and B, int64 accumulation, int32 wrap-around output."""
+    if A.dtype != B.dtype or A.dtype not in (torch.int8, torch.uint8):
+        raise TypeError("oracle.gemm_s8: A and B must both be int8 or both uint8")
     M, K = A.shape
     K2, N = B.shape
     if K != K2:
@@ -153,9 +192,13 @@ def gemm_s8(A: torch.Tensor, B: torch.Tensor, alpha: int = 1, beta: int = 0,
         C = np.array(c0, dtype=np.int32, order="C", copy=True)
         if C.shape != (M, N):
             raise ValueError("oracle.gemm_s8: C0 has the wrong shape")
-    _check(_lib().oracle_gemm_s8(M, N, K, int(alpha), A.data_ptr(), lda, B.data_ptr(), ldb,
-                                 int(beta), C.ctypes.data, max(N, 1)))
+    fn = _lib().oracle_gemm_u8 if A.dtype == torch.uint8 else _lib().oracle_gemm_s8
+    _check(fn(M, N, K, int(alpha), A.data_ptr(), lda, B.data_ptr(), ldb, int(beta),
+              C.ctypes.data, max(N, 1)))
     return C
+
+
+gemm_u8 = gemm_s8
 
 
 def gemm_rows(A: torch.Tensor, B: torch.Tensor, rows, alpha=1.0, beta=0.0, C0=None):
@@ -168,7 +211,7 @@ def gemm_rows(A: torch.Tensor, B: torch.Tensor, rows, alpha=1.0, beta=0.0, C0=No
     if C0 is not None:
         c0t = C0 if isinstance(C0, torch.Tensor) else torch.from_numpy(np.asarray(C0))
         c0 = c0t.index_select(0, idx)
-    if A.dtype == torch.int8:
+    if A.dtype in (torch.int8, torch.uint8):
         return gemm_s8(a, B, int(alpha), int(beta), c0)
     return gemm(a, B, alpha, beta, c0)
 
@@ -179,3 +222,18 @@ def decode_bf16(bits: int) -> float:
 
 def decode_f16(bits: int) -> float:
     return float(_lib().oracle_decode_f16(bits))
+
+
+def encode_f16(x: float) -> int:
+    """Bits of x rounded to IEEE binary16 (nearest, ties to even)."""
+    return int(_lib().oracle_encode_f16(float(x)))
+
+
+def encode_bf16(x: float) -> int:
+    """Bits of x rounded to bfloat16 (nearest, ties to even)."""
+    return int(_lib().oracle_encode_bf16(float(x)))
+
+
+def round_tf32(x: float) -> float:
+    """The fp32 value x reduced to tf32 (13 lowest fraction bits cleared)."""
+    return float(_lib().oracle_round_tf32(float(x)))

@@ -33,8 +33,26 @@ MUTANTS = [
     ("f16_exponent_bias", [("e - 25", "e - 24")]),
     ("f16_subnormal_scale", [("ldexp((double)m, -24)", "ldexp((double)m, -25)")]),
     ("bf16_shift", [("(uint32_t)h << 16", "(uint32_t)h << 15")]),
-    ("s8_read_as_unsigned", [("acc[j] += a * (int64_t)brow[j];",
-                              "acc[j] += a * (int64_t)(uint8_t)brow[j];")]),
+    ("s8_read_as_unsigned", [(": (int64_t)Bs[k * ldb + j];",
+                              ": (int64_t)(uint8_t)Bs[k * ldb + j];")]),
+    ("u8_read_as_signed", [("? (int64_t)Bu[k * ldb + j]", "? (int64_t)(int8_t)Bu[k * ldb + j]")]),
+    ("u8_A_read_as_signed", [("? (int64_t)Au[i * lda + k]", "? (int64_t)(int8_t)Au[i * lda + k]")]),
+    ("encode_ties_away_from_zero", [("(frac == 0.5 && fmod(r, 2.0) != 0.0)", "(frac == 0.5)")]),
+    ("encode_truncates", [("if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;",
+                           "")]),
+    ("encode_flushes_subnormals", [("if (ex < emin) ex = emin;",
+                                    "if (ex < emin) return sign_bit;")]),
+    ("encode_saturates_on_overflow", [("if (v > max_finite) return sign_bit | exp_all;",
+                                       "if (v > max_finite) v = max_finite;")]),
+    ("encode_drops_sign", [("const uint32_t sign = signbit(x) ? 1u : 0u;",
+                            "const uint32_t sign = 0u;")]),
+    ("tf32_clears_12_bits", [("u &= ~0x1fffu;", "u &= ~0xfffu;")]),
+    ("tf32_rounds_up", [("u &= ~0x1fffu;", "u = (u + 0x1000u) & ~0x1fffu;")]),
+    ("tf32_not_applied", [("return (double)oracle_round_tf32(((const float *)p)[i]);",
+                           "return (double)((const float *)p)[i];")]),
+    ("out16_c0_not_read", [("c[i * N + j] = (beta == 0.0) ? 0.0", "c[i * N + j] = 1 ? 0.0")]),
+    ("out16_wrong_format", [("C[i * ldc + j] = is_bf16 ? oracle_encode_bf16",
+                             "C[i * ldc + j] = !is_bf16 ? oracle_encode_bf16")]),
     ("s8_beta_dropped", [("v += (uint64_t)(int64_t)beta * (uint64_t)(int64_t)crow[j];",
                           "v += (uint64_t)(int64_t)crow[j];")]),
     ("s8_saturates_instead_of_wrapping",

@@ -303,3 +303,190 @@ def test_ldc_padding_direct(oracle_mod):
     # [5+16, 6-18, 7-20] = [21, -12, -13]; [15-32, 18+36, 21+40] = [-17, 54, 61]
     np.testing.assert_array_equal(Ci[:, :3], [[21, -12, -13], [-17, 54, 61]])
     assert (Ci[:, 3] == -7).all()
+
+
+# ------------------------------------------------------------------ uint8 (u8 -> int)
+
+def test_uint8_matches_numpy_int64(oracle_mod):
+    """unsigned char inputs (the WMMA table's u8 -> int row) against numpy's
+    int64 matmul, then int32 wrap-around."""
+    g = torch.Generator().manual_seed(31)
+    A = torch.randint(0, 256, (37, 300), generator=g, dtype=torch.int32).to(torch.uint8)
+    B = torch.randint(0, 256, (300, 29), generator=g, dtype=torch.int32).to(torch.uint8)
+    C0 = torch.randint(-1000, 1000, (37, 29), generator=g, dtype=torch.int32)
+    got = oracle_mod.gemm_u8(A, B, 5, -3, C0)
+    exact = 5 * (A.numpy().astype(np.int64) @ B.numpy().astype(np.int64)) \
+        - 3 * C0.numpy().astype(np.int64)
+    np.testing.assert_array_equal(got, ((exact + 2**31) % 2**32 - 2**31).astype(np.int32))
+
+
+def test_uint8_extremes_and_wrap(oracle_mod):
+    """All-255 operands: every entry is 65025 * K (no sign), and K = 40000
+    overflows int32 and wraps."""
+    for K in (1, 1000, 40000):
+        A = torch.full((2, K), 255, dtype=torch.uint8)
+        B = torch.full((K, 3), 255, dtype=torch.uint8)
+        v = (65025 * K) % 2**32
+        v = v - 2**32 if v >= 2**31 else v
+        assert (oracle_mod.gemm_u8(A, B) == v).all()
+
+
+def test_uint8_hand_computed(oracle_mod):
+    A = torch.tensor([[200, 1], [0, 255]], dtype=torch.uint8)
+    B = torch.tensor([[3, 128], [250, 2]], dtype=torch.uint8)
+    # [200*3 + 1*250, 200*128 + 1*2] = [850, 25602]; [0 + 255*250, 0 + 255*2] = [63750, 510]
+    np.testing.assert_array_equal(oracle_mod.gemm_u8(A, B), [[850, 25602], [63750, 510]])
+
+
+# ------------------------------------------------------------- 16-bit encoders
+
+def test_encode_f16_round_trips_every_pattern(oracle_mod):
+    """Every finite binary16 value encodes back to its own bits (-0 included);
+    every NaN pattern encodes to a NaN."""
+    for h in range(65536):
+        x = oracle_mod.decode_f16(h)
+        e = oracle_mod.encode_f16(x)
+        if np.isnan(x):
+            assert (e & 0x7c00) == 0x7c00 and (e & 0x3ff) != 0
+        else:
+            assert e == h, (hex(h), x, hex(e))
+
+
+def test_encode_bf16_round_trips_every_pattern(oracle_mod):
+    for h in range(65536):
+        x = oracle_mod.decode_bf16(h)
+        e = oracle_mod.encode_bf16(x)
+        if np.isnan(x):
+            assert (e & 0x7f80) == 0x7f80 and (e & 0x7f) != 0
+        else:
+            assert e == h, (hex(h), x, hex(e))
+
+
+def _f16_probe_values(seed):
+    """Random doubles over binary16's range, plus exact midpoints between
+    neighbouring binary16 values and points just off them (the round-to-even
+    cases), subnormals and overflow."""
+    rng = np.random.default_rng(seed)
+    vals = list(rng.standard_normal(2000) * np.exp2(rng.integers(-26, 17, 2000)))
+    h = rng.integers(0, 0x7bff, 500).astype(np.uint16)
+    lo = h.view(np.float16).astype(np.float64)
+    hi = (h + 1).astype(np.uint16).view(np.float16).astype(np.float64)
+    mid = (lo + hi) / 2
+    vals += list(mid) + list(-mid) + list(np.nextafter(mid, 0)) + list(np.nextafter(mid, 1e9))
+    vals += [65504.0, 65519.99, 65520.0, -65520.0, 1e6, 2**-24, 2**-25, 3 * 2**-26, 1e-9, 0.0]
+    return vals
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_encode_f16_matches_numpy(oracle_mod, seed):
+    """numpy's float64 -> float16 cast rounds to nearest, ties to even, in one
+    step: the library reference for binary16 rounding."""
+    with np.errstate(over="ignore"):
+        for x in _f16_probe_values(seed):
+            assert oracle_mod.encode_f16(x) == int(np.float16(x).view(np.uint16)), x
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_encode_bf16_matches_torch_on_float32_values(oracle_mod, seed):
+    """torch's float32 -> bfloat16 cast rounds to nearest, ties to even; for
+    values that are exact in float32 it is the one rounding of the value."""
+    g = torch.Generator().manual_seed(100 + seed)
+    x = torch.randn(3000, generator=g) * torch.exp2(torch.randint(-140, 120, (3000,), generator=g)
+                                                     .float())
+    bits16 = torch.randint(0, 0x7f7f, (500,), generator=g, dtype=torch.int32)
+    lo = (bits16 << 16).view(torch.float32)
+    mid = ((bits16 << 16) + 0x8000).view(torch.float32)   # exact midpoint to the next value
+    x = torch.cat([x, lo, mid, -mid, mid.nextafter(torch.zeros(1)),
+                   torch.tensor([3.3895313892515355e38, 3.40282e38, 1e-40, 1e-45])])
+    ref = x.to(torch.bfloat16).view(torch.int16).to(torch.int32) & 0xffff
+    for v, r in zip(x.tolist(), ref.tolist()):
+        assert oracle_mod.encode_bf16(v) == r, v
+
+
+def test_encode_ties_go_to_even(oracle_mod):
+    """Hand cases: halfway between two binary16 values the even one wins."""
+    # 1 + 2^-11 lies halfway between 1 (even) and 1 + 2^-10 (odd)
+    assert oracle_mod.encode_f16(1 + 2**-11) == 0x3C00
+    # 1 + 3 * 2^-11 lies halfway between 1 + 2^-10 (odd) and 1 + 2^-9 (even)
+    assert oracle_mod.encode_f16(1 + 3 * 2**-11) == 0x3C02
+    # bfloat16 keeps 7 fraction bits: 1 + 2^-8 -> 1, 1 + 3 * 2^-8 -> 1 + 2^-6
+    assert oracle_mod.encode_bf16(1 + 2**-8) == 0x3F80
+    assert oracle_mod.encode_bf16(1 + 3 * 2**-8) == 0x3F82
+
+
+# ------------------------------------------------------------- 16-bit outputs
+
+@pytest.mark.parametrize("seed", range(4))
+def test_f16_output_equals_numpy_rounding_of_exact_result(oracle_mod, seed):
+    """Small-integer fp16 inputs make the product exact in float64, so numpy's
+    float64 arithmetic and its one-step float16 cast give the exact answer."""
+    g = torch.Generator().manual_seed(200 + seed)
+    M, N, K = 9, 11, 37
+    A = torch.randint(-40, 41, (M, K), generator=g).to(torch.float16)
+    B = torch.randint(-40, 41, (K, N), generator=g).to(torch.float16)
+    C0 = (torch.randn(M, N, generator=g) * 100).to(torch.float16)
+    alpha, beta = 0.3, -1.75
+    got = oracle_mod.gemm_out16(A, B, alpha, beta, C0)
+    acc = A.double().numpy() @ B.double().numpy()
+    ref = (alpha * acc + beta * C0.double().numpy()).astype(np.float16)
+    np.testing.assert_array_equal(got.numpy().view(np.uint16), ref.view(np.uint16))
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_bf16_output_equals_torch_rounding_of_exact_result(oracle_mod, seed):
+    """Integer results below 2^24 are exact in float32, where torch's bf16
+    cast is the one rounding of the exact value."""
+    g = torch.Generator().manual_seed(300 + seed)
+    M, N, K = 7, 13, 50
+    A = torch.randint(-60, 61, (M, K), generator=g).to(torch.bfloat16)
+    B = torch.randint(-60, 61, (K, N), generator=g).to(torch.bfloat16)
+    C0 = torch.randint(-5000, 5000, (M, N), generator=g).to(torch.bfloat16)
+    got = oracle_mod.gemm_out16(A, B, 2.0, 3.0, C0)
+    exact = 2 * (A.to(torch.int64) @ B.to(torch.int64)) + 3 * C0.to(torch.int64)
+    ref = exact.to(torch.float32).to(torch.bfloat16)
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+
+
+def test_out16_beta_zero_does_not_read_c(oracle_mod):
+    A = torch.ones(3, 4, dtype=torch.float16)
+    B = torch.ones(4, 5, dtype=torch.float16)
+    C0 = torch.full((3, 5), float("nan"), dtype=torch.float16)
+    got = oracle_mod.gemm_out16(A, B, 1.0, 0.0, C0)
+    assert (got == 4).all()
+
+
+# ------------------------------------------------------------------------ tf32
+
+def test_round_tf32_hand_values(oracle_mod):
+    """tf32 keeps 10 fraction bits; the 13 lower ones are cleared (truncation)."""
+    assert oracle_mod.round_tf32(1.0) == 1.0
+    assert oracle_mod.round_tf32(1 + 2**-10) == 1 + 2**-10          # representable
+    assert oracle_mod.round_tf32(1 + 2**-11) == 1.0                  # below the last bit
+    assert oracle_mod.round_tf32(1 + 2**-10 + 2**-11 + 2**-20) == 1 + 2**-10
+    assert oracle_mod.round_tf32(-(1 + 2**-10 + 2**-11)) == -(1 + 2**-10)  # toward zero
+    assert oracle_mod.round_tf32(3 * 2**-130) == 3 * 2**-130         # subnormal, few bits
+    x = float(np.float32(np.pi))
+    assert oracle_mod.round_tf32(x) == 3.140625                      # 1.1001001000b * 2
+
+
+def test_tf32_gemm_on_tf32_exact_inputs_is_the_fp32_gemm(oracle_mod):
+    """Inputs that already fit in tf32 (integers below 2^11) are unchanged, so
+    the tf32 GEMM equals the exact integer product."""
+    g = torch.Generator().manual_seed(41)
+    A = torch.randint(-1000, 1001, (21, 33), generator=g).float()
+    B = torch.randint(-1000, 1001, (33, 17), generator=g).float()
+    got = oracle_mod.gemm(A, B, 1.0, 0.0, tf32=True)
+    np.testing.assert_array_equal(got, (A.to(torch.int64) @ B.to(torch.int64)).double().numpy())
+
+
+def test_tf32_gemm_ignores_low_fraction_bits(oracle_mod):
+    """Brute force on a tiny case: adding 2^-12 to a value near 1 (below tf32's
+    last fraction bit) must not change the tf32 product."""
+    A = torch.tensor([[1 + 2**-12, 2.0], [3.0, 1 + 2**-10 + 2**-13]], dtype=torch.float32)
+    B = torch.tensor([[1 + 2**-11, 1.0], [1.0, 4.0]], dtype=torch.float32)
+    got = oracle_mod.gemm(A, B, 1.0, 0.0, tf32=True)
+    a = [[Fraction(1), Fraction(2)], [Fraction(3), 1 + Fraction(1, 1024)]]
+    b = [[Fraction(1), Fraction(1)], [Fraction(1), Fraction(4)]]
+    for i in range(2):
+        for j in range(2):
+            assert got[i, j] == float(sum(a[i][k] * b[k][j] for k in range(2)))
