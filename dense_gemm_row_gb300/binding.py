@@ -41,17 +41,20 @@ STATUS = {
 }
 
 # Every function include/dense_gemm_row.h declares.
-EXPORTED = ("gemm_f32", "gemm_bf16", "gemm_f16", "gemm_s8", "gemm_f32_ex", "gemm_bf16_ex",
+EXPORTED = ("gemm_f32", "gemm_bf16", "gemm_f16", "gemm_s8", "gemm_u8", "gemm_f16_f16",
+            "gemm_bf16_bf16", "gemm_tf32", "gemm_f64", "gemm_f32_ex", "gemm_bf16_ex",
             "gemm_f16_ex", "gemm_s8_ex", "gemm_s8_noalloc", "gemm_status_string",
-            "gemm_check_device_error", "gemm_selftest_wait_timeout", "gemm_version")
+            "gemm_check_device_error", "gemm_selftest_wait_timeout", "gemm_last_launch_error",
+            "gemm_version")
 
 OP_N, OP_T = 0, 1  # gemm_op_t
 
 
 class GemmError(RuntimeError):
-    def __init__(self, status: int, where: str):
+    def __init__(self, status: int, where: str, detail: str = ""):
         self.status = int(status)
-        super().__init__(f"{where}: {STATUS.get(self.status, self.status)}")
+        msg = f"{where}: {STATUS.get(self.status, self.status)}"
+        super().__init__(msg + (f" ({detail})" if detail else ""))
 
 
 def _load():
@@ -62,11 +65,15 @@ def _load():
     lib = ctypes.CDLL(LIB_PATH)
     i64, vp = ctypes.c_int64, ctypes.c_void_p
     f32, i32 = ctypes.c_float, ctypes.c_int32
-    for name in ("gemm_f32", "gemm_bf16", "gemm_f16"):
+    for name in ("gemm_f32", "gemm_bf16", "gemm_f16", "gemm_f16_f16", "gemm_bf16_bf16",
+                 "gemm_tf32"):
         fn = getattr(lib, name)
         fn.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
         fn.restype = ctypes.c_int
-    for name in ("gemm_s8", "gemm_s8_noalloc"):
+    f64 = ctypes.c_double
+    lib.gemm_f64.argtypes = [i64, i64, i64, f64, vp, i64, vp, i64, f64, vp, i64, vp]
+    lib.gemm_f64.restype = ctypes.c_int
+    for name in ("gemm_s8", "gemm_s8_noalloc", "gemm_u8"):
         fn = getattr(lib, name)
         fn.argtypes = [i64, i64, i64, i32, vp, i64, vp, i64, i32, vp, i64, vp]
         fn.restype = ctypes.c_int
@@ -83,6 +90,8 @@ def _load():
     lib.gemm_check_device_error.restype = ctypes.c_int
     lib.gemm_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
     lib.gemm_selftest_wait_timeout.restype = ctypes.c_int
+    lib.gemm_last_launch_error.argtypes = []
+    lib.gemm_last_launch_error.restype = ctypes.c_char_p
     lib.gemm_version.argtypes = []
     lib.gemm_version.restype = ctypes.c_int
     return lib
@@ -110,7 +119,8 @@ def _stream(s) -> int | None:
 
 def _check(status: int, where: str) -> None:
     if status != 0:
-        raise GemmError(status, where)
+        detail = lib.gemm_last_launch_error().decode() if status == 3 else ""
+        raise GemmError(status, where, detail)
 
 
 def gemm_f32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
@@ -131,6 +141,31 @@ def gemm_f16(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
 def gemm_s8(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
     _check(lib.gemm_s8(M, N, K, int(alpha), _addr(A), lda, _addr(B), ldb, int(beta), _addr(C),
                        ldc, _stream(stream)), "gemm_s8")
+
+
+def gemm_u8(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
+    _check(lib.gemm_u8(M, N, K, int(alpha), _addr(A), lda, _addr(B), ldb, int(beta), _addr(C),
+                       ldc, _stream(stream)), "gemm_u8")
+
+
+def gemm_f16_f16(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
+    _check(lib.gemm_f16_f16(M, N, K, alpha, _addr(A), lda, _addr(B), ldb, beta, _addr(C), ldc,
+                            _stream(stream)), "gemm_f16_f16")
+
+
+def gemm_bf16_bf16(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
+    _check(lib.gemm_bf16_bf16(M, N, K, alpha, _addr(A), lda, _addr(B), ldb, beta, _addr(C), ldc,
+                              _stream(stream)), "gemm_bf16_bf16")
+
+
+def gemm_tf32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
+    _check(lib.gemm_tf32(M, N, K, alpha, _addr(A), lda, _addr(B), ldb, beta, _addr(C), ldc,
+                         _stream(stream)), "gemm_tf32")
+
+
+def gemm_f64(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
+    _check(lib.gemm_f64(M, N, K, float(alpha), _addr(A), lda, _addr(B), ldb, float(beta),
+                        _addr(C), ldc, _stream(stream)), "gemm_f64")
 
 
 def gemm_s8_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
@@ -177,10 +212,12 @@ def _ld(t, name) -> int:
     return max(int(t.stride(0)), int(t.shape[1]), 1)
 
 
-def gemm(A, B, C, alpha=1.0, beta=0.0, stream=None):
-    """C = alpha*A*B + beta*C for 2-D CUDA tensors; dtype selects the entry point:
-    float32 -> gemm_f32, bfloat16 -> gemm_bf16, float16 -> gemm_f16 (C float32),
-    int8 -> gemm_s8 (C int32)."""
+def gemm(A, B, C, alpha=1.0, beta=0.0, stream=None, tf32=False):
+    """C = alpha*A*B + beta*C for 2-D CUDA tensors; the dtypes select the entry
+    point: float32 -> gemm_f32 (gemm_tf32 with tf32=True), float64 -> gemm_f64,
+    bfloat16 / float16 with a float32 C -> gemm_bf16 / gemm_f16, with a C of the
+    inputs' dtype -> gemm_bf16_bf16 / gemm_f16_f16, int8 -> gemm_s8 and uint8
+    -> gemm_u8 (C int32)."""
     import torch
     M, K = A.shape
     K2, N = B.shape
@@ -188,11 +225,15 @@ def gemm(A, B, C, alpha=1.0, beta=0.0, stream=None):
         raise ValueError("gemm: shapes do not chain (A: MxK, B: KxN, C: MxN)")
     if A.dtype != B.dtype:
         raise TypeError("gemm: A and B must share a dtype")
-    fns = {torch.float32: (gemm_f32, torch.float32), torch.bfloat16: (gemm_bf16, torch.float32),
-           torch.float16: (gemm_f16, torch.float32), torch.int8: (gemm_s8, torch.int32)}
+    fns = {torch.float32: (gemm_tf32 if tf32 else gemm_f32, torch.float32),
+           torch.float64: (gemm_f64, torch.float64),
+           torch.bfloat16: (gemm_bf16, torch.float32), torch.float16: (gemm_f16, torch.float32),
+           torch.int8: (gemm_s8, torch.int32), torch.uint8: (gemm_u8, torch.int32)}
     if A.dtype not in fns:
         raise TypeError(f"gemm: unsupported dtype {A.dtype}")
     fn, c_dtype = fns[A.dtype]
+    if A.dtype in (torch.bfloat16, torch.float16) and C.dtype == A.dtype:
+        fn, c_dtype = (gemm_bf16_bf16 if A.dtype == torch.bfloat16 else gemm_f16_f16), A.dtype
     if C.dtype != c_dtype:
         raise TypeError(f"gemm: C must be {c_dtype} for {A.dtype} inputs")
     fn(M, N, K, alpha, A, _ld(A, "A"), B, _ld(B, "B"), beta, C, _ld(C, "C"), stream)

@@ -4,11 +4,14 @@
 // and dispatch to the kernels. Nothing here allocates or frees user memory,
 // prints, or aborts.
 #include <cstdint>
+#include <cstring>
 #include <map>
 #include <mutex>
 #include <type_traits>
 #include <utility>
 
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "../../include/dense_gemm_row.h"
@@ -80,8 +83,12 @@ gemm_status_t check_args(int64_t M, int64_t N, int64_t K, const void *A, int64_t
   return GEMM_OK;
 }
 
+// The CUDA error behind this thread's last GEMM_ERR_LAUNCH (gemm_last_launch_error).
+thread_local cudaError_t g_last_launch_error = cudaSuccess;
+
 gemm_status_t from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return GEMM_OK;
+  g_last_launch_error = e;
   cudaGetLastError();  // clear a sticky launch error so later calls are not blamed
   return GEMM_ERR_LAUNCH;
 }
@@ -117,6 +124,24 @@ cudaError_t launch_scale(int M, int N, T beta, T *C, int64_t ldc, cudaStream_t s
   scale_kernel<T><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(M, N, beta, C, ldc, batch,
                                                                      stride);
   return cudaGetLastError();
+}
+
+// 16-bit C: C = round16(beta * C), 0 when beta == 0.
+template <bool kBf16>
+__global__ void scale16_kernel(int M, int N, float beta, uint16_t *C, int64_t ldc) {
+  const int64_t total = static_cast<int64_t>(M) * N;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / N, c = i - r * N;
+    uint16_t *p = C + r * ldc + c;
+    if (kBf16) {
+      const float v = beta == 0.f ? 0.f : beta * __bfloat162float(__ushort_as_bfloat16(*p));
+      *p = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    } else {
+      const float v = beta == 0.f ? 0.f : beta * __half2float(__ushort_as_half(*p));
+      *p = __half_as_ushort(__float2half_rn(v));
+    }
+  }
 }
 
 // Argument checks of the extended entry points: operand forms, sizes, the
@@ -167,6 +192,32 @@ cudaError_t set_max_dynamic_smem(const void *kernel, int bytes, int device) {
   return e;
 }
 
+// Library-owned stream-ordered memory pool of a device (scratch for the 8-bit
+// paths, the tf32 operand copies and split-k workspaces); freed blocks stay
+// mapped for reuse.
+cudaError_t device_pool(const DeviceInfo &dev, cudaMemPool_t *out) {
+  static std::mutex mu;
+  static cudaMemPool_t pools[kMaxDevices] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev.device < 0 || dev.device >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!pools[dev.device]) {
+    cudaMemPoolProps props;
+    std::memset(&props, 0, sizeof props);
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev.device;
+    cudaMemPool_t pl;
+    cudaError_t e = cudaMemPoolCreate(&pl, &props);
+    if (e != cudaSuccess) return e;
+    uint64_t keep = ~0ull;  // keep freed memory mapped for the next call
+    cudaMemPoolSetAttribute(pl, cudaMemPoolAttrReleaseThreshold, &keep);
+    pools[dev.device] = pl;
+  }
+  *out = pools[dev.device];
+  return cudaSuccess;
+}
+
 cudaError_t launch_scale_batched_f32(int M, int N, float beta, float *C, int64_t ldc, int batch,
                                      int64_t stride, cudaStream_t stream) {
   return launch_scale<float>(M, N, beta, C, ldc, stream, batch, stride);
@@ -184,6 +235,24 @@ int abi_check_args(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, 
 int abi_current_device(const DeviceInfo **out) { return current_device(out); }
 
 int abi_from_cuda(cudaError_t e) { return from_cuda(e); }
+
+cudaError_t launch_scale_f64(int M, int N, double beta, double *C, int64_t ldc,
+                             cudaStream_t stream) {
+  return launch_scale<double>(M, N, beta, C, ldc, stream);
+}
+
+cudaError_t launch_scale_out16(bool is_bf16, int M, int N, float beta, uint16_t *C, int64_t ldc,
+                               cudaStream_t stream) {
+  const int64_t total = static_cast<int64_t>(M) * N;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  if (is_bf16) {
+    scale16_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(M, N, beta, C, ldc);
+  } else {
+    scale16_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(M, N, beta, C, ldc);
+  }
+  return cudaGetLastError();
+}
 
 cudaError_t launch_scale_f32(int M, int N, float beta, float *C, int64_t ldc,
                              cudaStream_t stream) {
@@ -267,6 +336,79 @@ gemm_status_t gemm_s8(int64_t M, int64_t N, int64_t K, int32_t alpha, const int8
                                             beta, C, ldc, stream));
   return from_cuda(dgr::launch_gemm_s8(*dev, int(M), int(N), int(K), alpha, A, lda, B, ldb, beta,
                                        C, ldc, stream));
+}
+
+gemm_status_t gemm_u8(int64_t M, int64_t N, int64_t K, int32_t alpha, const uint8_t *A,
+                      int64_t lda, const uint8_t *B, int64_t ldb, int32_t beta, int32_t *C,
+                      int64_t ldc, cudaStream_t stream) {
+  bool skip = false;
+  gemm_status_t st = check_args(M, N, K, A, lda, B, ldb, C, ldc, &skip);
+  if (st != GEMM_OK || skip) return st;
+  const DeviceInfo *dev = nullptr;
+  if ((st = current_device(&dev)) != GEMM_OK) return st;
+  if (K == 0) return from_cuda(dgr::launch_scale_s32(int(M), int(N), beta, C, ldc, stream));
+  return from_cuda(dgr::launch_gemm_u8(*dev, int(M), int(N), int(K), alpha, A, lda, B, ldb, beta,
+                                       C, ldc, stream));
+}
+
+static gemm_status_t gemm_out16(bool is_bf16, int64_t M, int64_t N, int64_t K, float alpha,
+                                const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
+                                float beta, uint16_t *C, int64_t ldc, cudaStream_t stream) {
+  bool skip = false;
+  gemm_status_t st = check_args(M, N, K, A, lda, B, ldb, C, ldc, &skip);
+  if (st != GEMM_OK || skip) return st;
+  if (K > 0) {
+    // TMA: 16-byte aligned bases and row strides.
+    if ((reinterpret_cast<uintptr_t>(A) & 15u) || (reinterpret_cast<uintptr_t>(B) & 15u) ||
+        (lda % 8) || (ldb % 8))
+      return GEMM_ERR_UNSUPPORTED_LAYOUT;
+  }
+  const DeviceInfo *dev = nullptr;
+  if ((st = current_device(&dev)) != GEMM_OK) return st;
+  if (K == 0)
+    return from_cuda(dgr::launch_scale_out16(is_bf16, int(M), int(N), beta, C, ldc, stream));
+  return from_cuda(dgr::launch_gemm_tc_out16(*dev, is_bf16, int(M), int(N), int(K), alpha, A, lda,
+                                             B, ldb, beta, C, ldc, stream));
+}
+
+gemm_status_t gemm_f16_f16(int64_t M, int64_t N, int64_t K, float alpha, const gemm_f16_t *A,
+                           int64_t lda, const gemm_f16_t *B, int64_t ldb, float beta,
+                           gemm_f16_t *C, int64_t ldc, cudaStream_t stream) {
+  return gemm_out16(false, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+}
+
+gemm_status_t gemm_bf16_bf16(int64_t M, int64_t N, int64_t K, float alpha, const gemm_bf16_t *A,
+                             int64_t lda, const gemm_bf16_t *B, int64_t ldb, float beta,
+                             gemm_bf16_t *C, int64_t ldc, cudaStream_t stream) {
+  return gemm_out16(true, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+}
+
+gemm_status_t gemm_tf32(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                        int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                        int64_t ldc, cudaStream_t stream) {
+  bool skip = false;
+  gemm_status_t st = check_args(M, N, K, A, lda, B, ldb, C, ldc, &skip);
+  if (st != GEMM_OK || skip) return st;
+  if (K > 0 && (reinterpret_cast<uintptr_t>(A) & 3u || reinterpret_cast<uintptr_t>(B) & 3u))
+    return GEMM_ERR_UNSUPPORTED_LAYOUT;  // fp32 elements must be 4-byte aligned
+  const DeviceInfo *dev = nullptr;
+  if ((st = current_device(&dev)) != GEMM_OK) return st;
+  if (K == 0) return from_cuda(dgr::launch_scale_f32(int(M), int(N), beta, C, ldc, stream));
+  return from_cuda(dgr::launch_gemm_tf32(*dev, int(M), int(N), int(K), alpha, A, lda, B, ldb,
+                                         beta, C, ldc, stream));
+}
+
+gemm_status_t gemm_f64(int64_t M, int64_t N, int64_t K, double alpha, const double *A,
+                       int64_t lda, const double *B, int64_t ldb, double beta, double *C,
+                       int64_t ldc, cudaStream_t stream) {
+  bool skip = false;
+  gemm_status_t st = check_args(M, N, K, A, lda, B, ldb, C, ldc, &skip);
+  if (st != GEMM_OK || skip) return st;
+  const DeviceInfo *dev = nullptr;
+  if ((st = current_device(&dev)) != GEMM_OK) return st;
+  if (K == 0) return from_cuda(dgr::launch_scale_f64(int(M), int(N), beta, C, ldc, stream));
+  return from_cuda(dgr::launch_dgemm(*dev, int(M), int(N), int(K), alpha, A, lda, B, ldb, beta, C,
+                                     ldc, stream));
 }
 
 static BatchOps make_ops(gemm_op_t opA, gemm_op_t opB, int64_t strideA, int64_t strideB,
@@ -389,6 +531,10 @@ gemm_status_t gemm_check_device_error(uint32_t *word) {
     return from_cuda(cudaErrorUnknown);
   if (word) *word = w;
   return (w & dgr::kErrTimeoutBit) ? GEMM_ERR_TIMEOUT : GEMM_OK;
+}
+
+const char *gemm_last_launch_error(void) {
+  return cudaGetErrorName(dgr::g_last_launch_error);
 }
 
 int gemm_version(void) { return dgr::kVersion; }

@@ -1,0 +1,257 @@
+// gemm_tc_int.cu -- exact 8-bit integer GEMM on the fp16 tensor pipe (int8 and
+// uint8 inputs, int32 C with wrap-around): each operand is widened to fp16 in
+// stream-ordered scratch memory (exact), then the tensor-core kernel
+// (gemm_tc_kernel.cuh) runs in exact-integer mode, restarting its fp32
+// accumulator every 1024 values of k so that every partial sum is an integer
+// of at most 2^24 in magnitude.
+//
+// uint8 runs on the same int8 kernel: with a = sa + 128 and b = sb + 128
+// (sa, sb in [-128, 127], exact in fp16 and the int8 kernel's range),
+//     sum_k a_ik b_kj = sum_k sa_ik sb_kj + 128 rowsum(A)_i + 128 colsum(B)_j
+//                       - 16384 K,
+// so the operands are widened as x - 128 and the epilogue adds
+// row_corr[i] = 128 rowsum(A)_i - 16384 K and col_corr[j] = 128 colsum(B)_j
+// (all modulo 2^32, like the result). A direct uint8 kernel would need
+// 256-value chunks (256 * 255^2 < 2^24 < 1024 * 255^2), four times as many
+// accumulator hand-offs to the epilogue.
+#include "gemm_tc_kernel.cuh"
+
+namespace dgr {
+namespace {
+
+// 8-bit -> fp16, exact, for a stack of `count` rows x cols matrices (source
+// matrix stride src_stride; destination matrices packed at rows * ldd). dst has
+// row stride ldd (multiple of 8) and its padding columns [cols, ldd) are
+// written with zeros. Each thread widens 16 consecutive elements of a row: one
+// 16-byte load when the source row is 16-byte aligned and the chunk is inside
+// the matrix, byte loads otherwise, and one or two 16-byte stores.
+// kOffset: uint8 values are stored as x - 128.
+template <typename T8, int kOffset = 0>
+__global__ void widen8_kernel(const T8 *__restrict__ src, int64_t lds, int64_t src_stride,
+                              __half *dst, int64_t ldd, int rows, int cols, int count,
+                              int vec_ok) {
+  const int64_t chunks_per_row = (ldd + 15) / 16;
+  const int64_t total = static_cast<int64_t>(rows) * count * chunks_per_row;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / chunks_per_row;  // row of the whole stack
+    const int c0 = static_cast<int>((i - r * chunks_per_row) * 16);
+    const int64_t m = r / rows;            // matrix of the stack
+    const T8 *s = src + m * src_stride + (r - m * rows) * lds;
+    __align__(16) __half h[16];
+    if (vec_ok && c0 + 16 <= cols) {
+      const int4 v = *reinterpret_cast<const int4 *>(s + c0);
+      const int w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        h[j] = __int2half_rn(
+            static_cast<int>(static_cast<T8>(static_cast<uint32_t>(w[j >> 2]) >> (8 * (j & 3)))) -
+            kOffset);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int c = c0 + j;
+        h[j] = __int2half_rn(c < cols ? static_cast<int>(s[c]) - kOffset : 0);
+      }
+    }
+    uint4 *d = reinterpret_cast<uint4 *>(dst + r * ldd + c0);
+    d[0] = *reinterpret_cast<const uint4 *>(h);
+    if (c0 + 16 <= ldd) d[1] = *reinterpret_cast<const uint4 *>(h + 8);
+  }
+}
+
+template <typename T8, int kOffset = 0>
+cudaError_t widen8(const DeviceInfo &dev, const T8 *src, int64_t lds, __half *dst, int64_t ldd,
+                   int rows, int cols, cudaStream_t stream, int count = 1,
+                   int64_t src_stride = 0) {
+  const int64_t total = static_cast<int64_t>(rows) * count * ((ldd + 15) / 16);
+  const int threads = 256;
+  int64_t blocks = (total + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(dev.sm_count) * 16;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  const int vec_ok = (reinterpret_cast<uintptr_t>(src) % 16 == 0) && (lds % 16 == 0) &&
+                     (count == 1 || src_stride % 16 == 0);
+  widen8_kernel<T8, kOffset><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+      src, lds, src_stride, dst, ldd, rows, cols, count, vec_ok);
+  return cudaGetLastError();
+}
+
+// The widened operands of an 8-bit GEMM in one scratch block: A's copies at
+// offset 0, B's at b_off (256-byte aligned); each copy packed (row stride
+// rounded up to 8 values, matrices back to back).
+struct WideLayout {
+  int a_rows, a_cols, b_rows, b_cols;  // stored shapes
+  int na, nb;                          // matrices widened per operand
+  int64_t lda16, ldb16, a_mat, b_mat;  // row and matrix strides of the copies (elements)
+  size_t b_off, total;                 // bytes
+
+  WideLayout(const BatchOps &ops, int M, int N, int K) {
+    a_rows = ops.a_t ? K : M;
+    a_cols = ops.a_t ? M : K;
+    b_rows = ops.b_t ? N : K;
+    b_cols = ops.b_t ? K : N;
+    na = (ops.batch > 1 && ops.stride_a != 0) ? ops.batch : 1;
+    nb = (ops.batch > 1 && ops.stride_b != 0) ? ops.batch : 1;
+    lda16 = (static_cast<int64_t>(a_cols) + 7) / 8 * 8;
+    ldb16 = (static_cast<int64_t>(b_cols) + 7) / 8 * 8;
+    a_mat = a_rows * lda16;
+    b_mat = b_rows * ldb16;
+    b_off = (static_cast<size_t>(na) * a_mat * 2 + 255) / 256 * 256;
+    total = b_off + static_cast<size_t>(nb) * b_mat * 2;
+  }
+};
+
+// Widens A and B into `scratch` and runs the exact-integer kernel of kind
+// kKind (kAllForms: built with every operand form).
+template <int kKind, bool kAllForms, typename T8>
+cudaError_t run_int(const DeviceInfo &dev, const BatchOps &ops, int M, int N, int K,
+                    int32_t alpha, const T8 *A, int64_t lda, const T8 *B, int64_t ldb,
+                    int32_t beta, int32_t *C, int64_t ldc, void *scratch, uint32_t *flags,
+                    size_t flags_words, cudaStream_t stream) {
+  const WideLayout w(ops, M, N, K);
+  __half *a16 = static_cast<__half *>(scratch);
+  __half *b16 = reinterpret_cast<__half *>(static_cast<uint8_t *>(scratch) + w.b_off);
+  cudaError_t e = widen8<T8>(dev, A, lda, a16, w.lda16, w.a_rows, w.a_cols, stream, w.na,
+                             ops.stride_a);
+  if (e == cudaSuccess)
+    e = widen8<T8>(dev, B, ldb, b16, w.ldb16, w.b_rows, w.b_cols, stream, w.nb, ops.stride_b);
+  if (e != cudaSuccess) return e;
+  // Short, wide int8 problems: the transposed-role kernel (1024-k chunks).
+  if (kKind == kKindS8 && M <= kSkinnyMaxM && ops.plain())
+    return launch_tc_skinny_int(dev, M, N, K, alpha, a16, w.lda16, b16, w.ldb16, beta, C, ldc,
+                                stream, flags, flags_words);
+  BatchOps wide = ops;
+  wide.stride_a = w.na > 1 ? w.a_mat : 0;
+  wide.stride_b = w.nb > 1 ? w.b_mat : 0;
+  return launch_tc<kKind, kAllForms>(dev, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, kFmtF16,
+                                     CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wide, M, N, K, alpha, a16,
+                                     w.lda16, b16, w.ldb16, beta, C, ldc, stream, flags,
+                                     flags_words);
+}
+
+// The same on scratch drawn from the library's stream-ordered pool and
+// returned to it on the same stream.
+template <int kKind, bool kAllForms, typename T8>
+cudaError_t run_int_pooled(const DeviceInfo &dev, const BatchOps &ops, int M, int N, int K,
+                           int32_t alpha, const T8 *A, int64_t lda, const T8 *B, int64_t ldb,
+                           int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream) {
+  const WideLayout w(ops, M, N, K);
+  cudaMemPool_t pool = nullptr;
+  cudaError_t e = device_pool(dev, &pool);
+  if (e != cudaSuccess) return e;
+  void *scratch = nullptr;
+  e = cudaMallocFromPoolAsync(&scratch, w.total, pool, stream);
+  if (e != cudaSuccess) return e;
+  e = run_int<kKind, kAllForms, T8>(dev, ops, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                                    scratch, nullptr, 0, stream);
+  cudaError_t f = cudaFreeAsync(scratch, stream);
+  return e != cudaSuccess ? e : f;
+}
+
+// row_corr[i] = 128 * sum_k A[i, k] - 16384 * K (mod 2^32): one warp per row,
+// lanes along k, a shuffle reduction.
+__global__ void u8_row_corr_kernel(const uint8_t *__restrict__ A, int64_t lda, int rows, int K,
+                                   int32_t *row_corr) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t r = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; r < rows;
+       r += warps) {
+    const uint8_t *row = A + r * lda;
+    uint32_t s = 0;
+    for (int k = lane; k < K; k += 32) s += row[k];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0)
+      row_corr[r] = static_cast<int32_t>(128u * s - 16384u * static_cast<uint32_t>(K));
+  }
+}
+
+// col_corr[j] += 128 * sum over this block's rows of B[k, j] (mod 2^32); col_corr
+// starts at zero. Threads along columns (coalesced rows), blocks along k.
+__global__ void u8_col_corr_kernel(const uint8_t *__restrict__ B, int64_t ldb, int K, int N,
+                                   int rows_per_block, int32_t *col_corr) {
+  const int64_t j = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  if (j >= N) return;
+  const int64_t k0 = static_cast<int64_t>(blockIdx.y) * rows_per_block;
+  const int64_t k1 = k0 + rows_per_block < K ? k0 + rows_per_block : K;
+  uint32_t s = 0;
+  for (int64_t k = k0; k < k1; ++k) s += B[k * ldb + j];
+  atomicAdd(reinterpret_cast<unsigned int *>(col_corr + j), 128u * s);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_s8(const DeviceInfo &dev, int M, int N, int K, int32_t alpha,
+                           const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
+                           int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream) {
+  return run_int_pooled<kKindS8, true, int8_t>(dev, BatchOps(), M, N, K, alpha, A, lda, B, ldb,
+                                                beta, C, ldc, stream);
+}
+
+cudaError_t launch_gemm_s8_ex(const DeviceInfo &dev, const BatchOps &ops, int M, int N, int K,
+                              int32_t alpha, const int8_t *A, int64_t lda, const int8_t *B,
+                              int64_t ldb, int32_t beta, int32_t *C, int64_t ldc,
+                              cudaStream_t stream) {
+  return run_int_pooled<kKindS8, true, int8_t>(dev, ops, M, N, K, alpha, A, lda, B, ldb, beta, C,
+                                                ldc, stream);
+}
+
+cudaError_t launch_gemm_u8(const DeviceInfo &dev, int M, int N, int K, int32_t alpha,
+                           const uint8_t *A, int64_t lda, const uint8_t *B, int64_t ldb,
+                           int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream) {
+  const WideLayout w(BatchOps(), M, N, K);
+  const size_t corr_off = (w.total + 255) / 256 * 256;
+  const size_t total = corr_off + (static_cast<size_t>(M) + N) * 4;
+  cudaMemPool_t pool = nullptr;
+  cudaError_t e = device_pool(dev, &pool);
+  if (e != cudaSuccess) return e;
+  void *scratch = nullptr;
+  e = cudaMallocFromPoolAsync(&scratch, total, pool, stream);
+  if (e != cudaSuccess) return e;
+  __half *a16 = static_cast<__half *>(scratch);
+  __half *b16 = reinterpret_cast<__half *>(static_cast<uint8_t *>(scratch) + w.b_off);
+  int32_t *row_corr = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(scratch) + corr_off);
+  int32_t *col_corr = row_corr + M;
+  e = widen8<uint8_t, 128>(dev, A, lda, a16, w.lda16, M, K, stream);
+  if (e == cudaSuccess) e = widen8<uint8_t, 128>(dev, B, ldb, b16, w.ldb16, K, N, stream);
+  if (e == cudaSuccess) {
+    int64_t blocks = (static_cast<int64_t>(M) * 32 + 255) / 256;
+    if (blocks > dev.sm_count * 8) blocks = dev.sm_count * 8;
+    u8_row_corr_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(A, lda, M, K,
+                                                                          row_corr);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = cudaMemsetAsync(col_corr, 0, static_cast<size_t>(N) * 4, stream);
+  if (e == cudaSuccess) {
+    int rows_per_block = 256;
+    if ((K + rows_per_block - 1) / rows_per_block > 65535) rows_per_block = (K + 65534) / 65535;
+    const dim3 grid(static_cast<unsigned>((N + 255) / 256),
+                    static_cast<unsigned>((K + rows_per_block - 1) / rows_per_block));
+    u8_col_corr_kernel<<<grid, 256, 0, stream>>>(B, ldb, K, N, rows_per_block, col_corr);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess)
+    e = launch_tc<kKindS8, true>(dev, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, kFmtF16,
+                                 CU_TENSOR_MAP_DATA_TYPE_FLOAT16, BatchOps(), M, N, K, alpha, a16,
+                                 w.lda16, b16, w.ldb16, beta, C, ldc, stream, nullptr, 0,
+                                 row_corr, col_corr);
+  cudaError_t f = cudaFreeAsync(scratch, stream);
+  return e != cudaSuccess ? e : f;
+}
+
+// The int8 path with scratch memory supplied by the caller instead of drawn
+// from the library's pool: widen A and B into `scratch` (which must hold
+// s8_scratch_bytes(M, N, K) bytes, 256-byte aligned) and run the tensor-core
+// kernel in exact-integer mode. Allocates nothing.
+size_t s8_scratch_bytes(int M, int N, int K) { return WideLayout(BatchOps(), M, N, K).total; }
+
+cudaError_t launch_gemm_s8_scratch(const DeviceInfo &dev, int M, int N, int K, int32_t alpha,
+                                   const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
+                                   int32_t beta, int32_t *C, int64_t ldc, void *scratch,
+                                   uint32_t *flags, size_t flags_words, cudaStream_t stream) {
+  return run_int<kKindS8, true, int8_t>(dev, BatchOps(), M, N, K, alpha, A, lda, B, ldb, beta, C,
+                                         ldc, scratch, flags, flags_words, stream);
+}
+
+}  // namespace dgr

@@ -1,55 +1,70 @@
-// gemm_tc.cu -- tensor-core GEMM for sm_103a: tcgen05.mma with the
-// accumulator in tensor memory (TMEM), operands staged by TMA.
+// gemm_tc_kernel.cuh -- the tensor-core GEMM kernel for sm_103a and its host
+// launcher, shared by the translation units that instantiate it (one per
+// element kind, compiled in parallel):
 //
 //     C = alpha * op(A) * op(B) + beta * C      op(A): M x K, op(B): K x N,
 //                                                C: M x N, all row-major
 //
+// tcgen05.mma with the accumulator in tensor memory (TMEM), operands staged by
+// TMA. Element kinds (TcKind below):
+//   * 16-bit inputs (bf16 or fp16), fp32 accumulation, fp32 C;
+//   * the same with a 16-bit C of the inputs' format (fp32 accumulation, one
+//     round-to-nearest-even at the end);
+//   * exact int32 C from integer-valued fp16 operands (the int8 and uint8
+//     paths). An int8 value is exact in fp16 and a product of two is exact in
+//     fp32; a sum of at most 1024 such products (each at most 2^14 in
+//     magnitude) is an integer of at most 2^24, which fp32 holds exactly. The
+//     kernel therefore restarts the fp32 accumulator every 1024 values of k,
+//     and the epilogue adds each finished partial sum into int32 registers
+//     (wrap-around). uint8 operands arrive offset by -128 (int8 range), and
+//     the epilogue adds the exact correction row_corr[i] + col_corr[j] once;
+//   * fp32 inputs used at tf32 precision (kind::tf32), fp32 C; both operands
+//     are staged K-major.
+//
 // op(X) is X as stored or its transpose, and the problem may be a stack of
 // `batch` such GEMMs at fixed element strides (strided-batched GEMM). Neither
 // costs anything on this path: a transposed operand is staged by TMA in the
-// other major order and the MMA's descriptors say so; the batch index is the
-// third coordinate of every tensor map and one more dimension of the tile
-// list.
-//
-// 16-bit inputs (bf16 or fp16), fp32 accumulation, and either
-//   * fp32 output (gemm_bf16 / gemm_f16), or
-//   * exact int32 output from integer-valued fp16 operands (the int8 path: an
-//     int8 value is exact in fp16, a product of two is at most 2^14 in
-//     magnitude, and a sum of at most 1024 such products is an integer of at
-//     most 2^24 in magnitude, which fp32 represents exactly. The kernel
-//     therefore restarts the fp32 accumulator every 1024 values of k, and the
-//     epilogue adds each finished partial sum into int32 registers).
+// other major order and the MMA's descriptors say so (the form is a template
+// parameter, so each loop is compiled for one layout); the batch index is the
+// third coordinate of every tensor map and one more dimension of the tile list.
 //
 // Sources: C++ warp-matrix-function page (D = A*B + C on tensor cores; type
-// table: half / bfloat16 inputs with float accumulate, signed char inputs with
-// int accumulate); "Sgemm [128,128,8]" (C = alpha*A*B + beta*C, row-major, the
+// table: half / bfloat16 inputs with float accumulate, half -> half, signed and
+// unsigned char inputs with int accumulate, precision::tf32 with float
+// accumulate); "Sgemm [128,128,8]" (C = alpha*A*B + beta*C, row-major, the
 // alpha/beta epilogue); "使用CUDA和瓦片算法计算矩阵乘法" (residual tiles act as
 // zeros: here the TMA unit fills out-of-range elements with zeros).
 //
-// Structure (one CTA per SM, persistent):
-//   warp 0      one thread issues TMA loads of A (128 x 64, K-major, 128-byte
-//               swizzle) and B (64 x 256 as four 64 x 64 boxes, N-major,
-//               128-byte swizzle) into a kStages-deep ring guarded by
-//               full/empty mbarriers. A stored transposed (K x M) arrives as
-//               two 64(M) x 64(K) M-major boxes; B stored transposed (N x K)
-//               as one 256(N) x 64(K) K-major box. Every layout fills the same
-//               bytes per stage.
-//   warp 1      allocates 512 TMEM columns; one thread issues
-//               tcgen05.mma.cta_group::1.kind::f16 (M=128, N=256, K=16) into
-//               one of two 256-column accumulators and commits each stage's
-//               completion to that stage's empty barrier.
+// Structure (one CTA per SM, or one CTA pair per two SMs, persistent):
+//   warp 0      one thread issues TMA loads of A (128 rows x 128 bytes of k,
+//               K-major, 128-byte swizzle) and B (128 bytes of k x 256 columns,
+//               N-major, as boxes 128 bytes wide) into a kStages-deep ring
+//               guarded by full/empty mbarriers. A stored transposed (K x M)
+//               arrives as M-major boxes; B stored transposed (N x K) as one
+//               256(n) x 128-byte(k) K-major box. Every layout and element size
+//               fills the same bytes per stage.
+//   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma
+//               (M = 128, or 256 on a CTA pair; N = 256) into one of two
+//               256-column accumulators and commits each stage's completion to
+//               that stage's empty barrier.
 //   warps 2..9  epilogue: tcgen05.ld of the finished accumulator (each warp
 //               reads its 32-lane quarter and one 128-column half), then
-//               alpha/beta and guarded stores to C. The two accumulators let
-//               the epilogue of one tile overlap the main loop of the next.
+//               alpha/beta and TMA (or guarded plain) stores to C. The two
+//               accumulators let the epilogue of one tile overlap the main loop
+//               of the next.
 // Tiles are visited in groups of kGroupM tile rows so that the CTAs resident
 // at one time share A rows and B columns in L2.
+#pragma once
+
 #include <cstdint>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <type_traits>
+#include <utility>
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -59,9 +74,6 @@
 namespace dgr {
 namespace {
 
-#ifndef DGR_TC_BK
-#define DGR_TC_BK 64
-#endif
 #ifndef DGR_TC_STAGES
 #define DGR_TC_STAGES 4
 #endif
@@ -77,23 +89,42 @@ namespace {
 #ifndef DGR_TC_PAIR
 #define DGR_TC_PAIR 1
 #endif
+#ifndef DGR_TC_MAX_SPLIT
+#define DGR_TC_MAX_SPLIT 4
+#endif
 
-// k-block: 64 16-bit values (one 128-byte swizzle row of A) or 32 (64-byte rows).
-constexpr int kBK = DGR_TC_BK;
-static_assert(kBK == 64 || kBK == 32, "k-block of 32 or 64 values");
+// Element kinds of one instantiation.
+constexpr int kKindF32 = 0;      // bf16 / fp16 in, fp32 C
+constexpr int kKindS8 = 1;       // int8 (or offset uint8) widened to fp16, exact int32 C
+constexpr int kKindF16Out = 3;   // fp16 in, fp16 C
+constexpr int kKindBF16Out = 4;  // bf16 in, bf16 C
+constexpr int kKindTF32 = 5;     // fp32 in at tf32 precision, fp32 C
+
+template <int kKind>
+struct TcKind {
+  static constexpr int kInBytes = kKind == kKindTF32 ? 4 : 2;
+  static constexpr bool kInt = kKind == kKindS8;
+  static constexpr bool kOut16 = kKind == kKindF16Out || kKind == kKindBF16Out;
+  // exact-int mode: values of k per fp32 chunk (sums stay within 2^24)
+  static constexpr int kChunkK = kKind == kKindS8 ? 1024 : 0;
+  using Out = typename std::conditional<
+      kInt, int32_t, typename std::conditional<kOut16, uint16_t, float>::type>::type;
+  using Scale = typename std::conditional<kInt, int32_t, float>::type;  // alpha, beta
+  // k per stage: one 128-byte swizzle row of a K-major operand
+  static constexpr int kBK = 128 / kInBytes;
+  // k per MMA instruction: 32 bytes
+  static constexpr int kMmaK = 32 / kInBytes;
+  // values of m or n in one 128-byte row of an MN-major box
+  static constexpr int kMNElems = 128 / kInBytes;
+};
+
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
-// int mode: k-blocks per exact fp32 chunk (1024 values of k)
-constexpr int kChunkKB = 1024 / kBK;
 constexpr uint32_t kTmemCols = 512;  // two 256-column fp32 accumulators
 constexpr int kBN = 256;             // tile columns (MMA N)
 constexpr int kBM = 128;             // tile rows held by one CTA (TMEM lanes)
-
-// A rows are kBK * 2 bytes long: 128-byte swizzle for 64 values, 64-byte for 32.
-constexpr uint32_t kARowBytes = kBK * 2;
-constexpr uint32_t kASwizzleMode = kBK == 64 ? 2u : 4u;   // descriptor encoding
-constexpr uint32_t kAAtomBytes = 8 * kARowBytes;          // 8-row swizzle atom
-constexpr uint32_t kMNBoxBytes = 64 * kBK * 2;            // any 64(M or N) x kBK MN-major box
+constexpr uint32_t kRowBytes = 128;  // one swizzle row
+constexpr uint32_t kAtomBytes = 8 * kRowBytes;  // 8-row swizzle atom (SBO)
 
 // Single CTA: 128 x 256 tile, the CTA stages all 256 columns of B.
 // CTA pair:   256 x 256 tile, each CTA stages its 128 rows of A and its 128
@@ -103,17 +134,16 @@ struct Cfg {
   static constexpr int kTileM = kPair ? 256 : 128;
   static constexpr int kBNLoad = kPair ? 128 : 256;   // B columns staged per CTA
   static constexpr int kStages = kPair ? DGR_TC_STAGES_PAIR : DGR_TC_STAGES;
-  // Tiles are visited in groups of kGroupM tile rows so that the CTAs resident
-  // at one time share A rows and B columns in L2.
   static constexpr int kGroupM = kPair ? DGR_TC_GROUP_M_PAIR : DGR_TC_GROUP_M;
-  static constexpr uint32_t kABytes = kBM * kBK * 2;
-  static constexpr uint32_t kBBytes = kBK * kBNLoad * 2;
+  static constexpr uint32_t kABytes = kBM * kRowBytes;
+  static constexpr uint32_t kBBytes = kBNLoad * kRowBytes;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;           // per CTA
   static constexpr uint32_t kTxBytes = kStageBytes * (kPair ? 2 : 1);  // per full phase
 };
 
-// Epilogue staging: one 32 x 32 x 4-byte block of C per epilogue warp, in the
-// 128-byte-swizzled layout of the C tensor map's box.
+// Epilogue staging: one 32-row x 128-byte block of C per epilogue warp (32 x
+// 32 fp32/int32 values or 32 x 64 16-bit values), in the 128-byte-swizzled
+// layout of the C tensor map's box.
 constexpr uint32_t kStageCBytes = 32 * 128;
 
 template <bool kPair>
@@ -130,18 +160,31 @@ struct __align__(1024) TcSmem {
   int abort;
 };
 
+// Exact-int kinds only: optional exact per-row and per-column terms added to
+// the product before alpha/beta (the uint8 path's offset correction). A base
+// that is empty for the other kinds: the fp32 kernels' code generation is
+// sensitive to the size of their argument block (two more pointers there
+// cost them 35 registers and spills).
 template <bool kInt>
-struct TcArgs {
-  using Out = typename std::conditional<kInt, int32_t, float>::type;
+struct TcCorr {};
+template <>
+struct TcCorr<true> {
+  const int32_t *row_corr, *col_corr;
+};
+
+template <int kKind>
+struct TcArgs : TcCorr<TcKind<kKind>::kInt> {
+  using Out = typename TcKind<kKind>::Out;
+  using Scale = typename TcKind<kKind>::Scale;
   int M, N, K;
-  Out alpha, beta;
+  Scale alpha, beta;
   Out *C;
   int64_t ldc;
   int tiles_m, tiles_n;
-  int tiles_per_batch;   // tiles_m * tiles_n; tile t is tile t % this of matrix t / this
+  int tiles_per_batch;       // tiles_m * tiles_n; tile t is tile t % this of matrix t / this
   int a_batched, b_batched;  // the operand's tensor map has one matrix per batch entry
-  int64_t stride_c;      // elements between consecutive C matrices
-  int c_vec_ok;  // C 16-byte aligned and ldc % 4 == 0
+  int64_t stride_c;          // elements between consecutive C matrices
+  int c_vec_ok;  // C 16-byte aligned and rows a whole number of 16-byte units apart
   int c_tma;     // the epilogue writes C through the C tensor map (needs c_vec_ok)
   uint32_t idesc;
   uint32_t *err_word;
@@ -160,8 +203,7 @@ struct WorkItem {
 };
 
 // Item n of unit u's work list (false past its end). kb_unit is the k
-// granularity of split points: 1 k-block, or one exact 1024-k chunk in int
-// mode.
+// granularity of split points: 1 k-block, or one exact chunk in int mode.
 __device__ __forceinline__ bool get_work(int u, int n, int units, int dp_tiles, int tail_tiles,
                                          int split, int KB, int kb_unit, WorkItem &w) {
   const int dp_per_unit = dp_tiles / units;
@@ -232,8 +274,8 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
 // Tile t of a batched problem: batch entry bt, tile (tm, tn) within it. The
 // tiles of one matrix are contiguous in t, so the resident CTAs work on one or
 // two matrices at a time and the grouped raster's L2 reuse holds within each.
-template <int kGroupM, bool kInt>
-__device__ __forceinline__ void batch_tile_coords(int t, const TcArgs<kInt> &p, int &bt, int &tm,
+template <int kGroupM, int kKind>
+__device__ __forceinline__ void batch_tile_coords(int t, const TcArgs<kKind> &p, int &bt, int &tm,
                                                   int &tn) {
   bt = t / p.tiles_per_batch;
   tile_coords<kGroupM>(t - bt * p.tiles_per_batch, p.tiles_m, p.tiles_n, tm, tn);
@@ -259,16 +301,36 @@ __device__ __forceinline__ int32_t scale_add(int32_t alpha, int32_t acc, int32_t
   return static_cast<int32_t>(r);
 }
 
-// C[row, col .. col+31] = alpha * v + beta * C (the C term only when use_c).
-// C is read through L2 (another SM may have just written it).
-template <bool kInt>
-__device__ __forceinline__ void store_row_chunk(const TcArgs<kInt> &p,
-                                                typename TcArgs<kInt>::Out *C, int row, int col,
-                                                const typename TcArgs<kInt>::Out (&v)[32],
-                                                typename TcArgs<kInt>::Out beta, bool use_c) {
-  using Out = typename TcArgs<kInt>::Out;
+// 16-bit C of kind kKind: the stored bits <-> float (exact widening; one
+// round-to-nearest-even narrowing).
+template <int kKind>
+__device__ __forceinline__ float out16_to_float(uint16_t h) {
+  if constexpr (kKind == kKindBF16Out) {
+    return __bfloat162float(__ushort_as_bfloat16(h));
+  } else {
+    return __half2float(__ushort_as_half(h));
+  }
+}
+template <int kKind>
+__device__ __forceinline__ uint16_t float_to_out16(float v) {
+  if constexpr (kKind == kKindBF16Out) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  } else {
+    return __half_as_ushort(__float2half_rn(v));
+  }
+}
+
+// C[row, col .. col+31] = alpha * v + beta * C (the C term only when use_c),
+// fp32 or int32 C. C is read through L2 (another SM may have just written it).
+template <int kKind>
+__device__ __forceinline__ void store_row_chunk(const TcArgs<kKind> &p,
+                                                typename TcArgs<kKind>::Out *C, int row, int col,
+                                                const typename TcArgs<kKind>::Scale (&v)[32],
+                                                typename TcArgs<kKind>::Scale beta, bool use_c) {
+  using Out = typename TcArgs<kKind>::Out;
+  constexpr bool kInt = TcKind<kKind>::kInt;
   Out *crow = C + static_cast<int64_t>(row) * p.ldc;
-  const Out alpha = p.alpha;
+  const auto alpha = p.alpha;
   if (p.c_vec_ok && col + 31 < p.N) {
     using Vec = typename std::conditional<kInt, int4, float4>::type;
 #pragma unroll
@@ -293,9 +355,25 @@ __device__ __forceinline__ void store_row_chunk(const TcArgs<kInt> &p,
   }
 }
 
-// Writes one 32 x 32 block of C matrix z (rows y .. y+31, columns x .. x+31;
-// the lane's row is y + lane) from registers: stages it in the warp's swizzled
-// buffer and issues one TMA store, or one TMA reduce-add when `addto`
+// 16-bit C: already-final values h[0..31] for C[row, col .. col+31].
+template <int kKind>
+__device__ __forceinline__ void store_row_chunk16(const TcArgs<kKind> &p, uint16_t *C, int row,
+                                                  int col, const uint32_t (&h)[16]) {
+  uint16_t *crow = C + static_cast<int64_t>(row) * p.ldc;
+  if (p.c_vec_ok && col + 31 < p.N) {
+#pragma unroll
+    for (int j = 0; j < 16; j += 4)
+      *reinterpret_cast<uint4 *>(crow + col + 2 * j) = make_uint4(h[j], h[j + 1], h[j + 2], h[j + 3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (col + j < p.N) crow[col + j] = static_cast<uint16_t>(h[j >> 1] >> (16 * (j & 1)));
+  }
+}
+
+// Writes one 32-row x 128-byte block of C matrix z (rows y .. y+31, columns
+// from x; the lane's row is y + lane) from registers: stages it in the warp's
+// swizzled buffer and issues one TMA store, or one TMA reduce-add when `addto`
 // (C += block). Elements outside C are dropped by the tensor map's bounds.
 __device__ __forceinline__ void tma_write_block(uint32_t stage, const void *tmC, int x, int y,
                                                 int z, int M, int N, const uint32_t (&w)[32],
@@ -319,14 +397,43 @@ __device__ __forceinline__ void tma_write_block(uint32_t stage, const void *tmC,
   }
 }
 
-// kAT / kBT: A stored K x M / B stored N x K (used transposed).
-template <bool kInt, bool kPair, bool kAT, bool kBT>
-__global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const TcArgs<kInt> p) {
+template <int kKind, bool kPair>
+__device__ __forceinline__ void issue_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t acc) {
+  if constexpr (kKind == kKindTF32) {
+    if constexpr (kPair) {
+      tc_mma_tf32_pair(d, a, b, idesc, acc);
+    } else {
+      tc_mma_tf32(d, a, b, idesc, acc);
+    }
+  } else {
+    if constexpr (kPair) {
+      tc_mma_f16_pair(d, a, b, idesc, acc);
+    } else {
+      tc_mma_f16(d, a, b, idesc, acc);
+    }
+  }
+}
+
+// The kernel body. kAT / kBT: A stored K x M / B stored N x K (used
+// transposed). The tensor maps are the kernel's grid-constant parameters,
+// passed by reference so that TMA reads them in parameter space.
+template <int kKind, bool kPair, bool kAT, bool kBT>
+__device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tmA, const CUtensorMap &tmB,
+                                             const CUtensorMap &tmC, const TcArgs<kKind> p) {
+  using K_ = TcKind<kKind>;
   using Cf = Cfg<kPair>;
-  using Out = typename TcArgs<kInt>::Out;
+  using Out = typename K_::Out;
+  using Scale = typename K_::Scale;
+  constexpr bool kInt = K_::kInt;
+  constexpr bool kOut16 = K_::kOut16;
+  constexpr int kBK = K_::kBK;
   constexpr int kStages = Cf::kStages;
+  // A box of kMNElems values of m or n by kBK rows of k (MN-major operands).
+  constexpr uint32_t kMNBoxBytes = kRowBytes * kBK;
+  // kMmaK rows of an MN-major operand: the step between MMAs along k.
+  constexpr uint32_t kMNStep = kRowBytes * K_::kMmaK;
+  static_assert(kKind != kKindTF32 || (!kAT && kBT), "tf32 operands are staged K-major");
   extern __shared__ uint8_t smem_raw[];
   // Swizzled TMA destinations need 1024-byte alignment. The offset is the same
   // in both CTAs of a pair, which the pair MMA relies on.
@@ -377,7 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = sm.tmem_base;
 
   const int KB = (p.K + kBK - 1) / kBK;
-  // int mode: exact fp32 chunks of 1024 k; float mode: one chunk per item
+  // int mode: exact fp32 chunks of kChunkK values of k; float mode: one chunk per item
+  constexpr int kChunkKB = kInt ? K_::kChunkK / kBK : 1;
   const int chunk_kb = kInt ? kChunkKB : KB;
   const int kb_unit = kInt ? kChunkKB : 1;
   WorkItem wi;
@@ -419,13 +527,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             load(smem_u32(sm.a[stage]), &tmA, k0, m0, za);  // 128 rows x kBK, K-major
           } else {
 #pragma unroll
-            for (int j = 0; j < kBM / 64; ++j)  // kBK rows of k x 64 values of m, twice
-              load(smem_u32(sm.a[stage] + j * kMNBoxBytes), &tmA, m0 + 64 * j, k0, za);
+            for (int j = 0; j < kBM / K_::kMNElems; ++j)  // kBK rows of k x kMNElems of m
+              load(smem_u32(sm.a[stage] + j * kMNBoxBytes), &tmA, m0 + K_::kMNElems * j, k0, za);
           }
           if constexpr (!kBT) {
 #pragma unroll
-            for (int j = 0; j < Cf::kBNLoad / 64; ++j)  // kBK rows of k x 64 values of n
-              load(smem_u32(sm.b[stage] + j * kMNBoxBytes), &tmB, nb + 64 * j, k0, zb);
+            for (int j = 0; j < Cf::kBNLoad / K_::kMNElems; ++j)  // kBK rows of k x kMNElems of n
+              load(smem_u32(sm.b[stage] + j * kMNBoxBytes), &tmB, nb + K_::kMNElems * j, k0, zb);
           } else {
             load(smem_u32(sm.b[stage]), &tmB, k0, nb, zb);  // kBNLoad rows x kBK, K-major
           }
@@ -483,24 +591,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t a_addr = smem_u32(sm.a[stage]);
             const uint32_t b_addr = smem_u32(sm.b[stage]);
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-              // K-major operand: swizzled rows of kBK values; 16 values of k =
-              // 32 B further along the row; SBO = one 8-row swizzle atom.
-              // MN-major operand: 128-byte swizzled rows of 64 values of m or n,
-              // one row per k; 16 values of k = 16 * 128 B further; LBO = one
-              // 64-value box, SBO = 1 KiB between groups of 8 k-rows.
+            for (int kk = 0; kk < kBK / K_::kMmaK; ++kk) {
+              // K-major operand: 128-byte swizzled rows of k; one MMA's k is 32 B
+              // further along the row; SBO = one 8-row swizzle atom.
+              // MN-major operand: 128-byte swizzled rows of m or n, one row per
+              // k; one MMA's k is kMmaK rows further; LBO = one box of
+              // kMNElems values, SBO = 1 KiB between groups of 8 k-rows.
               const uint64_t adesc =
-                  kAT ? smem_desc(a_addr + kk * 2048, kMNBoxBytes, 1024, 2u)
-                      : smem_desc(a_addr + kk * 32, 16, kAAtomBytes, kASwizzleMode);
+                  kAT ? smem_desc(a_addr + kk * kMNStep, kMNBoxBytes, kAtomBytes, 2u)
+                      : smem_desc(a_addr + kk * 32, 16, kAtomBytes, 2u);
               const uint64_t bdesc =
-                  kBT ? smem_desc(b_addr + kk * 32, 16, kAAtomBytes, kASwizzleMode)
-                      : smem_desc(b_addr + kk * 2048, kMNBoxBytes, 1024, 2u);
+                  kBT ? smem_desc(b_addr + kk * 32, 16, kAtomBytes, 2u)
+                      : smem_desc(b_addr + kk * kMNStep, kMNBoxBytes, kAtomBytes, 2u);
               const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
-              if constexpr (kPair) {
-                tc_mma_f16_pair(d_tmem, adesc, bdesc, p.idesc, acc);
-              } else {
-                tc_mma_f16(d_tmem, adesc, bdesc, p.idesc, acc);
-              }
+              issue_mma<kKind, kPair>(d_tmem, adesc, bdesc, p.idesc, acc);
             }
             any = true;
             // This stage's shared memory is free again in both CTAs.
@@ -553,8 +657,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Part 0 (or a whole tile) applies beta to the old C; a later part adds
       // its partial product to what the previous part stored.
       const bool addto = wi.part > 0;
-      const Out beta = addto ? Out(1) : p.beta;
-      const bool use_c = addto || p.beta != Out(0);
+      const Scale beta = addto ? Scale(1) : p.beta;
+      const bool use_c = addto || p.beta != Scale(0);
       uint32_t *flag = nullptr;
       if (wi.parts > 1)
         flag = p.tail_flags + (wi.tile - p.dp_tiles) * 2 + static_cast<int>(rank);
@@ -564,8 +668,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       uint32_t acc[kInt ? 128 : 1];  // int mode: running int32 sums (wrap-around)
       if constexpr (kInt) {
+        // The sums start at the offset correction row_corr + col_corr (part 0
+        // of a tile only), else at zero.
+        if (p.row_corr != nullptr && !addto && row < p.M) {
+          const uint32_t rc = static_cast<uint32_t>(__ldg(p.row_corr + row));
 #pragma unroll
-        for (int j = 0; j < 128; ++j) acc[j] = 0;
+          for (int j = 0; j < 128; ++j)
+            acc[j] = col0 + j < p.N ? rc + static_cast<uint32_t>(__ldg(p.col_corr + col0 + j)) : 0u;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 128; ++j) acc[j] = 0;
+        }
       }
       for (int kb0 = wi.kb0; kb0 < wi.kb1; kb0 += chunk_kb) {
         const uint32_t buf = chunk & 1u, use = (chunk >> 1) & 1u;
@@ -578,6 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!got) break;
         tc_fence_after_sync();
         const uint32_t taddr = tmem_base + lane_base + buf * kBN + col_half * 128;
+        [[maybe_unused]] uint32_t w16[32];  // 16-bit C: 64 packed values (one TMA block)
 #pragma unroll
         for (int c = 0; c < 128; c += 32) {
           uint32_t r[32];
@@ -587,6 +701,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j)
               acc[c + j] += static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[j])));
+          } else if constexpr (kOut16) {
+            // alpha * acc + beta * C in fp32, then one rounding to 16 bits
+            if (!*abort) {
+              const bool read_c = use_c && row < p.M;
+              const uint16_t *crow = Cb + static_cast<int64_t>(row) * p.ldc + col0 + c;
+              uint32_t h[16];
+#pragma unroll
+              for (int j = 0; j < 32; j += 2) {
+                const float c0 = (read_c && col0 + c + j < p.N)
+                                     ? out16_to_float<kKind>(__ldcg(crow + j)) : 0.f;
+                const float c1 = (read_c && col0 + c + j + 1 < p.N)
+                                     ? out16_to_float<kKind>(__ldcg(crow + j + 1)) : 0.f;
+                const uint32_t lo = float_to_out16<kKind>(
+                    scale_add(p.alpha, __uint_as_float(r[j]), beta, c0, read_c));
+                const uint32_t hi = float_to_out16<kKind>(
+                    scale_add(p.alpha, __uint_as_float(r[j + 1]), beta, c1, read_c));
+                h[j >> 1] = lo | (hi << 16);
+              }
+              if (p.c_tma) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) w16[(c & 32) / 2 + j] = h[j];
+                if (c & 32)
+                  tma_write_block(smem_u32(sm.stage_c[e]), &tmC, col0 + c - 32, row - lane, bt,
+                                  p.M, p.N, w16, false, lane);
+              } else if (row < p.M) {
+                store_row_chunk16<kKind>(p, Cb, row, col0 + c, h);
+              }
+            }
           } else if (p.c_tma) {
             if (!*abort) {
               uint32_t w[32];
@@ -606,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               float v[32];
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-              store_row_chunk<kInt>(p, Cb, row, col0 + c, v, beta, use_c);
+              store_row_chunk<kKind>(p, Cb, row, col0 + c, v, beta, use_c);
             }
           }
         }
@@ -644,7 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int32_t v[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = static_cast<int32_t>(acc[c + j]);
-            store_row_chunk<kInt>(p, Cb, row, col0 + c, v, beta, use_c);
+            store_row_chunk<kKind>(p, Cb, row, col0 + c, v, beta, use_c);
           }
         }
       }
@@ -680,6 +822,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+template <int kKind, bool kPair, bool kAT, bool kBT>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const TcArgs<kKind> p) {
+  gemm_tc_body<kKind, kPair, kAT, kBT>(tmA, tmB, tmC, p);
+}
+
 // ------------------------------------------------------------------ host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -687,7 +836,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-EncodeTiledFn get_encode_fn() {
+inline EncodeTiledFn get_encode_fn() {
   static std::once_flag once;
   static EncodeTiledFn fn = nullptr;
   std::call_once(once, [] {
@@ -703,77 +852,45 @@ EncodeTiledFn get_encode_fn() {
 
 // Stride in bytes between the matrices of a stack: the caller's stride, or,
 // for a single matrix, any legal value (the third coordinate is always 0).
-cuuint64_t matrix_stride_bytes(int64_t count, int64_t stride, int64_t rows, int64_t ld,
-                               int esize) {
+inline cuuint64_t matrix_stride_bytes(int64_t count, int64_t stride, int64_t rows, int64_t ld,
+                                      int esize) {
   if (count > 1) return static_cast<cuuint64_t>(stride) * esize;
   return (static_cast<cuuint64_t>(rows) * ld * esize + 15) / 16 * 16;
 }
 
-// A stack of `count` row-major rows x cols matrices of 16-bit elements, row
-// stride ld and matrix stride `stride` (elements), in boxes of box_rows x
-// box_cols elements; the swizzle spans one box row (box_cols * 2 bytes: 128
-// or 64).
-bool make_tmap(CUtensorMap *tm, CUtensorMapDataType dt, const void *base, int64_t rows,
-               int64_t cols, int64_t ld, int64_t count, int64_t stride, uint32_t box_rows,
-               uint32_t box_cols) {
+// A stack of `count` row-major rows x cols matrices (element size esize, row
+// stride ld and matrix stride `stride` in elements), in boxes of box_rows x
+// box_cols elements with 128-byte swizzle (a box row is 128 bytes).
+inline bool make_tmap(CUtensorMap *tm, CUtensorMapDataType dt, int esize, const void *base,
+                      int64_t rows, int64_t cols, int64_t ld, int64_t count, int64_t stride,
+                      uint32_t box_rows, uint32_t box_cols, bool l2_promote = true) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
                         static_cast<cuuint64_t>(count)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2,
-                           matrix_stride_bytes(count, stride, rows, ld, 2)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * esize,
+                           matrix_stride_bytes(count, stride, rows, ld, esize)};
   cuuint32_t box[3] = {box_cols, box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(tm, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-// C (a stack of `count` row-major rows x cols matrices, 4-byte elements, row
-// stride ld, matrix stride `stride`) in boxes of 32 x 32 elements with 128-byte
-// swizzle, for the epilogue's TMA stores and reduces.
-bool make_tmap_c(CUtensorMap *tm, bool is_int, const void *base, int64_t rows, int64_t cols,
-                 int64_t ld, int64_t count, int64_t stride) {
-  EncodeTiledFn enc = get_encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
-                        static_cast<cuuint64_t>(count)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 4,
-                           matrix_stride_bytes(count, stride, rows, ld, 4)};
-  cuuint32_t box[3] = {32, 32, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(tm, is_int ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                   3, const_cast<void *>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   l2_promote ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                              : CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
-}
-
-// The kernel for an operand form.
-template <bool kInt, bool kPair>
-auto tc_kernel_for(bool a_t, bool b_t) -> decltype(&gemm_tc_kernel<kInt, kPair, false, false>) {
-  if (a_t)
-    return b_t ? gemm_tc_kernel<kInt, kPair, true, true> : gemm_tc_kernel<kInt, kPair, true, false>;
-  return b_t ? gemm_tc_kernel<kInt, kPair, false, true>
-             : gemm_tc_kernel<kInt, kPair, false, false>;
 }
 
 // Co-resident CTA pairs for a pair kernel on this device (0 if pairs are not
 // available), queried once per device and kernel.
-template <bool kInt>
-int pair_capacity(const DeviceInfo &dev, size_t smem) {
+inline int pair_capacity(const DeviceInfo &dev, const void *kern, size_t smem) {
   static std::mutex mu;
-  static int cache[64];
-  static bool known[64] = {};
+  static std::map<std::pair<const void *, int>, int> cache;
   std::lock_guard<std::mutex> lock(mu);
-  if (dev.device < 0 || dev.device >= 64) return 0;
-  if (known[dev.device]) return cache[dev.device];
-  auto kern = gemm_tc_kernel<kInt, true, false, false>;
+  const auto key = std::make_pair(kern, dev.device);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
   int n = 0;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem)) == cudaSuccess) {
+  if (set_max_dynamic_smem(kern, static_cast<int>(smem), dev.device) == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * static_cast<unsigned>(dev.sm_count / 2), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -788,51 +905,18 @@ int pair_capacity(const DeviceInfo &dev, size_t smem) {
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
   }
   cudaGetLastError();
-  cache[dev.device] = n;
-  known[dev.device] = true;
+  cache[key] = n;
   return n;
 }
 
-}  // namespace
-
-// Library-owned stream-ordered memory pool of a device (scratch for the int8
-// path and the split-k tail flags); freed blocks stay mapped for reuse.
-cudaError_t device_pool(const DeviceInfo &dev, cudaMemPool_t *out) {
-  static std::mutex mu;
-  static cudaMemPool_t pools[64] = {};
-  std::lock_guard<std::mutex> lock(mu);
-  if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
-  if (!pools[dev.device]) {
-    cudaMemPoolProps props;
-    std::memset(&props, 0, sizeof props);
-    props.allocType = cudaMemAllocationTypePinned;
-    props.handleTypes = cudaMemHandleTypeNone;
-    props.location.type = cudaMemLocationTypeDevice;
-    props.location.id = dev.device;
-    cudaMemPool_t pl;
-    cudaError_t e = cudaMemPoolCreate(&pl, &props);
-    if (e != cudaSuccess) return e;
-    uint64_t keep = ~0ull;  // keep freed memory mapped for the next call
-    cudaMemPoolSetAttribute(pl, cudaMemPoolAttrReleaseThreshold, &keep);
-    pools[dev.device] = pl;
-  }
-  *out = pools[dev.device];
-  return cudaSuccess;
-}
-
-namespace {
-
-#ifndef DGR_TC_MAX_SPLIT
-#define DGR_TC_MAX_SPLIT 4
-#endif
 constexpr int kMaxSplit = DGR_TC_MAX_SPLIT;  // parts per tail tile (each adds one pass over C)
 
 // Splits T tiles of KB k-blocks over at most `cap` units: whole tiles
 // round-robin, then the leftover tiles split along k (at most max_split
 // parts, in steps of kb_unit k-blocks) so that every unit gets one part (see
 // TcArgs).
-void plan_work(int64_t T, int KB, int kb_unit, int cap, int max_split, int &units, int &dp_tiles,
-               int &tail_tiles, int &split) {
+inline void plan_work(int64_t T, int KB, int kb_unit, int cap, int max_split, int &units,
+                      int &dp_tiles, int &tail_tiles, int &split) {
   const int nunits = (KB + kb_unit - 1) / kb_unit;
   int U = cap;
   int64_t W = T / U, R = T - W * U;
@@ -854,28 +938,59 @@ void plan_work(int64_t T, int KB, int kb_unit, int cap, int max_split, int &unit
   split = S;
 }
 
-template <bool kInt>
-cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf16,
-                      const BatchOps &ops, int M, int N, int K,
-                      typename TcArgs<kInt>::Out alpha, const void *A, int64_t lda,
-                      const void *B, int64_t ldb, typename TcArgs<kInt>::Out beta,
-                      typename TcArgs<kInt>::Out *C, int64_t ldc, cudaStream_t stream,
-                      uint32_t *flags_ws, size_t flags_words) {
-  // Short, wide problems: the transposed-role kernel streams B at HBM speed
-  // instead of multiplying a mostly-zero 256-row tile.
-  if (M <= kSkinnyMaxM && ops.plain()) {
-    if constexpr (kInt) {
-      return launch_tc_skinny_int(dev, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream,
-                                  flags_ws, flags_words);
-    } else {
-      return launch_tc_skinny_float(dev, is_bf16, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
-                                    stream);
-    }
-  }
+// The kernel for an operand form (only the forms a kind is built with).
+template <int kKind, bool kPair, bool kAT, bool kBT>
+constexpr auto tc_kernel() {
+  return gemm_tc_kernel<kKind, kPair, kAT, kBT>;
+}
+
+// One tensor-core GEMM launch for element kind kKind. dt and ab_format are the
+// inputs' TMA data type and MMA operand format, c_dt the 16-bit C's TMA data
+// type (16-bit C only). Kinds built with every operand form take ops as given;
+// the others must be called with the single form they are built with.
+template <int kKind, bool kAllForms>
+cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, uint32_t ab_format,
+                      CUtensorMapDataType c_dt, const BatchOps &ops, int M, int N, int K,
+                      typename TcKind<kKind>::Scale alpha, const void *A, int64_t lda,
+                      const void *B, int64_t ldb, typename TcKind<kKind>::Scale beta,
+                      typename TcKind<kKind>::Out *C, int64_t ldc, cudaStream_t stream,
+                      uint32_t *flags_ws, size_t flags_words, const int32_t *row_corr = nullptr,
+                      const int32_t *col_corr = nullptr) {
+  using K_ = TcKind<kKind>;
+  constexpr int kEs = K_::kInBytes;
+  constexpr int kBK = K_::kBK;
   static_assert(sizeof(TcSmem<true>) + 1024 <= 232448, "pair kernel shared memory");
   static_assert(sizeof(TcSmem<false>) + 1024 <= 232448, "single-CTA kernel shared memory");
   const size_t smem_pair = sizeof(TcSmem<true>) + 1024;
-  const int pairs = DGR_TC_PAIR ? pair_capacity<kInt>(dev, smem_pair) : 0;
+  const size_t smem_single = sizeof(TcSmem<false>) + 1024;
+
+  // Kernel for this form.
+  using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, TcArgs<kKind>);
+  Kern kern_pair, kern_single;
+  if constexpr (kAllForms) {
+    if (ops.a_t) {
+      kern_pair =
+          ops.b_t ? tc_kernel<kKind, true, true, true>() : tc_kernel<kKind, true, true, false>();
+      kern_single =
+          ops.b_t ? tc_kernel<kKind, false, true, true>() : tc_kernel<kKind, false, true, false>();
+    } else {
+      kern_pair =
+          ops.b_t ? tc_kernel<kKind, true, false, true>() : tc_kernel<kKind, true, false, false>();
+      kern_single =
+          ops.b_t ? tc_kernel<kKind, false, false, true>() : tc_kernel<kKind, false, false, false>();
+    }
+  } else if constexpr (kKind == kKindTF32) {
+    if (ops.a_t || !ops.b_t) return cudaErrorInvalidValue;
+    kern_pair = tc_kernel<kKind, true, false, true>();
+    kern_single = tc_kernel<kKind, false, false, true>();
+  } else {
+    if (ops.a_t || ops.b_t) return cudaErrorInvalidValue;
+    kern_pair = tc_kernel<kKind, true, false, false>();
+    kern_single = tc_kernel<kKind, false, false, false>();
+  }
+
+  const int pairs =
+      DGR_TC_PAIR ? pair_capacity(dev, reinterpret_cast<const void *>(kern_pair), smem_pair) : 0;
   const bool use_pairs = pairs > 0;
   const int tile_m = use_pairs ? Cfg<true>::kTileM : Cfg<false>::kTileM;
   const uint32_t bn_load = use_pairs ? Cfg<true>::kBNLoad : Cfg<false>::kBNLoad;
@@ -886,10 +1001,10 @@ cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf1
   const int64_t nb = (batch > 1 && ops.stride_b != 0) ? batch : 1;
   CUtensorMap tmA, tmB;
   const bool maps_ok =
-      (ops.a_t ? make_tmap(&tmA, dt, A, K, M, lda, na, ops.stride_a, kBK, 64)
-               : make_tmap(&tmA, dt, A, M, K, lda, na, ops.stride_a, kBM, kBK)) &&
-      (ops.b_t ? make_tmap(&tmB, dt, B, N, K, ldb, nb, ops.stride_b, bn_load, kBK)
-               : make_tmap(&tmB, dt, B, K, N, ldb, nb, ops.stride_b, kBK, 64));
+      (ops.a_t ? make_tmap(&tmA, dt, kEs, A, K, M, lda, na, ops.stride_a, kBK, K_::kMNElems)
+               : make_tmap(&tmA, dt, kEs, A, M, K, lda, na, ops.stride_a, kBM, kBK)) &&
+      (ops.b_t ? make_tmap(&tmB, dt, kEs, B, N, K, ldb, nb, ops.stride_b, bn_load, kBK)
+               : make_tmap(&tmB, dt, kEs, B, K, N, ldb, nb, ops.stride_b, kBK, K_::kMNElems));
   if (!maps_ok) {
     if (na == 1 && nb == 1) return cudaErrorInvalidValue;
     // A stride the tensor-map encoder does not take (matrices that overlap):
@@ -897,15 +1012,16 @@ cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf1
     BatchOps one = ops;
     one.batch = 1;
     for (int64_t b = 0; b < batch; ++b) {
-      const void *Ab = static_cast<const uint16_t *>(A) + b * ops.stride_a;
-      const void *Bb = static_cast<const uint16_t *>(B) + b * ops.stride_b;
-      cudaError_t e = launch_tc<kInt>(dev, dt, is_bf16, one, M, N, K, alpha, Ab, lda, Bb, ldb,
-                                      beta, C + b * ops.stride_c, ldc, stream, nullptr, 0);
+      const void *Ab = static_cast<const uint8_t *>(A) + b * ops.stride_a * kEs;
+      const void *Bb = static_cast<const uint8_t *>(B) + b * ops.stride_b * kEs;
+      cudaError_t e = launch_tc<kKind, kAllForms>(dev, dt, ab_format, c_dt, one, M, N, K, alpha,
+                                                  Ab, lda, Bb, ldb, beta, C + b * ops.stride_c,
+                                                  ldc, stream, nullptr, 0, row_corr, col_corr);
       if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
   }
-  TcArgs<kInt> p;
+  TcArgs<kKind> p;
   p.M = M;
   p.N = N;
   p.K = K;
@@ -919,28 +1035,41 @@ cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf1
   p.a_batched = na > 1;
   p.b_batched = nb > 1;
   p.stride_c = batch > 1 ? ops.stride_c : 0;
-  p.c_vec_ok = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0);
+  // C in whole 16-byte units: base, row stride and (for a stack) matrix stride.
+  constexpr int kOutBytes = sizeof(typename K_::Out);
+  constexpr int kPer16 = 16 / kOutBytes;
+  p.c_vec_ok = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % kPer16 == 0);
   p.err_word = dev.err_word;
   p.tail_flags = nullptr;
+  if constexpr (K_::kInt) {
+    p.row_corr = row_corr;
+    p.col_corr = col_corr;
+  }
   // TMA stores of C need a 16-byte aligned base and row stride, and rows whose
   // length is a whole number of 16-byte units: a store box is clipped at the
-  // right edge of C only in 16-byte units, so with N % 4 != 0 it would also
-  // write the first columns of the row padding. A stack of C matrices also
-  // needs a matrix stride of whole 16-byte units. Otherwise the epilogue
-  // writes C with plain guarded stores.
+  // right edge of C only in 16-byte units, so otherwise it would also write
+  // the first columns of the row padding. A stack of C matrices also needs a
+  // matrix stride of whole 16-byte units. Otherwise the epilogue writes C with
+  // plain guarded stores.
   CUtensorMap tmC;
   std::memset(&tmC, 0, sizeof tmC);
-  p.c_tma = p.c_vec_ok && (N % 4 == 0) && (batch == 1 || ops.stride_c % 4 == 0) &&
-            make_tmap_c(&tmC, kInt, C, M, N, ldc, batch, ops.stride_c);
-  p.idesc = idesc_f16(is_bf16, ops.a_t, !ops.b_t, tile_m, kBN);
+  const CUtensorMapDataType cdt =
+      K_::kOut16 ? c_dt
+                 : (K_::kInt ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
+  p.c_tma = p.c_vec_ok && (N % kPer16 == 0) && (batch == 1 || ops.stride_c % kPer16 == 0) &&
+            make_tmap(&tmC, cdt, kOutBytes, C, M, N, ldc, batch, ops.stride_c, 32,
+                      128 / kOutBytes, false);
+  p.idesc = idesc_mma(ab_format, ops.a_t, !ops.b_t, tile_m, kBN);
   const int64_t tiles = static_cast<int64_t>(p.tiles_per_batch) * batch;
   if (static_cast<int64_t>(p.tiles_m) * p.tiles_n > 0x7fffffffLL || tiles > 0x7fffffffLL)
     return cudaErrorInvalidValue;
   const int KB = (K + kBK - 1) / kBK;
   const int cap = use_pairs ? pairs : dev.sm_count;
-  const int kb_unit = kInt ? kChunkKB : 1;
+  const int kb_unit = K_::kInt ? K_::kChunkK / kBK : 1;
+  // 16-bit C: no k-split (partial sums would be rounded to 16 bits in between).
+  const int max_split = K_::kOut16 ? 1 : kMaxSplit;
   int units = 0;
-  plan_work(tiles, KB, kb_unit, cap, kMaxSplit, units, p.dp_tiles, p.tail_tiles, p.split);
+  plan_work(tiles, KB, kb_unit, cap, max_split, units, p.dp_tiles, p.tail_tiles, p.split);
 
   // Tail flags: zeroed per call; from the caller's buffer or the pool.
   void *pool_flags = nullptr;
@@ -983,19 +1112,13 @@ cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf1
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    auto kern = tc_kernel_for<kInt, true>(ops.a_t, ops.b_t);
-    // Every form has the same shared memory; raise the limit for this one.
-    e = set_max_dynamic_smem(reinterpret_cast<const void *>(kern), static_cast<int>(smem_pair),
-                             dev.device);
-    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, p);
+    e = cudaLaunchKernelEx(&cfg, kern_pair, tmA, tmB, tmC, p);
     if (e == cudaSuccess) e = cudaGetLastError();
   } else {
-    const size_t smem = sizeof(TcSmem<false>) + 1024;
-    auto kern = tc_kernel_for<kInt, false>(ops.a_t, ops.b_t);
-    e = set_max_dynamic_smem(reinterpret_cast<const void *>(kern), static_cast<int>(smem),
-                             dev.device);
+    e = set_max_dynamic_smem(reinterpret_cast<const void *>(kern_single),
+                             static_cast<int>(smem_single), dev.device);
     if (e == cudaSuccess) {
-      kern<<<units, kThreads, smem, stream>>>(tmA, tmB, tmC, p);
+      kern_single<<<units, kThreads, smem_single, stream>>>(tmA, tmB, tmC, p);
       e = cudaGetLastError();
     }
   }
@@ -1006,182 +1129,5 @@ cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf1
   return e;
 }
 
-// int8 -> fp16, exact (|x| <= 128), for a stack of `count` rows x cols
-// matrices (source matrix stride src_stride; destination matrices packed at
-// rows * ldd). dst has row stride ldd (multiple of 8) and its padding columns
-// [cols, ldd) are written with zeros. Each thread widens 16 consecutive
-// elements of a row: one 16-byte load when the source row is 16-byte aligned
-// and the chunk is inside the matrix, byte loads otherwise, and one or two
-// 16-byte stores.
-__global__ void widen_s8_kernel(const int8_t *__restrict__ src, int64_t lds, int64_t src_stride,
-                                __half *dst, int64_t ldd, int rows, int cols, int count,
-                                int vec_ok) {
-  const int64_t chunks_per_row = (ldd + 15) / 16;
-  const int64_t total = static_cast<int64_t>(rows) * count * chunks_per_row;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t r = i / chunks_per_row;  // row of the whole stack
-    const int c0 = static_cast<int>((i - r * chunks_per_row) * 16);
-    const int64_t m = r / rows;            // matrix of the stack
-    const int8_t *s = src + m * src_stride + (r - m * rows) * lds;
-    __align__(16) __half h[16];
-    if (vec_ok && c0 + 16 <= cols) {
-      const int4 v = *reinterpret_cast<const int4 *>(s + c0);
-      const int w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        h[j] = __int2half_rn(static_cast<int8_t>(static_cast<uint32_t>(w[j >> 2]) >> (8 * (j & 3))));
-    } else {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int c = c0 + j;
-        h[j] = __int2half_rn(c < cols ? static_cast<int>(s[c]) : 0);
-      }
-    }
-    uint4 *d = reinterpret_cast<uint4 *>(dst + r * ldd + c0);
-    d[0] = *reinterpret_cast<const uint4 *>(h);
-    if (c0 + 16 <= ldd) d[1] = *reinterpret_cast<const uint4 *>(h + 8);
-  }
-}
-
-cudaError_t widen_s8(const DeviceInfo &dev, const int8_t *src, int64_t lds, __half *dst,
-                     int64_t ldd, int rows, int cols, cudaStream_t stream, int count = 1,
-                     int64_t src_stride = 0) {
-  const int64_t total = static_cast<int64_t>(rows) * count * ((ldd + 15) / 16);
-  const int threads = 256;
-  int64_t blocks = (total + threads - 1) / threads;
-  const int64_t cap = static_cast<int64_t>(dev.sm_count) * 16;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
-  const int vec_ok = (reinterpret_cast<uintptr_t>(src) % 16 == 0) && (lds % 16 == 0) &&
-                     (count == 1 || src_stride % 16 == 0);
-  widen_s8_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-      src, lds, src_stride, dst, ldd, rows, cols, count, vec_ok);
-  return cudaGetLastError();
-}
-
 }  // namespace
-
-cudaError_t launch_gemm_tc_f16(const DeviceInfo &dev, bool is_bf16, int M, int N, int K,
-                               float alpha, const void *A, int64_t lda, const void *B,
-                               int64_t ldb, float beta, float *C, int64_t ldc,
-                               cudaStream_t stream) {
-  const CUtensorMapDataType dt =
-      is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  return launch_tc<false>(dev, dt, is_bf16, BatchOps(), M, N, K, alpha, A, lda, B, ldb, beta, C,
-                          ldc, stream, nullptr, 0);
-}
-
-cudaError_t launch_gemm_tc_f16_ex(const DeviceInfo &dev, bool is_bf16, const BatchOps &ops, int M,
-                                  int N, int K, float alpha, const void *A, int64_t lda,
-                                  const void *B, int64_t ldb, float beta, float *C, int64_t ldc,
-                                  cudaStream_t stream) {
-  const CUtensorMapDataType dt =
-      is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  return launch_tc<false>(dev, dt, is_bf16, ops, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
-                          stream, nullptr, 0);
-}
-
-// The int8 path widens A and B to fp16 in stream-ordered scratch memory from a
-// library-owned pool, runs the tensor-core kernel in exact-integer mode and
-// returns the scratch to the pool on the same stream.
-cudaError_t launch_gemm_s8(const DeviceInfo &dev, int M, int N, int K, int32_t alpha,
-                           const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
-                           int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream) {
-  const int64_t lda16 = (static_cast<int64_t>(K) + 7) / 8 * 8;
-  const int64_t ldb16 = (static_cast<int64_t>(N) + 7) / 8 * 8;
-  const size_t a_bytes = static_cast<size_t>(M) * lda16 * 2;
-  const size_t a_off = (a_bytes + 255) / 256 * 256;
-  const size_t total = a_off + static_cast<size_t>(K) * ldb16 * 2;
-
-  cudaMemPool_t pool = nullptr;
-  {
-    cudaError_t e = device_pool(dev, &pool);
-    if (e != cudaSuccess) return e;
-  }
-  void *scratch = nullptr;
-  cudaError_t e = cudaMallocFromPoolAsync(&scratch, total, pool, stream);
-  if (e != cudaSuccess) return e;
-  __half *a16 = static_cast<__half *>(scratch);
-  __half *b16 = reinterpret_cast<__half *>(static_cast<uint8_t *>(scratch) + a_off);
-  e = widen_s8(dev, A, lda, a16, lda16, M, K, stream);
-  if (e == cudaSuccess) e = widen_s8(dev, B, ldb, b16, ldb16, K, N, stream);
-  if (e == cudaSuccess)
-    e = launch_tc<true>(dev, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, false, BatchOps(), M, N, K, alpha,
-                        a16, lda16, b16, ldb16, beta, C, ldc, stream, nullptr, 0);
-  cudaError_t f = cudaFreeAsync(scratch, stream);
-  return e != cudaSuccess ? e : f;
-}
-
-// Batched / transposed int8: each operand is widened in its stored layout
-// (one matrix, or one per batch entry, packed), then the tensor-core kernel
-// reads the fp16 copies with the same transposes and strides.
-cudaError_t launch_gemm_s8_ex(const DeviceInfo &dev, const BatchOps &ops, int M, int N, int K,
-                              int32_t alpha, const int8_t *A, int64_t lda, const int8_t *B,
-                              int64_t ldb, int32_t beta, int32_t *C, int64_t ldc,
-                              cudaStream_t stream) {
-  // Stored shapes: A is M x K or K x M, B is K x N or N x K.
-  const int a_rows = ops.a_t ? K : M, a_cols = ops.a_t ? M : K;
-  const int b_rows = ops.b_t ? N : K, b_cols = ops.b_t ? K : N;
-  const int na = (ops.batch > 1 && ops.stride_a != 0) ? ops.batch : 1;
-  const int nb = (ops.batch > 1 && ops.stride_b != 0) ? ops.batch : 1;
-  const int64_t lda16 = (static_cast<int64_t>(a_cols) + 7) / 8 * 8;
-  const int64_t ldb16 = (static_cast<int64_t>(b_cols) + 7) / 8 * 8;
-  const int64_t a_mat = a_rows * lda16, b_mat = b_rows * ldb16;  // packed strides (elements)
-  const size_t a_bytes = static_cast<size_t>(na) * a_mat * 2;
-  const size_t a_off = (a_bytes + 255) / 256 * 256;
-  const size_t total = a_off + static_cast<size_t>(nb) * b_mat * 2;
-
-  cudaMemPool_t pool = nullptr;
-  {
-    cudaError_t e = device_pool(dev, &pool);
-    if (e != cudaSuccess) return e;
-  }
-  void *scratch = nullptr;
-  cudaError_t e = cudaMallocFromPoolAsync(&scratch, total, pool, stream);
-  if (e != cudaSuccess) return e;
-  __half *a16 = static_cast<__half *>(scratch);
-  __half *b16 = reinterpret_cast<__half *>(static_cast<uint8_t *>(scratch) + a_off);
-  e = widen_s8(dev, A, lda, a16, lda16, a_rows, a_cols, stream, na, ops.stride_a);
-  if (e == cudaSuccess)
-    e = widen_s8(dev, B, ldb, b16, ldb16, b_rows, b_cols, stream, nb, ops.stride_b);
-  if (e == cudaSuccess) {
-    BatchOps wide = ops;
-    wide.stride_a = na > 1 ? a_mat : 0;
-    wide.stride_b = nb > 1 ? b_mat : 0;
-    e = launch_tc<true>(dev, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, false, wide, M, N, K, alpha, a16,
-                        lda16, b16, ldb16, beta, C, ldc, stream, nullptr, 0);
-  }
-  cudaError_t f = cudaFreeAsync(scratch, stream);
-  return e != cudaSuccess ? e : f;
-}
-
-// The int8 path with scratch memory supplied by the caller instead of drawn
-// from the library's pool: widen A and B into `scratch` (which must hold
-// s8_scratch_bytes(M, N, K) bytes, 256-byte aligned) and run the tensor-core
-// kernel in exact-integer mode. Allocates nothing.
-size_t s8_scratch_bytes(int M, int N, int K) {
-  const int64_t lda16 = (static_cast<int64_t>(K) + 7) / 8 * 8;
-  const int64_t ldb16 = (static_cast<int64_t>(N) + 7) / 8 * 8;
-  const size_t a_off = (static_cast<size_t>(M) * lda16 * 2 + 255) / 256 * 256;
-  return a_off + static_cast<size_t>(K) * ldb16 * 2;
-}
-
-cudaError_t launch_gemm_s8_scratch(const DeviceInfo &dev, int M, int N, int K, int32_t alpha,
-                                   const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
-                                   int32_t beta, int32_t *C, int64_t ldc, void *scratch,
-                                   uint32_t *flags, size_t flags_words, cudaStream_t stream) {
-  const int64_t lda16 = (static_cast<int64_t>(K) + 7) / 8 * 8;
-  const int64_t ldb16 = (static_cast<int64_t>(N) + 7) / 8 * 8;
-  const size_t a_off = (static_cast<size_t>(M) * lda16 * 2 + 255) / 256 * 256;
-  __half *a16 = static_cast<__half *>(scratch);
-  __half *b16 = reinterpret_cast<__half *>(static_cast<uint8_t *>(scratch) + a_off);
-  cudaError_t e = widen_s8(dev, A, lda, a16, lda16, M, K, stream);
-  if (e == cudaSuccess) e = widen_s8(dev, B, ldb, b16, ldb16, K, N, stream);
-  if (e == cudaSuccess)
-    e = launch_tc<true>(dev, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, false, BatchOps(), M, N, K, alpha,
-                        a16, lda16, b16, ldb16, beta, C, ldc, stream, flags, flags_words);
-  return e;
-}
-
 }  // namespace dgr

@@ -65,6 +65,28 @@ cudaError_t launch_gemm_s8(const DeviceInfo &dev, int M, int N, int K, int32_t a
                            const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
                            int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream);
 
+// uint8 inputs, exact int32 C (wrap-around) on the fp16 tensor pipe.
+cudaError_t launch_gemm_u8(const DeviceInfo &dev, int M, int N, int K, int32_t alpha,
+                           const uint8_t *A, int64_t lda, const uint8_t *B, int64_t ldb,
+                           int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream);
+
+// 16-bit inputs and a 16-bit C of the same format (is_bf16), fp32 accumulation,
+// one round-to-nearest-even. Layout rule of launch_gemm_tc_f16 for A and B.
+cudaError_t launch_gemm_tc_out16(const DeviceInfo &dev, bool is_bf16, int M, int N, int K,
+                                 float alpha, const void *A, int64_t lda, const void *B,
+                                 int64_t ldb, float beta, uint16_t *C, int64_t ldc,
+                                 cudaStream_t stream);
+
+// fp32 inputs at tf32 precision on the tensor cores, fp32 C. Any layout.
+cudaError_t launch_gemm_tf32(const DeviceInfo &dev, int M, int N, int K, float alpha,
+                             const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
+                             float *C, int64_t ldc, cudaStream_t stream);
+
+// fp64 on the SIMT pipe (dgemm_simt.cu).
+cudaError_t launch_dgemm(const DeviceInfo &dev, int M, int N, int K, double alpha,
+                         const double *A, int64_t lda, const double *B, int64_t ldb, double beta,
+                         double *C, int64_t ldc, cudaStream_t stream);
+
 // Bytes of scratch the int8 path needs, and the int8 path on caller-provided
 // scratch (256-byte aligned, at least s8_scratch_bytes(M, N, K) bytes) and
 // caller-provided split-k tail flags (flags_words 32-bit words, zeroed by the
@@ -117,6 +139,12 @@ cudaError_t launch_scale_f32(int M, int N, float beta, float *C, int64_t ldc,
                              cudaStream_t stream);
 cudaError_t launch_scale_s32(int M, int N, int32_t beta, int32_t *C, int64_t ldc,
                              cudaStream_t stream);
+// K == 0 for the other C types: C = beta * C (16-bit: decoded, scaled in fp32,
+// rounded to nearest even).
+cudaError_t launch_scale_f64(int M, int N, double beta, double *C, int64_t ldc,
+                             cudaStream_t stream);
+cudaError_t launch_scale_out16(bool is_bf16, int M, int N, float beta, uint16_t *C, int64_t ldc,
+                               cudaStream_t stream);
 // The same over a stack of `batch` C matrices, `stride` elements apart.
 cudaError_t launch_scale_batched_f32(int M, int N, float beta, float *C, int64_t ldc, int batch,
                                      int64_t stride, cudaStream_t stream);

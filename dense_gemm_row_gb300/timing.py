@@ -28,7 +28,12 @@ from . import workloads as w
 _DTYPES = {"f32": (torch.float32, torch.float32, binding.gemm_f32),
            "bf16": (torch.bfloat16, torch.float32, binding.gemm_bf16),
            "f16": (torch.float16, torch.float32, binding.gemm_f16),
-           "s8": (torch.int8, torch.int32, binding.gemm_s8)}
+           "s8": (torch.int8, torch.int32, binding.gemm_s8),
+           "u8": (torch.uint8, torch.int32, binding.gemm_u8),
+           "f16o": (torch.float16, torch.float16, binding.gemm_f16_f16),
+           "bf16o": (torch.bfloat16, torch.bfloat16, binding.gemm_bf16_bf16),
+           "tf32": (torch.float32, torch.float32, binding.gemm_tf32),
+           "f64": (torch.float64, torch.float64, binding.gemm_f64)}
 _EX = {"f32": binding.gemm_f32_ex, "bf16": binding.gemm_bf16_ex, "f16": binding.gemm_f16_ex,
        "s8": binding.gemm_s8_ex}
 
@@ -45,14 +50,16 @@ def main(argv=None) -> int:
     a = ap.parse_args(argv)
     M, N, K = (int(x) for x in a.shape.split(","))
     in_dt, out_dt, fn = _DTYPES[a.dtype]
-    dist = "int8" if a.dtype == "s8" else "normal"
+    dist = {"s8": "int8", "u8": "uint8"}.get(a.dtype, "normal")
     a_t, b_t = a.ops[0] == "T", a.ops[1] == "T"
     nb = a.batch
     A = w.stack(nb, *((K, M) if a_t else (M, K)), in_dt, dist, a.seed * 3).flat.cuda()
     B = w.stack(nb, *((N, K) if b_t else (K, N)), in_dt, dist, a.seed * 3 + 1000).flat.cuda()
     C = torch.zeros(nb * M * N, dtype=out_dt, device="cuda")
-    one, zero = (1, 0) if a.dtype == "s8" else (1.0, 0.0)
+    one, zero = (1, 0) if a.dtype in ("s8", "u8") else (1.0, 0.0)
     stream = torch.cuda.current_stream()
+    if (a.ops != "NN" or nb != 1) and a.dtype not in _EX:
+        raise SystemExit(f"--ops/--batch: no extended entry point for {a.dtype}")
     if a.ops == "NN" and nb == 1:
         def call():
             fn(M, N, K, one, A, K, B, N, zero, C, N, stream)

@@ -44,7 +44,8 @@ def matrix(rows: int, cols: int, dtype: torch.dtype, dist: str, seed: int,
     """A rows x cols matrix with row stride ``ld`` (>= cols), drawn from ``dist``.
 
     dist: "int0_99" (integers 0..99), "uniform_pm1" (U[-1, 1)), "normal"
-    (N(0, 1)), "int8" (integers -128..127), "zeros", "nan".
+    (N(0, 1)), "int8" (integers -128..127), "uint8" (integers 0..255), "zeros",
+    "nan".
     Float draws are made in float32 and then rounded to ``dtype`` with
     round-to-nearest-even (``Tensor.to``).
     """
@@ -61,6 +62,8 @@ def matrix(rows: int, cols: int, dtype: torch.dtype, dist: str, seed: int,
         v = torch.randn(shape, generator=g, dtype=torch.float32)
     elif dist == "int8":
         v = torch.randint(-128, 128, shape, generator=g, dtype=torch.int32)
+    elif dist == "uint8":
+        v = torch.randint(0, 256, shape, generator=g, dtype=torch.int32)
     elif dist == "zeros":
         v = torch.zeros(shape, dtype=torch.float32)
     elif dist == "nan":
@@ -70,7 +73,7 @@ def matrix(rows: int, cols: int, dtype: torch.dtype, dist: str, seed: int,
     v = v.to(dtype)
     if ld == cols:
         return v.contiguous().to(device)
-    poison = INT8_POISON if dtype == torch.int8 else (
+    poison = INT8_POISON if dtype in (torch.int8, torch.uint8) else (
         -2**31 if dtype == torch.int32 else FLOAT_POISON)
     store = torch.full((rows, ld), poison, dtype=dtype)
     store[:, :cols] = v
@@ -105,7 +108,7 @@ def stack(batch: int, rows: int, cols: int, dtype: torch.dtype, dist: str, seed:
     if ld < cols:
         raise ValueError("ld must be >= cols")
     stride = rows * ld + int(gap)
-    poison = INT8_POISON if dtype == torch.int8 else FLOAT_POISON
+    poison = INT8_POISON if dtype in (torch.int8, torch.uint8) else FLOAT_POISON
     flat = torch.full((max(batch * stride, 1),), poison, dtype=dtype)
     st = Stack(flat, batch, rows, cols, ld, stride)
     for b in range(batch):

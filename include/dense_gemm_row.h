@@ -123,6 +123,50 @@ GEMM_API gemm_status_t gemm_s8(int64_t M, int64_t N, int64_t K, int32_t alpha,
                       const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
                       int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream);
 
+/*
+ * Further rows of the warp-matrix-function page's type table (C++ warp matrix
+ * functions, the matrix_a / matrix_b / accumulator type table). Same call
+ * shape, row-major layout, statuses, K == 0 and beta == 0 rules as the entry
+ * points above.
+ *
+ * gemm_u8 -- unsigned char -> int row: uint8 A and B, int32 C and int32
+ *   alpha/beta, exact (the product accumulated in 64-bit integers, the update
+ *   alpha*acc + beta*C taken modulo 2^32). Any layout.
+ *
+ * gemm_f16_f16, gemm_bf16_bf16 -- half -> half row (and its bf16 analogue):
+ *   16-bit A, B and C of one format. The result is accumulated in fp32, the
+ *   update alpha*acc + beta*C is evaluated in fp32 and rounded once to the
+ *   16-bit format (round-to-nearest-even) when C is written. A and B follow the
+ *   layout rule of gemm_bf16 (16-byte aligned bases, lda and ldb multiples of
+ *   8, else GEMM_ERR_UNSUPPORTED_LAYOUT); C may have any layout.
+ *
+ * gemm_tf32 -- precision::tf32 -> float row: fp32 A, B, C; the tensor cores
+ *   use A and B at tf32 precision (8 exponent bits, 10 fraction bits: the low
+ *   13 fraction bits of each input are not used), accumulate in fp32. Opt-in:
+ *   gemm_f32 stays exact fp32. Any layout with 4-byte aligned elements. The
+ *   call allocates and frees stream-ordered scratch for a K-major copy of B.
+ *
+ * gemm_f64 -- double -> double row: fp64 A, B, C, alpha, beta, fp64 fused
+ *   multiply-adds. Any layout; M up to 4194240 (65535 tiles of 64 rows).
+ */
+GEMM_API gemm_status_t gemm_u8(int64_t M, int64_t N, int64_t K, int32_t alpha,
+                               const uint8_t *A, int64_t lda, const uint8_t *B, int64_t ldb,
+                               int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream);
+GEMM_API gemm_status_t gemm_f16_f16(int64_t M, int64_t N, int64_t K, float alpha,
+                                    const gemm_f16_t *A, int64_t lda, const gemm_f16_t *B,
+                                    int64_t ldb, float beta, gemm_f16_t *C, int64_t ldc,
+                                    cudaStream_t stream);
+GEMM_API gemm_status_t gemm_bf16_bf16(int64_t M, int64_t N, int64_t K, float alpha,
+                                      const gemm_bf16_t *A, int64_t lda, const gemm_bf16_t *B,
+                                      int64_t ldb, float beta, gemm_bf16_t *C, int64_t ldc,
+                                      cudaStream_t stream);
+GEMM_API gemm_status_t gemm_tf32(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                                 int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                                 int64_t ldc, cudaStream_t stream);
+GEMM_API gemm_status_t gemm_f64(int64_t M, int64_t N, int64_t K, double alpha, const double *A,
+                                int64_t lda, const double *B, int64_t ldb, double beta, double *C,
+                                int64_t ldc, cudaStream_t stream);
+
 /* Operand forms for the extended entry points. */
 typedef enum {
     GEMM_OP_N = 0, /* the operand as stored (row-major) */
@@ -232,6 +276,13 @@ GEMM_API gemm_status_t gemm_check_device_error(uint32_t *word);
  * the library's own failure detection.
  */
 GEMM_API gemm_status_t gemm_selftest_wait_timeout(uint32_t limit_us, cudaStream_t stream);
+
+/*
+ * The CUDA runtime's name for the error behind the calling thread's most
+ * recent GEMM_ERR_LAUNCH (e.g. "cudaErrorLaunchOutOfResources"), or
+ * "cudaSuccess" if there was none. A static string; never NULL.
+ */
+GEMM_API const char *gemm_last_launch_error(void);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 GEMM_API int gemm_version(void);

@@ -55,10 +55,15 @@ def test_status_strings_and_version(gemm_mod):
 FAKE = 1 << 20  # a non-NULL address that is never dereferenced: checks fail first
 
 
-@pytest.mark.parametrize("fn", ["gemm_f32", "gemm_bf16", "gemm_f16", "gemm_s8"])
+PLAIN = ["gemm_f32", "gemm_bf16", "gemm_f16", "gemm_s8", "gemm_u8", "gemm_f16_f16",
+         "gemm_bf16_bf16", "gemm_tf32", "gemm_f64"]
+INT_ALPHA = ("gemm_s8", "gemm_u8")
+
+
+@pytest.mark.parametrize("fn", PLAIN)
 def test_invalid_arguments_rejected_on_host(gemm_mod, fn):
     f = getattr(gemm_mod.lib, fn)
-    a = 1 if fn == "gemm_s8" else 1.0
+    a = 1 if fn in INT_ALPHA else 1.0
     cases = [
         (-1, 8, 8, 8, 8, 8),    # negative M
         (8, -1, 8, 8, 8, 8),    # negative N
@@ -76,15 +81,15 @@ def test_invalid_arguments_rejected_on_host(gemm_mod, fn):
     assert f(8, 8, 8, a, FAKE, 8, FAKE, 8, a, None, 8, None) == INVALID
 
 
-@pytest.mark.parametrize("fn", ["gemm_f32", "gemm_bf16", "gemm_f16", "gemm_s8"])
+@pytest.mark.parametrize("fn", PLAIN)
 def test_empty_output_is_a_no_op(gemm_mod, fn):
     f = getattr(gemm_mod.lib, fn)
-    a = 1 if fn == "gemm_s8" else 1.0
+    a = 1 if fn in INT_ALPHA else 1.0
     assert f(0, 8, 8, a, None, 8, None, 8, a, None, 8, None) == OK
     assert f(8, 0, 8, a, None, 8, None, 8, a, None, 0, None) == OK
 
 
-@pytest.mark.parametrize("fn", ["gemm_bf16", "gemm_f16"])
+@pytest.mark.parametrize("fn", ["gemm_bf16", "gemm_f16", "gemm_f16_f16", "gemm_bf16_bf16"])
 def test_tensor_core_layout_rule(gemm_mod, fn):
     """16-byte aligned A and B bases and lda, ldb multiples of 8, else
     GEMM_ERR_UNSUPPORTED_LAYOUT (checked before any device work)."""
@@ -141,3 +146,9 @@ def test_extended_tensor_core_layout_rule(gemm_mod, fn):
     assert call_ex(f, fn, sB=12) == LAYOUT
     assert call_ex(f, fn, A=FAKE + 2) == LAYOUT
     assert call_ex(f, fn, opA=T_, lda=12, M=12, ldc=12, N=8, sC=256) == LAYOUT
+
+
+def test_tf32_needs_aligned_elements(gemm_mod):
+    f = gemm_mod.lib.gemm_tf32
+    assert f(8, 8, 8, 1.0, FAKE + 2, 8, FAKE, 8, 0.0, FAKE, 8, None) == LAYOUT
+    assert f(8, 8, 8, 1.0, FAKE, 8, FAKE + 1, 8, 0.0, FAKE, 8, None) == LAYOUT
