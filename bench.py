@@ -64,9 +64,9 @@ WORKLOADS = {
 
 # Sources whose change invalidates recorded ncu traffic for a workload.
 KERNEL_SOURCES = {
-    "bf16_8192": ["gemm_tc.cu", "ptx.cuh"],
-    "f16_8192": ["gemm_tc.cu", "ptx.cuh"],
-    "s8_8192": ["gemm_tc.cu", "ptx.cuh"],
+    "bf16_8192": ["gemm_tc_kernel.cuh", "gemm_tc_f16.cu", "ptx.cuh"],
+    "f16_8192": ["gemm_tc_kernel.cuh", "gemm_tc_f16.cu", "ptx.cuh"],
+    "s8_8192": ["gemm_tc_kernel.cuh", "gemm_tc_int.cu", "ptx.cuh"],
     "f32_4096": ["sgemm_simt.cu", "ptx.cuh"],
 }
 
@@ -420,6 +420,90 @@ def measure_skinny(binding, torch, peaks, stream):
     return out
 
 
+def measure_types(binding, torch, peaks, stream):
+    """The further entry points (uint8, 16-bit C, tf32, fp64) and the extended
+    forms (transposed operands, strided batches), device-timed at one size
+    each: TFLOP/s (TOPS for uint8) and the fraction of the pipe's peak. tf32's
+    peak is the measured bf16 rate times the nominal tf32/bf16 ratio (1.1 /
+    2.25 PFLOP/s dense); fp64's is the nominal 1.25 TFLOP/s (no measured fp64
+    peak exists)."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(4321)
+    bf16 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    out = {}
+
+    def run(name, fn, args, steps, flops, peak, unit, note=None):
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                fn(*args)
+        torch.cuda.synchronize()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(steps):
+            fn(*args)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        t = ev0.elapsed_time(ev1) / steps / 1e3
+        ach = flops / t / 1e12
+        out[name] = {"ms": t * 1e3, "value": ach, "unit": unit, "peak": peak,
+                     "frac": ach / peak}
+        if note:
+            out[name]["note"] = note
+
+    S = 8192
+    f = flops_of(S, S, S)
+    A8 = torch.randint(0, 256, (S, S), device="cuda", dtype=torch.int32, generator=g).to(
+        torch.uint8)
+    B8 = torch.randint(0, 256, (S, S), device="cuda", dtype=torch.int32, generator=g).to(
+        torch.uint8)
+    C32 = torch.empty(S, S, device="cuda", dtype=torch.int32)
+    run("u8_8192", binding.gemm_u8, (S, S, S, 1, A8, S, B8, S, 0, C32, S, stream), 20, f, bf16,
+        "TOPS", "includes widening and the row/column offset sums")
+    del A8, B8, C32
+    for kind, dt, fn in (("f16_f16", torch.float16, binding.gemm_f16_f16),
+                         ("bf16_bf16", torch.bfloat16, binding.gemm_bf16_bf16)):
+        A = torch.randn(S, S, device="cuda", generator=g).to(dt)
+        B = torch.randn(S, S, device="cuda", generator=g).to(dt)
+        C = torch.empty(S, S, device="cuda", dtype=dt)
+        run(f"{kind}_8192", fn, (S, S, S, 1.0, A, S, B, S, 0.0, C, S, stream), 20, f, bf16,
+            "TFLOP/s")
+        del A, B, C
+    A = torch.randn(S, S, device="cuda", generator=g)
+    B = torch.randn(S, S, device="cuda", generator=g)
+    C = torch.empty(S, S, device="cuda")
+    run("tf32_8192", binding.gemm_tf32, (S, S, S, 1.0, A, S, B, S, 0.0, C, S, stream), 20, f,
+        bf16 * 1.1 / 2.25, "TFLOP/s", "includes the K-major copy of B")
+    del A, B, C
+    D = 2048
+    A = torch.randn(D, D, device="cuda", generator=g, dtype=torch.float64)
+    B = torch.randn(D, D, device="cuda", generator=g, dtype=torch.float64)
+    C = torch.empty(D, D, device="cuda", dtype=torch.float64)
+    run("f64_2048", binding.gemm_f64, (D, D, D, 1.0, A, D, B, D, 0.0, C, D, stream), 3,
+        flops_of(D, D, D), 1.25, "TFLOP/s", "peak is the nominal fp64 rate")
+    del A, B, C
+    A = torch.randn(S, S, device="cuda", generator=g).to(torch.bfloat16)
+    B = torch.randn(S, S, device="cuda", generator=g).to(torch.bfloat16)
+    C = torch.empty(S, S, device="cuda")
+    for ops in ("NT", "TN", "TT"):
+        oa = binding.OP_T if ops[0] == "T" else binding.OP_N
+        ob = binding.OP_T if ops[1] == "T" else binding.OP_N
+        run(f"bf16_8192_{ops}", binding.gemm_bf16_ex,
+            (oa, ob, S, S, S, 1.0, A, S, 0, B, S, 0, 0.0, C, S, 0, 1, stream), 20, f, bf16,
+            "TFLOP/s")
+    del A, B, C
+    nb, E = 64, 1024
+    A = torch.randn(nb, E, E, device="cuda", generator=g).to(torch.bfloat16)
+    B = torch.randn(nb, E, E, device="cuda", generator=g).to(torch.bfloat16)
+    C = torch.empty(nb, E, E, device="cuda")
+    run("bf16_batched_64x1024", binding.gemm_bf16_ex,
+        (binding.OP_N, binding.OP_N, E, E, E, 1.0, A, E, E * E, B, E, E * E, 0.0, C, E, E * E,
+         nb, stream), 20, nb * flops_of(E, E, E), bf16, "TFLOP/s")
+    del A, B, C
+    torch.cuda.empty_cache()
+    return out
+
+
 # ----------------------------------------------------------------------- main
 
 def main():
@@ -431,6 +515,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-skinny", action="store_true")
+    ap.add_argument("--no-types", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -526,6 +611,9 @@ def main():
     skinny = {}
     if not args.no_skinny:
         skinny = measure_skinny(binding, torch, peaks, stream)
+    types = {}
+    if not args.no_types:
+        types = measure_types(binding, torch, peaks, stream)
         binding.check_device_error()
 
     cpu = None
@@ -552,6 +640,7 @@ def main():
                    "window": clocks["window"]},
         "extras": extras,
         "skinny": skinny,
+        "types": types,
     }
     print(json.dumps(line), flush=True)
     if dist is not None:

@@ -21,7 +21,7 @@
 // deterministic (and exact in the int8 mode, whose split points fall on
 // 1024-k chunks), and no part waits for another.
 //
-// Sources: as gemm_tc.cu (C = alpha*A*B + beta*C, "Sgemm [128,128,8]"; half /
+// Sources: as gemm_tc_kernel.cuh (C = alpha*A*B + beta*C, "Sgemm [128,128,8]"; half /
 // bfloat16 x half / bfloat16 -> float and signed char -> int, C++ warp matrix
 // function page, type table). The pages have no skinny-shape kernel; this is a
 // layout choice for the same computation.
