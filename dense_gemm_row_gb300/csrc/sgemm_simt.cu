@@ -43,8 +43,13 @@
 
 #include <cuda_runtime.h>
 
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "launch.h"
 #include "ptx.cuh"
+#include "work_split.cuh"
 
 namespace dgr {
 namespace {
@@ -78,6 +83,11 @@ struct SimtArgs {
   int64_t stride_a, stride_b, stride_c;  // elements between batch entries (blockIdx.y)
   int tiles_m, tiles_n;
   int c_vec_ok;  // C 16-byte aligned and ldc % 4 == 0
+  // Persistent single-problem form: the work split (work_split.cuh) and the
+  // tail flags (zero at launch), and the device error word for bounded waits.
+  int dp_tiles, tail_tiles, split;
+  uint32_t *tail_flags;
+  uint32_t *err_word;
 };
 
 // Row stride of the transposed A tile: 132 = 128 + 4 floats. With it, the
@@ -180,40 +190,20 @@ __device__ __forceinline__ void load_tile(const SimtArgs &p, const float *A, con
   }
 }
 
-// BATCH: blockIdx.y selects the batch entry (otherwise a single problem, and
-// the operand addresses stay in the parameter bank instead of registers).
-template <int BK, int STAGES, bool A_T, bool VEC_A, bool B_T, bool VEC_B, bool BATCH>
-__global__ void __launch_bounds__(kThreads, 2) sgemm_simt_kernel(const SimtArgs p) {
-  constexpr int kBStride = B_T ? kAStride : kBN;
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  auto &sm = *reinterpret_cast<SimtSmem<BK, STAGES, kBStride> *>(smem_raw);
-
-  const int tid = threadIdx.x;
-  const float *A = BATCH ? p.A + blockIdx.y * p.stride_a : p.A;
-  const float *B = BATCH ? p.B + blockIdx.y * p.stride_b : p.B;
-  float *C = BATCH ? p.C + blockIdx.y * p.stride_c : p.C;
-  int tm, tn;
-  tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, tm, tn);
-  const int m0 = tm * kBM, n0 = tn * kBN;
-
-  // Thread -> 8x8 outputs. Warps form a 4 (rows) x 2 (cols) grid, lanes a
-  // 4 x 8 grid; rows rm..rm+3 and 64+rm..64+rm+3, cols cn..cn+3 and 64+cn..
-  const int warp = tid >> 5, lane = tid & 31;
-  const int rm = (warp >> 1) * 16 + (lane >> 3) * 4;
-  const int cn = (warp & 1) * 32 + (lane & 7) * 4;
-
-  float acc[8][8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-
-  const int KT = (p.K + BK - 1) / BK;
+// The k-loop of one 128 x 128 tile at (m0, n0) over k-tiles [kt0, kt1):
+// acc += op(A) op(B) over those k. Leaves shared memory free for the next
+// tile (every copy waited for, every thread past its last read).
+template <int BK, int STAGES, bool A_T, bool VEC_A, bool B_T, bool VEC_B, int BStride>
+__device__ __forceinline__ void tile_mainloop(const SimtArgs &p, const float *A, const float *B,
+                                              SimtSmem<BK, STAGES, BStride> &sm, int m0, int n0,
+                                              int kt0, int kt1, int tid, int rm, int cn,
+                                              float (&acc)[8][8]) {
+  const int KT = kt1 - kt0;
 #pragma unroll
   for (int s = 0; s < STAGES - 1; ++s) {
     if (s < KT)
-      load_tile<BK, A_T, VEC_A, B_T, VEC_B, kBStride>(p, A, B, sm.a[s], sm.b[s], m0, n0, s * BK,
-                                                       tid);
+      load_tile<BK, A_T, VEC_A, B_T, VEC_B, BStride>(p, A, B, sm.a[s], sm.b[s], m0, n0,
+                                                      (kt0 + s) * BK, tid);
     cp_async_commit();
   }
 
@@ -224,8 +214,8 @@ __global__ void __launch_bounds__(kThreads, 2) sgemm_simt_kernel(const SimtArgs 
       const int nt = kt + STAGES - 1;
       if (nt < KT) {
         const int s = nt % STAGES;
-        load_tile<BK, A_T, VEC_A, B_T, VEC_B, kBStride>(p, A, B, sm.a[s], sm.b[s], m0, n0,
-                                                         nt * BK, tid);
+        load_tile<BK, A_T, VEC_A, B_T, VEC_B, BStride>(p, A, B, sm.a[s], sm.b[s], m0, n0,
+                                                        (kt0 + nt) * BK, tid);
       }
       cp_async_commit();
     }
@@ -253,9 +243,16 @@ __global__ void __launch_bounds__(kThreads, 2) sgemm_simt_kernel(const SimtArgs 
     }
   }
   cp_async_wait<0>();
+  __syncthreads();  // no thread still reads the ring when the next tile's copies start
+}
 
-  // Epilogue.
-  const float alpha = p.alpha, beta = p.beta;
+// C[tile] = alpha * acc + beta * C (the C term only when use_c; beta = 1 when
+// a later k-part adds to what an earlier one stored). C is read through L2
+// (another CTA may have just written it).
+__device__ __forceinline__ void tile_epilogue(const SimtArgs &p, float *C, int m0, int n0, int rm,
+                                              int cn, const float (&acc)[8][8], float beta,
+                                              bool use_c) {
+  const float alpha = p.alpha;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int row = m0 + rm + (i & 3) + (i >> 2) * 64;
@@ -267,8 +264,8 @@ __global__ void __launch_bounds__(kThreads, 2) sgemm_simt_kernel(const SimtArgs 
       const float *v = &acc[i][h * 4];
       if (p.c_vec_ok && col + 3 < p.N) {
         float4 out;
-        if (beta != 0.f) {
-          const float4 c = *reinterpret_cast<const float4 *>(crow + col);
+        if (use_c) {
+          const float4 c = __ldcg(reinterpret_cast<const float4 *>(crow + col));
           out = make_float4(alpha * v[0] + beta * c.x, alpha * v[1] + beta * c.y,
                             alpha * v[2] + beta * c.z, alpha * v[3] + beta * c.w);
         } else {
@@ -280,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 2) sgemm_simt_kernel(const SimtArgs 
         for (int j = 0; j < 4; ++j) {
           if (col + j < p.N) {
             const float r = alpha * v[j];
-            crow[col + j] = (beta != 0.f) ? r + beta * crow[col + j] : r;
+            crow[col + j] = use_c ? r + beta * __ldcg(crow + col + j) : r;
           }
         }
       }
@@ -288,14 +285,142 @@ __global__ void __launch_bounds__(kThreads, 2) sgemm_simt_kernel(const SimtArgs 
   }
 }
 
-template <int BK, int STAGES, bool A_T, bool VEC_A, bool B_T, bool VEC_B, bool BATCH = true>
-cudaError_t launch_variant(const SimtArgs &a, int batch, int device, cudaStream_t stream) {
+// Grid forms of the kernel.
+constexpr int kModeTile = 0;     // one problem, one CTA per tile
+constexpr int kModeBatch = 1;    // one CTA per tile, blockIdx.y = batch entry
+constexpr int kModeSplit = 2;    // one problem, persistent CTAs over a k-split work list
+
+// kModeSplit: a persistent grid of at most the co-resident CTAs walks the work
+// list of work_split.cuh (whole tiles, then the last wave's leftover tiles
+// split along k, parts added in order). For grids of fewer than two waves;
+// with more, one CTA per tile measures faster (CTAs that start together stay
+// in step, and their loads stop overlapping each other's arithmetic).
+template <int BK, int STAGES, bool A_T, bool VEC_A, bool B_T, bool VEC_B, int MODE>
+__global__ void __launch_bounds__(kThreads, 2) sgemm_simt_kernel(const SimtArgs p) {
+  constexpr int kBStride = B_T ? kAStride : kBN;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  auto &sm = *reinterpret_cast<SimtSmem<BK, STAGES, kBStride> *>(smem_raw);
+
+  const int tid = threadIdx.x;
+  // Thread -> 8x8 outputs. Warps form a 4 (rows) x 2 (cols) grid, lanes a
+  // 4 x 8 grid; rows rm..rm+3 and 64+rm..64+rm+3, cols cn..cn+3 and 64+cn..
+  const int warp = tid >> 5, lane = tid & 31;
+  const int rm = (warp >> 1) * 16 + (lane >> 3) * 4;
+  const int cn = (warp & 1) * 32 + (lane & 7) * 4;
+  const int KT = (p.K + BK - 1) / BK;
+  float acc[8][8];
+
+  if constexpr (MODE != kModeSplit) {
+    // The operand addresses of a single problem stay in the parameter bank.
+    const float *A = MODE == kModeBatch ? p.A + blockIdx.y * p.stride_a : p.A;
+    const float *B = MODE == kModeBatch ? p.B + blockIdx.y * p.stride_b : p.B;
+    float *C = MODE == kModeBatch ? p.C + blockIdx.y * p.stride_c : p.C;
+    int tm, tn;
+    tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, tm, tn);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    tile_mainloop<BK, STAGES, A_T, VEC_A, B_T, VEC_B, kBStride>(p, A, B, sm, tm * kBM, tn * kBN,
+                                                                0, KT, tid, rm, cn, acc);
+    tile_epilogue(p, C, tm * kBM, tn * kBN, rm, cn, acc, p.beta, p.beta != 0.f);
+  } else {
+    __shared__ int abort;
+    if (tid == 0) abort = 0;
+    const int units = static_cast<int>(gridDim.x);
+    WorkItem w;
+    for (int n = 0; get_work(static_cast<int>(blockIdx.x), n, units, p.dp_tiles, p.tail_tiles,
+                             p.split, KT, 1, w);
+         ++n) {
+      int tm, tn;
+      tile_coords(w.tile, p.tiles_m, p.tiles_n, tm, tn);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+      tile_mainloop<BK, STAGES, A_T, VEC_A, B_T, VEC_B, kBStride>(p, p.A, p.B, sm, tm * kBM,
+                                                                  tn * kBN, w.kb0, w.kb1, tid, rm,
+                                                                  cn, acc);
+      if (w.parts == 1) {
+        tile_epilogue(p, p.C, tm * kBM, tn * kBN, rm, cn, acc, p.beta, p.beta != 0.f);
+        continue;
+      }
+      // k-split tile: part j adds after part j - 1 has stored (in order).
+      uint32_t *flag = p.tail_flags + (w.tile - p.dp_tiles);
+      if (w.part > 0) {
+        if (tid == 0) wait_flag(flag, static_cast<uint32_t>(w.part), &abort, p.err_word);
+        __syncthreads();
+        tile_epilogue(p, p.C, tm * kBM, tn * kBN, rm, cn, acc, 1.f, true);
+      } else {
+        tile_epilogue(p, p.C, tm * kBM, tn * kBN, rm, cn, acc, p.beta, p.beta != 0.f);
+      }
+      __threadfence();
+      __syncthreads();  // every thread's part of the tile is stored and visible
+      if (tid == 0) st_release_gpu(flag, static_cast<uint32_t>(w.part + 1));
+    }
+  }
+}
+
+// CTAs of `kern` that can be resident at once on the device (cached).
+int resident_ctas(const DeviceInfo &dev, const void *kern, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::pair<const void *, int>, int> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_pair(kern, dev.device);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) !=
+      cudaSuccess)
+    per_sm = 0;
+  cudaGetLastError();
+  const int n = per_sm * dev.sm_count;
+  cache[key] = n;
+  return n;
+}
+
+constexpr int kSimtMaxSplit = 4;  // parts per leftover tile (each adds one pass over its C)
+
+template <int BK, int STAGES, bool A_T, bool VEC_A, bool B_T, bool VEC_B, int MODE = kModeBatch>
+cudaError_t launch_variant(const SimtArgs &a_in, int batch, const DeviceInfo &dev,
+                           cudaStream_t stream) {
   constexpr size_t smem = sizeof(SimtSmem<BK, STAGES, B_T ? kAStride : kBN>);
-  auto kern = sgemm_simt_kernel<BK, STAGES, A_T, VEC_A, B_T, VEC_B, BATCH>;
+  auto kern = sgemm_simt_kernel<BK, STAGES, A_T, VEC_A, B_T, VEC_B, MODE>;
   cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void *>(kern),
-                                       static_cast<int>(smem), device);
+                                       static_cast<int>(smem), dev.device);
   if (e != cudaSuccess) return e;
+  SimtArgs a = a_in;
+  a.err_word = dev.err_word;
+  a.tail_flags = nullptr;
   const int64_t blocks = static_cast<int64_t>(a.tiles_m) * a.tiles_n;
+  if constexpr (MODE == kModeSplit) {
+    // Persistent grid over the co-resident CTAs, the last wave split along k.
+    const int cap = resident_ctas(dev, reinterpret_cast<const void *>(kern), smem);
+    if (cap <= 0) return cudaErrorLaunchOutOfResources;
+    const int KT = (a.K + BK - 1) / BK;
+    int units = 0;
+    plan_work(blocks, KT, 1, cap, kSimtMaxSplit, units, a.dp_tiles, a.tail_tiles, a.split);
+    void *flags = nullptr;
+    if (a.split > 1) {
+      cudaMemPool_t pool;
+      e = device_pool(dev, &pool);
+      if (e != cudaSuccess) return e;
+      const size_t bytes = static_cast<size_t>(a.tail_tiles) * 4;
+      e = cudaMallocFromPoolAsync(&flags, bytes, pool, stream);
+      if (e != cudaSuccess) return e;
+      e = cudaMemsetAsync(flags, 0, bytes, stream);
+      a.tail_flags = static_cast<uint32_t *>(flags);
+    }
+    if (e == cudaSuccess) {
+      kern<<<static_cast<unsigned>(units), kThreads, smem, stream>>>(a);
+      e = cudaGetLastError();
+    }
+    if (flags) {
+      cudaError_t f = cudaFreeAsync(flags, stream);
+      if (e == cudaSuccess) e = f;
+    }
+    return e;
+  }
   // The batch runs on gridDim.y, at most 65535 entries per launch.
   constexpr int kMaxY = 65535;
   for (int b0 = 0; b0 < batch; b0 += kMaxY) {
@@ -320,13 +445,13 @@ cudaError_t launch_variant(const SimtArgs &a, int batch, int device, cudaStream_
 constexpr int kSimtBK = DGR_SIMT_BK, kSimtStages = DGR_SIMT_STAGES;
 
 template <bool A_T, bool VEC_A>
-cudaError_t launch_b(const SimtArgs &a, bool b_t, bool vec_b, int batch, int device,
+cudaError_t launch_b(const SimtArgs &a, bool b_t, bool vec_b, int batch, const DeviceInfo &dev,
                      cudaStream_t stream) {
   if (b_t)
-    return launch_variant<kSimtBK, kSimtStages, A_T, VEC_A, true, false>(a, batch, device, stream);
-  return vec_b ? launch_variant<kSimtBK, kSimtStages, A_T, VEC_A, false, true>(a, batch, device,
+    return launch_variant<kSimtBK, kSimtStages, A_T, VEC_A, true, false>(a, batch, dev, stream);
+  return vec_b ? launch_variant<kSimtBK, kSimtStages, A_T, VEC_A, false, true>(a, batch, dev,
                                                                                stream)
-               : launch_variant<kSimtBK, kSimtStages, A_T, VEC_A, false, false>(a, batch, device,
+               : launch_variant<kSimtBK, kSimtStages, A_T, VEC_A, false, false>(a, batch, dev,
                                                                                 stream);
 }
 
@@ -368,14 +493,23 @@ cudaError_t launch_sgemm_simt_ex(const DeviceInfo &dev, const BatchOps &ops, int
   if (static_cast<int64_t>(a.tiles_m) * a.tiles_n > 0x7fffffffLL) return cudaErrorInvalidValue;
   const bool vec_a = ops.a_t && vec_ok(A, lda, M, batch, a.stride_a);
   const bool vec_b = !ops.b_t && vec_ok(B, ldb, N, batch, a.stride_b);
-  if (ops.plain())  // one problem, no transposes: the kernels without a batch index
-    return vec_b ? launch_variant<kSimtBK, kSimtStages, false, false, false, true, false>(
-                       a, 1, dev.device, stream)
-                 : launch_variant<kSimtBK, kSimtStages, false, false, false, false, false>(
-                       a, 1, dev.device, stream);
-  if (!ops.a_t) return launch_b<false, false>(a, ops.b_t, vec_b, batch, dev.device, stream);
-  return vec_a ? launch_b<true, true>(a, ops.b_t, vec_b, batch, dev.device, stream)
-               : launch_b<true, false>(a, ops.b_t, vec_b, batch, dev.device, stream);
+  if (ops.plain()) {  // one problem, no transposes
+    // Fewer tiles than two waves of resident CTAs (2 per SM): the persistent
+    // k-split form keeps every SM busy; otherwise one CTA per tile.
+    const int64_t tiles = static_cast<int64_t>(a.tiles_m) * a.tiles_n;
+    if (tiles < 4LL * dev.sm_count)
+      return vec_b ? launch_variant<kSimtBK, kSimtStages, false, false, false, true, kModeSplit>(
+                         a, 1, dev, stream)
+                   : launch_variant<kSimtBK, kSimtStages, false, false, false, false, kModeSplit>(
+                         a, 1, dev, stream);
+    return vec_b ? launch_variant<kSimtBK, kSimtStages, false, false, false, true, kModeTile>(
+                       a, 1, dev, stream)
+                 : launch_variant<kSimtBK, kSimtStages, false, false, false, false, kModeTile>(
+                       a, 1, dev, stream);
+  }
+  if (!ops.a_t) return launch_b<false, false>(a, ops.b_t, vec_b, batch, dev, stream);
+  return vec_a ? launch_b<true, true>(a, ops.b_t, vec_b, batch, dev, stream)
+               : launch_b<true, false>(a, ops.b_t, vec_b, batch, dev, stream);
 }
 
 cudaError_t launch_sgemm_simt(const DeviceInfo &dev, int M, int N, int K, float alpha,
