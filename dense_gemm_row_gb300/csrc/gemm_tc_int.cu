@@ -10,8 +10,9 @@
 //     sum_k a_ik b_kj = sum_k sa_ik sb_kj + 128 rowsum(A)_i + 128 colsum(B)_j
 //                       - 16384 K,
 // so the operands are widened as x - 128 and the epilogue adds
-// row_corr[i] = 128 rowsum(A)_i - 16384 K and col_corr[j] = 128 colsum(B)_j
-// (all modulo 2^32, like the result). A direct uint8 kernel would need
+// row_corr[i] + col_corr[j] + corr_const with row_corr[i] = 128 rowsum(A)_i,
+// col_corr[j] = 128 colsum(B)_j and corr_const = -16384 K (all modulo 2^32,
+// like the result). A direct uint8 kernel would need
 // 256-value chunks (256 * 255^2 < 2^24 < 1024 * 255^2), four times as many
 // accumulator hand-offs to the epilogue.
 #include "gemm_tc_kernel.cuh"
@@ -149,35 +150,79 @@ cudaError_t run_int_pooled(const DeviceInfo &dev, const BatchOps &ops, int M, in
   return e != cudaSuccess ? e : f;
 }
 
-// row_corr[i] = 128 * sum_k A[i, k] - 16384 * K (mod 2^32): one warp per row,
-// lanes along k, a shuffle reduction.
+// row_corr[i] = 128 * sum_k A[i, k] (mod 2^32): one warp per row, lanes along
+// k, 16 bytes per lane per step when rows are 16-byte aligned (byte sums by
+// dp4a against 0x01010101), a shuffle reduction at the end.
 __global__ void u8_row_corr_kernel(const uint8_t *__restrict__ A, int64_t lda, int rows, int K,
-                                   int32_t *row_corr) {
+                                   int vec, int32_t *row_corr) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   for (int64_t r = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; r < rows;
        r += warps) {
     const uint8_t *row = A + r * lda;
     uint32_t s = 0;
-    for (int k = lane; k < K; k += 32) s += row[k];
+    int k0 = 0;
+    if (vec) {
+      const int kv = K / 16 * 16;
+      for (int k = lane * 16; k < kv; k += 32 * 16) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(row + k);
+        s = __dp4a(w.x, 0x01010101u, s);
+        s = __dp4a(w.y, 0x01010101u, s);
+        s = __dp4a(w.z, 0x01010101u, s);
+        s = __dp4a(w.w, 0x01010101u, s);
+      }
+      k0 = kv;
+    }
+    for (int k = k0 + lane; k < K; k += 32) s += row[k];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0)
-      row_corr[r] = static_cast<int32_t>(128u * s - 16384u * static_cast<uint32_t>(K));
+    if (lane == 0) row_corr[r] = static_cast<int32_t>(128u * s);
   }
 }
 
-// col_corr[j] += 128 * sum over this block's rows of B[k, j] (mod 2^32); col_corr
-// starts at zero. Threads along columns (coalesced rows), blocks along k.
-__global__ void u8_col_corr_kernel(const uint8_t *__restrict__ B, int64_t ldb, int K, int N,
-                                   int rows_per_block, int32_t *col_corr) {
-  const int64_t j = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
-  if (j >= N) return;
-  const int64_t k0 = static_cast<int64_t>(blockIdx.y) * rows_per_block;
-  const int64_t k1 = k0 + rows_per_block < K ? k0 + rows_per_block : K;
-  uint32_t s = 0;
-  for (int64_t k = k0; k < k1; ++k) s += B[k * ldb + j];
-  atomicAdd(reinterpret_cast<unsigned int *>(col_corr + j), 128u * s);
+// col_corr[j] += 128 * sum over this block's rows of B[k, j] (mod 2^32);
+// col_corr starts at zero. A block covers 512 columns x kColRows rows: lane l
+// of every warp owns columns 16 l .. 16 l + 15 (one 16-byte load per row when
+// rows are 16-byte aligned, so a warp reads 512 contiguous bytes), warp w owns
+// every 8th row of the block's range; the 8 warps' sums meet in shared memory
+// and one atomic per column leaves the block.
+constexpr int kColRows = 256;
+__global__ void __launch_bounds__(256)
+    u8_col_corr_kernel(const uint8_t *__restrict__ B, int64_t ldb, int K, int N, int vec,
+                       int32_t *col_corr) {
+  __shared__ uint32_t part[8][512];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 512 + lane * 16;
+  const int64_t k0 = static_cast<int64_t>(blockIdx.y) * kColRows;
+  const int64_t k1 = k0 + kColRows < K ? k0 + kColRows : K;
+  uint32_t s[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) s[j] = 0;
+  if (vec && c0 + 15 < N) {
+#pragma unroll 4
+    for (int64_t k = k0 + warp; k < k1; k += 8) {
+      const uint4 w = *reinterpret_cast<const uint4 *>(B + k * ldb + c0);
+      const uint32_t q[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int j = 0; j < 16; ++j) s[j] += (q[j >> 2] >> (8 * (j & 3))) & 0xffu;
+    }
+  } else {
+    for (int64_t k = k0 + warp; k < k1; k += 8)
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (c0 + j < N) s[j] += B[k * ldb + c0 + j];
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) part[warp][lane * 16 + j] = s[j];
+  __syncthreads();
+  for (int c = threadIdx.x; c < 512; c += 256) {
+    const int64_t col = static_cast<int64_t>(blockIdx.x) * 512 + c;
+    if (col >= N) continue;
+    uint32_t t = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t += part[w][c];
+    atomicAdd(reinterpret_cast<unsigned int *>(col_corr + col), 128u * t);
+  }
 }
 
 }  // namespace
@@ -218,24 +263,28 @@ cudaError_t launch_gemm_u8(const DeviceInfo &dev, int M, int N, int K, int32_t a
   if (e == cudaSuccess) {
     int64_t blocks = (static_cast<int64_t>(M) * 32 + 255) / 256;
     if (blocks > dev.sm_count * 8) blocks = dev.sm_count * 8;
-    u8_row_corr_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(A, lda, M, K,
+    const int vec = (reinterpret_cast<uintptr_t>(A) % 16 == 0) && (lda % 16 == 0);
+    u8_row_corr_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(A, lda, M, K, vec,
                                                                           row_corr);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) e = cudaMemsetAsync(col_corr, 0, static_cast<size_t>(N) * 4, stream);
   if (e == cudaSuccess) {
-    int rows_per_block = 256;
-    if ((K + rows_per_block - 1) / rows_per_block > 65535) rows_per_block = (K + 65534) / 65535;
-    const dim3 grid(static_cast<unsigned>((N + 255) / 256),
-                    static_cast<unsigned>((K + rows_per_block - 1) / rows_per_block));
-    u8_col_corr_kernel<<<grid, 256, 0, stream>>>(B, ldb, K, N, rows_per_block, col_corr);
-    e = cudaGetLastError();
+    const int64_t gy = (static_cast<int64_t>(K) + kColRows - 1) / kColRows;
+    if (gy > 65535) e = cudaErrorInvalidValue;  // K beyond 16.7 million
+    const dim3 grid(static_cast<unsigned>((N + 511) / 512), static_cast<unsigned>(gy));
+    const int vec = (reinterpret_cast<uintptr_t>(B) % 16 == 0) && (ldb % 16 == 0);
+    if (e == cudaSuccess) {
+      u8_col_corr_kernel<<<grid, 256, 0, stream>>>(B, ldb, K, N, vec, col_corr);
+      e = cudaGetLastError();
+    }
   }
   if (e == cudaSuccess)
     e = launch_tc<kKindS8, true>(dev, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, kFmtF16,
                                  CU_TENSOR_MAP_DATA_TYPE_FLOAT16, BatchOps(), M, N, K, alpha, a16,
                                  w.lda16, b16, w.ldb16, beta, C, ldc, stream, nullptr, 0,
-                                 row_corr, col_corr);
+                                 row_corr, col_corr, static_cast<int32_t>(0u - 16384u *
+                                                                          static_cast<uint32_t>(K)));
   cudaError_t f = cudaFreeAsync(scratch, stream);
   return e != cudaSuccess ? e : f;
 }

@@ -17,7 +17,8 @@
 //     kernel therefore restarts the fp32 accumulator every 1024 values of k,
 //     and the epilogue adds each finished partial sum into int32 registers
 //     (wrap-around). uint8 operands arrive offset by -128 (int8 range), and
-//     the epilogue adds the exact correction row_corr[i] + col_corr[j] once;
+//     the epilogue adds the exact correction row_corr[i] + col_corr[j] +
+//     corr_const once;
 //   * fp32 inputs used at tf32 precision (kind::tf32), fp32 C; both operands
 //     are staged K-major.
 //
@@ -171,6 +172,7 @@ struct TcCorr {};
 template <>
 struct TcCorr<true> {
   const int32_t *row_corr, *col_corr;
+  int32_t corr_const;
 };
 
 template <int kKind>
@@ -611,10 +613,11 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tmA, const CUten
       }
       uint32_t acc[kInt ? 128 : 1];  // int mode: running int32 sums (wrap-around)
       if constexpr (kInt) {
-        // The sums start at the offset correction row_corr + col_corr (part 0
-        // of a tile only), else at zero.
+        // The sums start at the offset correction row_corr + col_corr +
+        // corr_const (part 0 of a tile only), else at zero.
         if (p.row_corr != nullptr && !addto && row < p.M) {
-          const uint32_t rc = static_cast<uint32_t>(__ldg(p.row_corr + row));
+          const uint32_t rc = static_cast<uint32_t>(__ldg(p.row_corr + row)) +
+                              static_cast<uint32_t>(p.corr_const);
 #pragma unroll
           for (int j = 0; j < 128; ++j)
             acc[j] = col0 + j < p.N ? rc + static_cast<uint32_t>(__ldg(p.col_corr + col0 + j)) : 0u;
@@ -871,7 +874,7 @@ cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, uint32_t ab
                       const void *B, int64_t ldb, typename TcKind<kKind>::Scale beta,
                       typename TcKind<kKind>::Out *C, int64_t ldc, cudaStream_t stream,
                       uint32_t *flags_ws, size_t flags_words, const int32_t *row_corr = nullptr,
-                      const int32_t *col_corr = nullptr) {
+                      const int32_t *col_corr = nullptr, int32_t corr_const = 0) {
   using K_ = TcKind<kKind>;
   constexpr int kEs = K_::kInBytes;
   constexpr int kBK = K_::kBK;
@@ -932,7 +935,8 @@ cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, uint32_t ab
       const void *Bb = static_cast<const uint8_t *>(B) + b * ops.stride_b * kEs;
       cudaError_t e = launch_tc<kKind, kAllForms>(dev, dt, ab_format, c_dt, one, M, N, K, alpha,
                                                   Ab, lda, Bb, ldb, beta, C + b * ops.stride_c,
-                                                  ldc, stream, nullptr, 0, row_corr, col_corr);
+                                                  ldc, stream, nullptr, 0, row_corr, col_corr,
+                                                  corr_const);
       if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -960,6 +964,7 @@ cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, uint32_t ab
   if constexpr (K_::kInt) {
     p.row_corr = row_corr;
     p.col_corr = col_corr;
+    p.corr_const = corr_const;
   }
   // TMA stores of C need a 16-byte aligned base and row stride, and rows whose
   // length is a whole number of 16-byte units: a store box is clipped at the

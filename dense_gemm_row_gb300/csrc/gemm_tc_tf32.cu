@@ -15,24 +15,55 @@ namespace dgr {
 namespace {
 
 // dst (cols x rows, row stride ldd) = transpose of src (rows x cols, row
-// stride lds), through 32 x 32 tiles in shared memory (the extra column keeps
-// the transposed reads free of bank conflicts). Reads and writes are both
-// coalesced along rows. Blocks of 32 x 8 threads walk the tiles grid-stride.
-__global__ void transpose_f32_kernel(const float *__restrict__ src, int64_t lds,
-                                     float *__restrict__ dst, int64_t ldd, int rows, int cols) {
-  __shared__ float tile[32][33];
-  const int64_t tiles_c = (cols + 31) / 32;
-  const int64_t tiles = (static_cast<int64_t>(rows) + 31) / 32 * tiles_c;
+// stride lds), through 64 x 64 tiles in shared memory (row stride 65: the
+// column reads of the write phase fall in distinct banks). Each of the 256
+// threads moves 16 values per phase: 16-byte loads along src rows when the
+// source allows them (vec_src) and 16-byte stores along dst rows when dst
+// does (vec_dst), element accesses otherwise. Blocks walk the tiles
+// grid-stride.
+__global__ void __launch_bounds__(256)
+    transpose_f32_kernel(const float *__restrict__ src, int64_t lds, float *__restrict__ dst,
+                         int64_t ldd, int rows, int cols, int vec_src, int vec_dst) {
+  __shared__ float tile[64][65];
+  const int tid = threadIdx.x;
+  const int64_t tiles_c = (cols + 63) / 64;
+  const int64_t tiles = (static_cast<int64_t>(rows) + 63) / 64 * tiles_c;
   for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
-    const int64_t r0 = t / tiles_c * 32, c0 = t % tiles_c * 32;
-    for (int i = threadIdx.y; i < 32; i += 8) {
-      const int64_t r = r0 + i, c = c0 + threadIdx.x;
-      if (r < rows && c < cols) tile[i][threadIdx.x] = src[r * lds + c];
+    const int64_t r0 = t / tiles_c * 64, c0 = t % tiles_c * 64;
+    // Read phase: 64 rows x 16 chunks of 4 columns; thread -> (row, chunk).
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = tid + 256 * i;
+      const int r = e >> 4, q = (e & 15) * 4;
+      const int64_t gr = r0 + r, gc = c0 + q;
+      float v[4];
+      if (vec_src && gr < rows && gc + 3 < cols) {
+        const float4 f = *reinterpret_cast<const float4 *>(src + gr * lds + gc);
+        v[0] = f.x, v[1] = f.y, v[2] = f.z, v[3] = f.w;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = (gr < rows && gc + j < cols) ? src[gr * lds + gc + j] : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) tile[r][q + j] = v[j];
     }
     __syncthreads();
-    for (int i = threadIdx.y; i < 32; i += 8) {
-      const int64_t c = c0 + i, r = r0 + threadIdx.x;  // dst row c, column r
-      if (c < cols && r < rows) dst[c * ldd + r] = tile[threadIdx.x][i];
+    // Write phase: dst rows c0 .. c0+63 (src columns), 16 chunks of 4 src rows.
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = tid + 256 * i;
+      const int c = e >> 4, q = (e & 15) * 4;
+      const int64_t gc = c0 + c, gr = r0 + q;  // dst row gc, columns gr .. gr+3
+      if (gc >= cols) continue;
+      const float v0 = tile[q][c], v1 = tile[q + 1][c], v2 = tile[q + 2][c], v3 = tile[q + 3][c];
+      if (vec_dst && gr + 3 < rows) {
+        *reinterpret_cast<float4 *>(dst + gc * ldd + gr) = make_float4(v0, v1, v2, v3);
+      } else {
+        const float v[4] = {v0, v1, v2, v3};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (gr + j < rows) dst[gc * ldd + gr + j] = v[j];
+      }
     }
     __syncthreads();
   }
@@ -65,11 +96,12 @@ cudaError_t launch_gemm_tf32(const DeviceInfo &dev, int M, int N, int K, float a
     lda_used = ldk;
   }
   if (e == cudaSuccess) {
-    const int64_t tiles = (static_cast<int64_t>(K) + 31) / 32 * ((N + 31) / 32);
-    int64_t blocks = tiles < static_cast<int64_t>(dev.sm_count) * 16 ? tiles
-                                                                      : dev.sm_count * 16;
-    transpose_f32_kernel<<<static_cast<unsigned>(blocks), dim3(32, 8), 0, stream>>>(B, ldb, bt,
-                                                                                   ldk, K, N);
+    const int64_t tiles = (static_cast<int64_t>(K) + 63) / 64 * ((N + 63) / 64);
+    int64_t blocks = tiles < static_cast<int64_t>(dev.sm_count) * 8 ? tiles : dev.sm_count * 8;
+    const int vec_src = (reinterpret_cast<uintptr_t>(B) % 16 == 0) && (ldb % 4 == 0);
+    const int vec_dst = 1;  // bt: 256-byte aligned, ldk a multiple of 4
+    transpose_f32_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(B, ldb, bt, ldk, K,
+                                                                           N, vec_src, vec_dst);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) {

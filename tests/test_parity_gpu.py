@@ -275,13 +275,14 @@ def test_split_tail_shapes(gemm_mod, oracle_mod, dtype, shape):
 # ---------------------------------------------------------- short, wide shapes
 
 @pytest.mark.parametrize("dtype", ALL_DTYPES, ids=str)
-@pytest.mark.parametrize("M", [1, 5, 16, 17, 32, 33])
+@pytest.mark.parametrize("M", [1, 5, 16, 17, 32, 33, 48, 64, 65])
 def test_skinny_shapes(gemm_mod, oracle_mod, dtype, M):
     """Few rows of A (for M <= 32: the transposed-role tensor-core kernel, and
     for fp32 / int8 the small-M kernel when A and B rows are 16-byte multiples;
-    the tiled kernels above), a ragged N and a K that is split across SMs, with
-    beta != 0; every output checked. K = 3008 keeps int8 rows 16-byte multiples,
-    K = 3000 does not (fallback paths)."""
+    fp32 with 33..64 rows: two small-M passes; the tiled kernels above), a
+    ragged N and a K that is split across SMs, with beta != 0; every output
+    checked. K = 3008 keeps int8 rows 16-byte multiples, K = 3000 does not
+    (fallback paths)."""
     N = 2056
     for aligned, K in ((True, 3008), (False, 3000), (True, 3000)):
         if dtype == torch.int8:
