@@ -634,6 +634,16 @@ def main():
                 "kernel_ms": kernel_ms}
     if kind == "s8":
         roofline["note"] = "step time includes the two int8->fp16 widening launches"
+    if kind != "f32":
+        # Context for a long timed loop: the measured sustained (power-capped)
+        # peak, and the fraction of the dense rate at the clock sampled during
+        # the timed region (152 x 8192 flop/clk for kind::f16 at that clock).
+        sus = peak_for(kind, peaks, sm_count, sustained=True)
+        roofline["frac_of_sustained_peak"] = achieved / sus
+        roofline["sustained_peak"] = sus
+        if clocks.get("sm_mhz"):
+            roofline["frac_at_sampled_clock"] = achieved / (
+                sm_count * 8192 * clocks["sm_mhz"] * 1e6 / 1e12)
 
     # End to end through the C ABI with pinned host buffers.
     Ah = p.A.pin_memory()
