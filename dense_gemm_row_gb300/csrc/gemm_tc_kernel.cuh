@@ -94,6 +94,12 @@ namespace {
 #ifndef DGR_TC_MAX_SPLIT
 #define DGR_TC_MAX_SPLIT 4
 #endif
+// L2 eviction hints on the TMA copies: A (reused across a group's tile
+// columns) evict-last, C stores evict-first. Measured on GB300 at 8192^3:
+// bf16 +0.5 %, int8 +0.9 % over no hints.
+#ifndef DGR_TC_L2HINT
+#define DGR_TC_L2HINT 1
+#endif
 
 // Element kinds of one instantiation.
 constexpr int kKindF32 = 0;      // bf16 / fp16 in, fp32 C
@@ -323,6 +329,8 @@ __device__ __forceinline__ void store_row_chunk16(const TcArgs<kKind> &p, uint16
 __device__ __forceinline__ void tma_write_block(uint32_t stage, const void *tmC, int x, int y,
                                                 int z, int M, int N, const uint32_t (&w)[32],
                                                 bool addto, int lane) {
+  [[maybe_unused]] uint64_t pol_stream = 0;
+  if constexpr (DGR_TC_L2HINT != 0) pol_stream = l2_policy_evict_first();
   if (lane == 0) bulk_wait_read_all();  // the previous block has left the buffer
   __syncwarp();
   const uint32_t row = stage + static_cast<uint32_t>(lane) * 128u;
@@ -335,6 +343,8 @@ __device__ __forceinline__ void tma_write_block(uint32_t stage, const void *tmC,
   if (lane == 0 && x < N && y < M) {  // a block wholly outside C issues nothing
     if (addto) {
       tma_reduce_add_3d(tmC, x, y, z, stage);
+    } else if constexpr (DGR_TC_L2HINT != 0) {
+      tma_store_3d_hint(tmC, x, y, z, stage, pol_stream);
     } else {
       tma_store_3d(tmC, x, y, z, stage);
     }
@@ -438,6 +448,8 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tmA, const CUten
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      [[maybe_unused]] uint64_t pol_keep = 0;
+      if constexpr (DGR_TC_L2HINT != 0) pol_keep = l2_policy_evict_last();
       uint32_t stage = 0, phase = 0;
       uint32_t issued = 0;         // stages with a load issued
       uint32_t issued_parity = 0;  // parity of the last load issued per stage
@@ -467,13 +479,25 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tmA, const CUten
               tma_load_3d(dst, tm, bar, x, y, z);
             }
           };
+          auto load_keep = [&](uint32_t dst, const CUtensorMap *tm, int x, int y, int z) {
+            if constexpr (DGR_TC_L2HINT != 0) {
+              if constexpr (kPair) {
+                tma_load_3d_pair_hint(dst, tm, bar, x, y, z, pol_keep);
+              } else {
+                tma_load_3d_hint(dst, tm, bar, x, y, z, pol_keep);
+              }
+            } else {
+              load(dst, tm, x, y, z);
+            }
+          };
           const int k0 = kb * kBK;
           if constexpr (!kAT) {
-            load(smem_u32(sm.a[stage]), &tmA, k0, m0, za);  // 128 rows x kBK, K-major
+            load_keep(smem_u32(sm.a[stage]), &tmA, k0, m0, za);  // 128 rows x kBK, K-major
           } else {
 #pragma unroll
             for (int j = 0; j < kBM / K_::kMNElems; ++j)  // kBK rows of k x kMNElems of m
-              load(smem_u32(sm.a[stage] + j * kMNBoxBytes), &tmA, m0 + K_::kMNElems * j, k0, za);
+              load_keep(smem_u32(sm.a[stage] + j * kMNBoxBytes), &tmA, m0 + K_::kMNElems * j, k0,
+                        za);
           }
           if constexpr (!kBT) {
 #pragma unroll

@@ -151,6 +151,34 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
       "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+// L2 eviction-priority policies (createpolicy) and the TMA forms that carry
+// one (.L2::cache_hint). Hints only: they change what L2 keeps, not results.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *tmap, uint32_t bar,
+                                                 int c0, int c1, int c2, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;\n" ::"r"(dst),
+      "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(pol)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_3d_hint(const void *tmap, int c0, int c1, int c2,
+                                                  uint32_t src, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint"
+      " [%0, {%1, %2, %3}], [%4], %5;\n" ::"l"(tmap),
+      "r"(c0), "r"(c1), "r"(c2), "r"(src), "l"(pol)
+      : "memory");
+}
 __device__ __forceinline__ void tma_store_3d(const void *tmap, int c0, int c1, int c2,
                                              uint32_t src) {
   asm volatile(
@@ -413,6 +441,15 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void *tmap,
       "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile"
       ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];\n" ::"r"(dst),
       "l"(tmap), "r"(cluster_bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const void *tmap,
+                                                      uint32_t cluster_bar, int c0, int c1, int c2,
+                                                      uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile"
+      ".mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;\n" ::"r"(dst),
+      "l"(tmap), "r"(cluster_bar), "r"(c0), "r"(c1), "r"(c2), "l"(pol)
       : "memory");
 }
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *tmap,
