@@ -21,6 +21,18 @@
 // deterministic (and exact in the int8 mode, whose split points fall on
 // 1024-k chunks), and no part waits for another.
 //
+// Stream-K form (gemm_tc_skinny_sk_kernel), for 9..32 rows and 16..151 column
+// blocks: the (column block, k-unit) space is cut into one equal contiguous
+// range per SM, so no SM idles when #SMs is not a multiple of the number of
+// blocks. A range is a run of segments (a block and a k-range of it); a block
+// covered by one CTA is written directly, a block shared by several CTAs (only
+// a range's first and last segment can be) gets each share in a workspace
+// slot, and the block's last contributor adds them in CTA order. Measured on
+// GB300 (bf16, N = K = 8192): M = 16 35.3 vs 38.1 us, M = 32 36.1 vs 45.8 us,
+// 32 x 4096 x 4096 21.4 vs 26.5 us against the per-block split, which stays
+// faster for <= 8 rows (HBM-bound: 128 CTAs already saturate it) and for few
+// column blocks (many contributors per block).
+//
 // Sources: as gemm_tc_kernel.cuh (C = alpha*A*B + beta*C, "Sgemm [128,128,8]"; half /
 // bfloat16 x half / bfloat16 -> float and signed char -> int, C++ warp matrix
 // function page, type table). The pages have no skinny-shape kernel; this is a
@@ -74,10 +86,18 @@ struct SkArgs {
   Out alpha, beta;
   Out *C;
   int64_t ldc;
+  // Per-block split (gemm_tc_skinny_kernel): every CTA one part of one block.
   int split;           // parts of k per column block
-  uint32_t *counters;  // parts done, one per column block (split > 1), zero at launch
-  Out *ws;             // partial sums [split][M][ws_ld] (split > 1)
+  uint32_t *counters;  // parts done, one per column block (split > 1), zero at launch;
+                       // stream-K: one per CTA, indexed by a shared block's first contributor
+  Out *ws;             // partial sums [split][M][ws_ld] (split > 1); stream-K:
+                       // [CTA][slot 0 (first segment) or 1 (last)][M][128]
   int64_t ws_ld;       // column blocks * 128
+  // Stream-K (gemm_tc_skinny_sk_kernel): `units` = column blocks * nunits
+  // k-units over gridDim.x CTAs.
+  int64_t units;
+  int nunits;
+  int small_index;  // (units + nunits + 1) * gridDim.x < 2^32: segment arithmetic in 32 bits
   uint32_t idesc;
   uint32_t *err_word;
 };
@@ -336,6 +356,328 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// The CTA whose range holds unit x: the largest c with c * U / G <= x. I is
+// the index type: 32 bits when U * G fits (integer division is a software
+// routine; the 64-bit one costs several times more).
+template <typename I>
+__device__ __forceinline__ int unit_owner(I x, I U, I G) {
+  return static_cast<int>(((x + 1) * G - 1) / U);
+}
+
+// One segment of a CTA's range: block `blk`, k-blocks [kb0, kb1), and whether
+// another CTA also contributes to the block (then `first` is the block's
+// first contributor, `rank` this CTA's place among them, `count` their number
+// and `slot` this segment's workspace slot).
+struct Segment {
+  int blk, kb0, kb1;
+  bool shared;
+  int first, rank, count, slot;
+};
+
+// Segment number `s` of CTA c (false past its range's end). `first_slot` is
+// the workspace slot in which the block's first contributor keeps its share:
+// 0 if the block is that CTA's first segment, else 1 (every later contributor
+// starts inside the block, so its share is in its slot 0).
+template <typename I>
+__device__ __forceinline__ bool get_segment_t(int c, int s, I G, I U, I nunits, int kb_unit,
+                                              int KB, Segment &g, int &first_slot) {
+  const I u0 = static_cast<I>(c) * U / G, u1 = (static_cast<I>(c) + 1) * U / G;
+  I u = u0;
+  for (int i = 0; i < s && u < u1; ++i) {
+    const I blk_end = (u / nunits + 1) * nunits;
+    u = blk_end < u1 ? blk_end : u1;
+  }
+  if (u >= u1) return false;
+  g.blk = static_cast<int>(u / nunits);
+  const I base = static_cast<I>(g.blk) * nunits;
+  const I end = base + nunits < u1 ? base + nunits : u1;
+  g.kb0 = static_cast<int>(u - base) * kb_unit;
+  g.kb1 = min(KB, static_cast<int>(end - base) * kb_unit);
+  g.first = unit_owner<I>(base, U, G);
+  const int last = unit_owner<I>(base + nunits - 1, U, G);
+  g.count = last - g.first + 1;
+  g.shared = g.count > 1;
+  g.rank = c - g.first;
+  g.slot = (u == u0) ? 0 : 1;
+  first_slot = (static_cast<I>(g.first) * U / G == base) ? 0 : 1;
+  return true;
+}
+
+__device__ __forceinline__ bool get_segment(int c, int s, int G, int64_t U, int nunits,
+                                            int kb_unit, int KB, bool small, Segment &g,
+                                            int &first_slot) {
+  if (small)
+    return get_segment_t<uint32_t>(c, s, static_cast<uint32_t>(G), static_cast<uint32_t>(U),
+                                   static_cast<uint32_t>(nunits), kb_unit, KB, g, first_slot);
+  return get_segment_t<int64_t>(c, s, G, U, nunits, kb_unit, KB, g, first_slot);
+}
+
+// Stream-K form: the same pipeline over a CTA's run of segments (see the
+// work-split comment at the top of the file).
+template <bool kInt>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_skinny_sk_kernel(const __grid_constant__ CUtensorMap tmA,
+                          const __grid_constant__ CUtensorMap tmB, const SkArgs<kInt> p) {
+  using Out = typename SkArgs<kInt>::Out;
+  extern __shared__ uint8_t smem_raw[];
+  SkSmem &sm = *reinterpret_cast<SkSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  volatile int *abort = &sm.abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&sm.full[s]), 1);
+      mbar_init(smem_u32(&sm.empty[s]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&sm.tmem_full[i]), 1);
+      mbar_init(smem_u32(&sm.tmem_empty[i]), kEpiWarps);
+    }
+    mbar_init(smem_u32(&sm.drain), 1);
+    sm.abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = sm.tmem_base;
+
+  // This CTA's range of the (column block, k-unit) space, as segments.
+  const int c = static_cast<int>(blockIdx.x);
+  const int G = static_cast<int>(gridDim.x);
+  const int KB = (p.K + kBK - 1) / kBK;
+  const int kb_unit = kInt ? kChunkKB : 1;
+  const int chunk_kb = kInt ? kChunkKB : KB;
+  const uint32_t a_bytes = static_cast<uint32_t>(p.mp) * kBK * 2;
+  const bool small = p.small_index != 0;
+  Segment g;
+  int first_slot = 0;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, issued = 0, issued_parity = 0;
+      bool ok = true;
+      for (int s = 0; ok && get_segment(c, s, G, p.units, p.nunits, kb_unit, KB, small, g, first_slot); ++s) {
+        const int n0 = g.blk * kBN;
+        for (int kb = g.kb0; kb < g.kb1; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&sm.empty[stage]), phase ^ 1u, abort, p.err_word,
+                                 kWaitEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full_bar = smem_u32(&sm.full[stage]);
+          mbar_arrive_expect_tx(full_bar, kBBytes + a_bytes);
+          tma_load_2d(smem_u32(sm.b[stage]), &tmB, full_bar, n0, kb * kBK);
+          tma_load_2d(smem_u32(sm.b[stage] + kBBox), &tmB, full_bar, n0 + 64, kb * kBK);
+          tma_load_2d(smem_u32(sm.a[stage]), &tmA, full_bar, kb * kBK, 0);
+          issued |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      for (int s = 0; s < kStages; ++s)
+        if (issued & (1u << s))
+          drain_wait(smem_u32(&sm.full[s]), (issued_parity >> s) & 1u, p.err_word);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, chunk = 0;
+      bool ok = true, any = false;
+      for (int s = 0; ok && get_segment(c, s, G, p.units, p.nunits, kb_unit, KB, small, g, first_slot); ++s)
+      for (int c0 = g.kb0; ok && c0 < g.kb1; c0 += chunk_kb) {
+        const int c1 = min(g.kb1, c0 + chunk_kb);
+        const uint32_t buf = chunk & 1u, use = (chunk >> 1) & 1u;
+        ++chunk;
+        if (!mbar_wait_bounded(smem_u32(&sm.tmem_empty[buf]), use ^ 1u, abort, p.err_word,
+                               kWaitTmemEmpty))
+          break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + buf * kBufCols;
+        for (int kb = c0; kb < c1; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&sm.full[stage]), phase, abort, p.err_word,
+                                 kWaitFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t b_addr = smem_u32(sm.b[stage]);
+          const uint32_t a_addr = smem_u32(sm.a[stage]);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            // MMA A operand = B tile, N-major: LBO = one 64-column box, SBO = 1 KiB
+            // between groups of 8 k-rows; 16 k = 16 rows of 128 B further.
+            const uint64_t adesc = smem_desc(b_addr + kk * 2048, kBBox, 1024, 2u);
+            // MMA B operand = A tile, K-major: SBO = 8 rows of 128 B; 16 k = 32 B.
+            const uint64_t bdesc = smem_desc(a_addr + kk * 32, 16, 1024, 2u);
+            tc_mma_f16(d_tmem, adesc, bdesc, p.idesc, (kb > c0 || kk > 0) ? 1u : 0u);
+          }
+          any = true;
+          tc_commit(smem_u32(&sm.empty[stage]));
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&sm.tmem_full[buf]));
+      }
+      if (any) {
+        tc_commit(smem_u32(&sm.drain));
+        drain_wait(smem_u32(&sm.drain), 0, p.err_word);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    // Lanes are columns of C: lane -> column n0 + 32 * quarter + lane.
+    const int quarter = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    // Every epilogue warp walks every segment and meets the same named
+    // barriers whatever its waits return; whether a segment is written is
+    // decided once (seg_skip, read after a barrier) so all warps agree.
+    __shared__ int last, seg_skip;
+    uint32_t chunk = 0;
+    for (int s = 0; get_segment(c, s, G, p.units, p.nunits, kb_unit, KB, small, g, first_slot); ++s) {
+    const int n = g.blk * kBN + quarter * 32 + lane;
+    uint32_t acc[kInt ? kMaxM : 1];
+    if constexpr (kInt) {
+#pragma unroll
+      for (int j = 0; j < kMaxM; ++j) acc[j] = 0;
+    }
+    float facc[kInt ? 1 : kMaxM];
+    bool done = true;  // every chunk of the segment arrived
+    for (int c0 = g.kb0; c0 < g.kb1; c0 += chunk_kb) {
+      const uint32_t buf = chunk & 1u, use = (chunk >> 1) & 1u;
+      ++chunk;
+      int got = 0;
+      if (lane == 0)
+        got = mbar_wait_bounded(smem_u32(&sm.tmem_full[buf]), use, abort, p.err_word,
+                                kWaitTmemFull);
+      got = __shfl_sync(0xffffffffu, got, 0);
+      if (!got) {
+        done = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t taddr = tmem_base + lane_base + buf * 64;
+#pragma unroll
+      for (int c = 0; c < kMaxM; c += 16) {
+        if (c < p.mp) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(taddr + c, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if constexpr (kInt) {
+              acc[c + j] += static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[j])));
+            } else {
+              facc[c + j] = __uint_as_float(r[j]);
+            }
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.tmem_empty[buf]));
+    }
+    auto value = [&](int m) -> Out {
+      if constexpr (kInt) {
+        return static_cast<int32_t>(acc[m]);
+      } else {
+        return facc[m];
+      }
+    };
+    const bool use_c = p.beta != Out(0);
+    if (!done) *abort = 1;  // a wait gave up: the error word says so
+    epilogue_sync();
+    if (warp == 2 && lane == 0) seg_skip = *abort;
+    epilogue_sync();
+    if (seg_skip) continue;  // uniform across the epilogue warps
+    if (!g.shared) {
+      if (n < p.N) {
+#pragma unroll
+        for (int m = 0; m < kMaxM; ++m)
+          if (m < p.M) {
+            Out *cp = p.C + static_cast<int64_t>(m) * p.ldc + n;
+            *cp = axpby(p.alpha, value(m), p.beta, use_c ? *cp : Out(0), use_c);
+          }
+      }
+    } else {
+      // Store this segment's partial sums in this CTA's slot, count the
+      // contribution; the block's last contributor adds all of them in CTA
+      // order.
+      const int lc = n - g.blk * kBN;  // column within the block
+#pragma unroll
+      for (int m = 0; m < kMaxM; ++m)
+        if (m < p.M) p.ws[((static_cast<int64_t>(c) * 2 + g.slot) * p.M + m) * kBN + lc] = value(m);
+      __threadfence();
+      epilogue_sync();
+      if (warp == 2 && lane == 0)
+        last = (atomicAdd(p.counters + g.first, 1u) == static_cast<uint32_t>(g.count - 1));
+      epilogue_sync();
+      if (last) {
+        __threadfence();
+        if (n < p.N) {
+          // Contributors in CTA order (each element's sum in one fixed order);
+          // within a contributor all rows at once, so the loads overlap.
+          Out sum[kMaxM];
+#pragma unroll
+          for (int m = 0; m < kMaxM; ++m) sum[m] = Out(0);
+          for (int q = 0; q < g.count; ++q) {
+            // contributor first + q holds its share in slot 0, except the
+            // first contributor when the block is not its first segment
+            const int cq = g.first + q;
+            const int slot = q == 0 ? first_slot : 0;
+            const Out *src = p.ws + (static_cast<int64_t>(cq) * 2 + slot) * p.M * kBN + lc;
+#pragma unroll
+            for (int m = 0; m < kMaxM; ++m) {
+              if (m < p.M) {
+                const Out v = __ldcg(src + static_cast<int64_t>(m) * kBN);
+                if constexpr (kInt) {
+                  sum[m] = static_cast<int32_t>(static_cast<uint32_t>(sum[m]) +
+                                                static_cast<uint32_t>(v));
+                } else {
+                  sum[m] += v;
+                }
+              }
+            }
+          }
+#pragma unroll
+          for (int m = 0; m < kMaxM; ++m) {
+            if (m < p.M) {
+              Out *cp = p.C + static_cast<int64_t>(m) * p.ldc + n;
+              *cp = axpby(p.alpha, sum[m], p.beta, use_c ? *cp : Out(0), use_c);
+            }
+          }
+        }
+      }
+      epilogue_sync();  // `last` is read before the next segment writes it
+    }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -370,6 +712,43 @@ bool tmap16(CUtensorMap *tm, CUtensorMapDataType dt, const void *base, int64_t r
          CUDA_SUCCESS;
 }
 
+// Stream-K launch: one CTA per SM over equal shares of the (column block,
+// k-unit) space; two partial-sum slots and one counter per CTA.
+template <bool kInt>
+cudaError_t launch_stream_k(const DeviceInfo &dev, SkArgs<kInt> p, const CUtensorMap &tmA,
+                            const CUtensorMap &tmB, int blocks, int nunits, cudaStream_t stream) {
+  using Out = typename SkArgs<kInt>::Out;
+  const int64_t units = static_cast<int64_t>(blocks) * nunits;
+  const int G = units < dev.sm_count ? static_cast<int>(units) : dev.sm_count;
+  p.units = units;
+  p.nunits = nunits;
+  p.small_index = (units + nunits + 1) * static_cast<int64_t>(G) < (int64_t(1) << 32);
+  p.split = 1;
+  p.ws_ld = 0;
+  cudaMemPool_t pool;
+  cudaError_t e = device_pool(dev, &pool);
+  if (e != cudaSuccess) return e;
+  const size_t ws_bytes = static_cast<size_t>(G) * 2 * p.M * kBN * sizeof(Out);
+  const size_t cnt_off = (ws_bytes + 255) / 256 * 256;
+  void *pool_ws = nullptr;
+  e = cudaMallocFromPoolAsync(&pool_ws, cnt_off + static_cast<size_t>(G) * 4, pool, stream);
+  if (e != cudaSuccess) return e;
+  p.ws = static_cast<Out *>(pool_ws);
+  p.counters = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(pool_ws) + cnt_off);
+  e = cudaMemsetAsync(p.counters, 0, static_cast<size_t>(G) * 4, stream);
+  const size_t smem = sizeof(SkSmem) + 1024;
+  auto kern = gemm_tc_skinny_sk_kernel<kInt>;
+  if (e == cudaSuccess)
+    e = set_max_dynamic_smem(reinterpret_cast<const void *>(kern), static_cast<int>(smem),
+                             dev.device);
+  if (e == cudaSuccess) {
+    kern<<<static_cast<unsigned>(G), kThreads, smem, stream>>>(tmA, tmB, p);
+    e = cudaGetLastError();
+  }
+  cudaError_t f = cudaFreeAsync(pool_ws, stream);
+  return e != cudaSuccess ? e : f;
+}
+
 template <bool kInt>
 cudaError_t launch(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf16, int M, int N,
                    int K, typename SkArgs<kInt>::Out alpha, const void *A, int64_t lda,
@@ -392,11 +771,14 @@ cudaError_t launch(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf16, 
   if (!tmap16(&tmA, dt, A, M, K, lda, static_cast<uint32_t>(p.mp))) return cudaErrorInvalidValue;
   if (!tmap16(&tmB, dt, B, K, N, ldb, kBK)) return cudaErrorInvalidValue;
 
-  // One slice per CTA: column blocks times parts of k, at most one CTA per SM
-  // when k is split.
   const int blocks = (N + kBN - 1) / kBN;
   const int KB = (K + kBK - 1) / kBK;
   const int nunits = kInt ? (KB + kChunkKB - 1) / kChunkKB : KB;
+  if (M > 8 && blocks >= 16 && blocks < dev.sm_count && flags_ws == nullptr &&
+      static_cast<int64_t>(blocks) * nunits > dev.sm_count)
+    return launch_stream_k<kInt>(dev, p, tmA, tmB, blocks, nunits, stream);
+  // One slice per CTA: column blocks times parts of k, at most one CTA per SM
+  // when k is split.
   int split = blocks < dev.sm_count ? dev.sm_count / blocks : 1;
   if (split > kMaxSplit) split = kMaxSplit;
   if (split > nunits) split = nunits;

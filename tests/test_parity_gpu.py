@@ -296,6 +296,26 @@ def test_skinny_shapes(gemm_mod, oracle_mod, dtype, M):
         out.check_canaries()
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.int8], ids=str)
+@pytest.mark.parametrize("shape", [(9, 2048, 4096), (24, 4160, 8200), (32, 8192, 2048),
+                                   (16, 19200, 1024)], ids=lambda s: "x".join(map(str, s)))
+def test_skinny_stream_k(gemm_mod, oracle_mod, dtype, shape):
+    """9..32 rows and 16..151 column blocks of 128: the stream-K form of the
+    transposed-role kernel (equal shares of the (block, k) space per SM; blocks
+    shared by several CTAs are summed by their last contributor in CTA order).
+    int8 with K not a multiple of 16 takes the same kernel on widened operands
+    (1024-k units). Every output checked (M is small)."""
+    M, N, K = shape
+    if dtype == torch.int8:
+        K = K + 3  # rows not 16-byte multiples: not the small-M kernel
+        p = w.problem(M, N, K, dtype, "int8", 401 + M, alpha=3, beta=-2, c_dist="int")
+    else:
+        p = w.problem(M, N, K, dtype, "normal", 401 + M, alpha=0.5, beta=-1.0, c_dist="normal")
+    got, out = run_gpu(gemm_mod, p)
+    assert_parity(got, oracle_of(oracle_mod, p), exact=(dtype == torch.int8))
+    out.check_canaries()
+
+
 @pytest.mark.parametrize("dtype", ALL_DTYPES, ids=str)
 @pytest.mark.parametrize("shape", [(8, 520, 8192), (32, 1024, 4096), (1, 128, 16384),
                                    (3, 4096, 2048)], ids=lambda s: "x".join(map(str, s)))
