@@ -10,7 +10,7 @@ cudaError_t launch_gemm_tc_f16_ex(const DeviceInfo &dev, bool is_bf16, const Bat
                                   cudaStream_t stream) {
   // Short, wide problems: the transposed-role kernel streams B at HBM speed
   // instead of multiplying a mostly-zero 256-row tile.
-  if (M <= kSkinnyMaxM && ops.plain())
+  if (tc_skinny_route(M, N, dev.sm_count) && ops.plain())
     return launch_tc_skinny_float(dev, is_bf16, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
                                   stream);
   const CUtensorMapDataType dt =

@@ -119,7 +119,7 @@ cudaError_t run_int(const DeviceInfo &dev, const BatchOps &ops, int M, int N, in
     e = widen8<T8>(dev, B, ldb, b16, w.ldb16, w.b_rows, w.b_cols, stream, w.nb, ops.stride_b);
   if (e != cudaSuccess) return e;
   // Short, wide int8 problems: the transposed-role kernel (1024-k chunks).
-  if (kKind == kKindS8 && M <= kSkinnyMaxM && ops.plain())
+  if (kKind == kKindS8 && tc_skinny_route(M, N, dev.sm_count) && ops.plain())
     return launch_tc_skinny_int(dev, M, N, K, alpha, a16, w.lda16, b16, w.ldb16, beta, C, ldc,
                                 stream, flags, flags_words);
   BatchOps wide = ops;

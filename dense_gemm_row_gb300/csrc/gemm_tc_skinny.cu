@@ -21,7 +21,7 @@
 // deterministic (and exact in the int8 mode, whose split points fall on
 // 1024-k chunks), and no part waits for another.
 //
-// Stream-K form (gemm_tc_skinny_sk_kernel), for 9..32 rows and 16..151 column
+// Stream-K form (gemm_tc_skinny_sk_kernel), for 9..64 rows and 16..151 column
 // blocks: the (column block, k-unit) space is cut into one equal contiguous
 // range per SM, so no SM idles when #SMs is not a multiple of the number of
 // blocks. A range is a run of segments (a block and a k-range of it); a block
@@ -31,7 +31,8 @@
 // GB300 (bf16, N = K = 8192): M = 16 35.3 vs 38.1 us, M = 32 36.1 vs 45.8 us,
 // 32 x 4096 x 4096 21.4 vs 26.5 us against the per-block split, which stays
 // faster for <= 8 rows (HBM-bound: 128 CTAs already saturate it) and for few
-// column blocks (many contributors per block).
+// column blocks (many contributors per block). 33..64 rows take this kernel
+// only in the stream-K form (tc_skinny_route).
 //
 // Sources: as gemm_tc_kernel.cuh (C = alpha*A*B + beta*C, "Sgemm [128,128,8]"; half /
 // bfloat16 x half / bfloat16 -> float and signed char -> int, C++ warp matrix
@@ -829,6 +830,12 @@ cudaError_t launch(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf16, 
 }
 
 }  // namespace
+
+bool tc_skinny_route(int M, int N, int sm_count) {
+  if (M <= kSkinnyMaxM) return true;
+  const int blocks = (N + kBN - 1) / kBN;
+  return M <= kMaxM && blocks >= 16 && blocks < sm_count;
+}
 
 cudaError_t launch_tc_skinny_float(const DeviceInfo &dev, bool is_bf16, int M, int N, int K,
                                    float alpha, const void *A, int64_t lda, const void *B,

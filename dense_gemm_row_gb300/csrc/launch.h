@@ -104,6 +104,12 @@ cudaError_t launch_gemm_s8_scratch(const DeviceInfo &dev, int M, int N, int K, i
 // Measured on GB300 (N = K = 8192): faster than the 256-row CTA-pair tiles up to
 // M = 32 (M = 1: 34 vs 50 us), slower at M = 64.
 constexpr int kSkinnyMaxM = 32;
+// Whether the 16-bit / int8 tensor-core paths take the transposed-role kernel
+// for an M x N problem: up to 32 rows always; 33..64 rows when its stream-K
+// form applies (16..sm_count-1 column blocks of 128). Measured on GB300 at
+// 33..64 rows against the 256-row pair tiles: bf16 N = K = 8192 36.4-38.6 vs
+// 38.5-39.1 us, 64 x 4096 x 4096 23.4 vs 31.3 us; int8 77 vs 97 us.
+bool tc_skinny_route(int M, int N, int sm_count);
 cudaError_t launch_tc_skinny_float(const DeviceInfo &dev, bool is_bf16, int M, int N, int K,
                                    float alpha, const void *A, int64_t lda, const void *B,
                                    int64_t ldb, float beta, float *C, int64_t ldc,
