@@ -66,10 +66,10 @@ WORKLOADS = {
 
 # Sources whose change invalidates recorded ncu traffic for a workload.
 KERNEL_SOURCES = {
-    "bf16_8192": ["gemm_tc_kernel.cuh", "gemm_tc_f16.cu", "ptx.cuh"],
-    "f16_8192": ["gemm_tc_kernel.cuh", "gemm_tc_f16.cu", "ptx.cuh"],
-    "s8_8192": ["gemm_tc_kernel.cuh", "gemm_tc_int.cu", "ptx.cuh"],
-    "f32_4096": ["sgemm_simt.cu", "ptx.cuh"],
+    "bf16_8192": ["gemm_tc_kernel.cuh", "gemm_tc_f16.cu", "work_split.cuh", "ptx.cuh"],
+    "f16_8192": ["gemm_tc_kernel.cuh", "gemm_tc_f16.cu", "work_split.cuh", "ptx.cuh"],
+    "s8_8192": ["gemm_tc_kernel.cuh", "gemm_tc_int.cu", "work_split.cuh", "ptx.cuh"],
+    "f32_4096": ["sgemm_simt.cu", "work_split.cuh", "ptx.cuh"],
 }
 
 
