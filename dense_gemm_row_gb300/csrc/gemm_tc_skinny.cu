@@ -1,4 +1,4 @@
-// gemm_tc_skinny.cu -- tensor-core GEMM for short, wide problems (M <= 32).
+// gemm_tc_skinny.cu -- tensor-core GEMM for short, wide problems (M <= 64).
 //
 //     C = alpha * A * B + beta * C       A: M x K, B: K x N, C: M x N, row-major
 //

@@ -97,12 +97,12 @@ cudaError_t launch_gemm_s8_scratch(const DeviceInfo &dev, int M, int N, int K, i
                                    int32_t beta, int32_t *C, int64_t ldc, void *scratch,
                                    uint32_t *flags, size_t flags_words, cudaStream_t stream);
 
-// Short, wide problems (M <= kSkinnyMaxM) on the tensor cores, computed as
-// C^T = B^T A^T so that N fills the MMA rows (gemm_tc_skinny.cu). 16-bit inputs
-// with the same layout rule as launch_gemm_tc_f16; the int version takes the
-// fp16-widened operands of the int8 path and optional caller-provided flags.
-// Measured on GB300 (N = K = 8192): faster than the 256-row CTA-pair tiles up to
-// M = 32 (M = 1: 34 vs 50 us), slower at M = 64.
+// Short, wide problems on the tensor cores, computed as C^T = B^T A^T so that N
+// fills the MMA rows (gemm_tc_skinny.cu, up to 64 rows; which problems take it:
+// tc_skinny_route). 16-bit inputs with the same layout rule as
+// launch_gemm_tc_f16; the int version takes the fp16-widened operands of the
+// int8 path and optional caller-provided flags. kSkinnyMaxM is also the row
+// limit of the small-M SIMT kernel (gemm_small_m.cu).
 constexpr int kSkinnyMaxM = 32;
 // Whether the 16-bit / int8 tensor-core paths take the transposed-role kernel
 // for an M x N problem: up to 32 rows always; 33..64 rows when its stream-K
