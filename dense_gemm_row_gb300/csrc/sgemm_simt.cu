@@ -3,24 +3,26 @@
 //     C = alpha * A * B + beta * C
 //
 // Design (restated from the pages, rebuilt for sm_103a):
-//  * One CTA of 256 threads computes a 128 x 128 tile of C; every thread owns
-//    8 x 8 outputs split into four 4 x 4 blocks at row offsets {0, 64} and
-//    column offsets {0, 64}, so that neighbouring threads touch neighbouring
+//  * One CTA computes a 128 x 128 tile of C; every thread owns 8 rows x TN
+//    columns of it, in 4 x 4 blocks at row offsets {0, 64} and column offsets
+//    128 / (TN / 4) apart, so that neighbouring threads touch neighbouring
 //    16-byte chunks of C ("Sgemm [128,128,8]", the kernel's header comment:
 //    256 threads, 128x128 tile, 8x8 per thread, cyclic distribution of C for
-//    coalescing).
+//    coalescing). Two shapes: TN = 8 (256 threads, the pages' shape) and
+//    TN = 16 (128 threads, 8 x 16 per thread: half the shared loads per FMA),
+//    both at two CTAs per SM.
 //  * A is staged into shared memory transposed (k-major), so the eight A
 //    values a thread needs for one k are two 16-byte shared loads ("Sgemm
 //    [128,128,8]", the transposed smema buffer; "CUDA学习之路[11]", section
 //    V3 双缓冲, the transposed A tile).
-//  * Staging uses cp.async with an S-stage ring (default: two stages of 32
-//    values of k) instead of the pages' register prefetch plus two shared
-//    buffers: the same overlap of the next tile's load with this tile's FMAs,
-//    without holding the prefetch in registers. The transposing copy of A is
-//    4 bytes per lane, arranged so a warp's 32 stores hit 32 distinct banks.
-//  * The 64 FMAs per k of a thread are issued as 32 packed fma.rn.f32x2
-//    (two independent fp32 FMAs, each rounded to nearest like fmaf), which
-//    halves the issue slots the FP32 pipe needs on sm_103a.
+//  * Staging uses cp.async with an S-stage ring of BK-deep k tiles instead of
+//    the pages' register prefetch plus two shared buffers: the same overlap of
+//    the next tiles' loads with this tile's FMAs, without holding the prefetch
+//    in registers. The transposing copy of A is 4 bytes per lane, arranged so
+//    a warp's 32 stores hit 32 distinct banks.
+//  * The FMAs of a thread are issued as packed fma.rn.f32x2 (two independent
+//    fp32 FMAs, each rounded to nearest like fmaf), which halves the issue
+//    slots the FP32 pipe needs on sm_103a.
 //  * Residual tiles: out-of-range cells of the A and B tiles are filled with
 //    zeros by the copy itself (cp.async with a zero source size) and the
 //    epilogue's stores are guarded, so any M, N, K works ("使用CUDA和瓦片算法
@@ -39,13 +41,18 @@
 //    N x K is copied with the same conflict-free transposing pattern as A
 //    (its tile then also has a padded row stride of 132). The batch entry is
 //    blockIdx.y.
+//  * Grids of at least two waves of resident CTAs run TN = 16 with 8-deep k
+//    tiles in a 6-stage ring (one CTA per tile); smaller single problems run
+//    TN = 8 with 32-deep k tiles in a 2-stage ring on the persistent k-split
+//    grid, where the extra warps per SM pay more than the wider thread tile.
 #include <cstdint>
 
 #include <cuda_runtime.h>
 
 #include <map>
 #include <mutex>
-#include <utility>
+#include <tuple>
+#include <type_traits>
 
 #include "launch.h"
 #include "ptx.cuh"
@@ -68,8 +75,20 @@ __device__ __forceinline__ void ffma2(float &c0, float &c1, float a, float b0, f
 
 constexpr int kBM = 128;
 constexpr int kBN = 128;
-constexpr int kThreads = 256;
 constexpr int kGroupM = 8;  // tiles of M visited together (L2 reuse of B columns)
+
+// Outputs per thread: 8 rows x TN columns (TN = 8: 256 threads; TN = 16: 128
+// threads). Rows sit at offsets {0, 64}, columns in TN / 4 blocks of 4,
+// 128 / (TN / 4) apart; lanes form a 4 x 8 grid, warps a grid of (64 / 16)
+// rows x (block stride / 32) columns.
+template <int TN>
+struct SimtShape {
+  static_assert(TN == 8 || TN == 16, "8 or 16 columns per thread");
+  static constexpr int kThreads = kBM * kBN / (8 * TN);
+  static constexpr int kColBlocks = TN / 4;
+  static constexpr int kColStride = kBN / kColBlocks;  // 64 or 32
+  static constexpr int kWarpsN = kColStride / 32;
+};
 
 struct SimtArgs {
   int M, N, K;
@@ -116,97 +135,96 @@ __device__ __forceinline__ void tile_coords(int bid, int tiles_m, int tiles_n, i
 // Copies a 4 x 8 (rows x k) block per warp instruction from a row-major matrix
 // whose rows run along k into the k-major tile dst[k][row] (row stride 132):
 // lane = 8 * row + k, so one warp reads four 32-byte segments and its 32
-// stores hit 32 distinct banks. rows_valid / k_valid bound the source.
-template <int BK>
-__device__ __forceinline__ void copy_transposing(const float *src, int64_t ld, float (*dst)[kAStride],
-                                                 int r0, int k0, int rows_valid, int k_valid,
-                                                 int tid) {
+// stores hit 32 distinct banks. rows_valid / k_valid bound the source. Each
+// of the THREADS threads issues kCount copies; one() issues copy number c.
+template <int BK, int THREADS>
+struct TransposingCopy {
   static_assert(BK % 8 == 0, "transposing copies take k in groups of 8");
-  constexpr int kGroupsK = BK / 8;
-  const int warp = tid >> 5, lane = tid & 31;
-  const int r_lo = lane >> 3, k_lo = lane & 7;
-#pragma unroll
-  for (int i = 0; i < BK / 2; ++i) {
-    const int pair = warp * (BK / 2) + i;        // 0 .. 4*BK-1
-    const int r = (pair / kGroupsK) * 4 + r_lo;   // 32 groups of 4 rows
-    const int k = (pair % kGroupsK) * 8 + k_lo;   // groups of 8 k
+  static constexpr int kCount = 4 * BK / (THREADS / 32);
+  __device__ static __forceinline__ void one(int c, const float *src, int64_t ld,
+                                             float (*dst)[kAStride], int r0, int k0,
+                                             int rows_valid, int k_valid, int tid) {
+    constexpr int kGroupsK = BK / 8;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int pair = warp * kCount + c;                // 0 .. 4*BK-1
+    const int r = (pair / kGroupsK) * 4 + (lane >> 3);  // 32 groups of 4 rows
+    const int k = (pair % kGroupsK) * 8 + (lane & 7);   // groups of 8 k
     const int gr = r0 + r, gk = k0 + k;
     const bool ok = gr < rows_valid && gk < k_valid;
     const float *p = ok ? src + static_cast<int64_t>(gr) * ld + gk : src;
     cp_async_4(smem_u32(&dst[k][r]), p, ok ? 4u : 0u);
   }
-}
+};
 
 // Copies rows k0 .. k0+BK-1, columns c0 .. c0+127 of a row-major matrix whose
 // rows run along k straight into dst[k][col]: 16-byte chunks when VEC (every
 // chunk then lies wholly inside or outside the matrix), 4-byte elements
-// otherwise.
-template <int BK, bool VEC, int Stride>
-__device__ __forceinline__ void copy_straight(const float *src, int64_t ld, float (*dst)[Stride],
-                                              int k0, int c0, int k_valid, int c_valid, int tid) {
-  if constexpr (VEC) {
-    constexpr int kChunks = BK * 128 / 4 / kThreads;
-#pragma unroll
-    for (int i = 0; i < kChunks; ++i) {
-      const int c = tid + i * kThreads;
-      const int row = c >> 5;
-      const int col = (c & 31) * 4;
-      const int gk = k0 + row, gc = c0 + col;
-      const bool ok = gk < k_valid && gc < c_valid;
-      const float *p = ok ? src + static_cast<int64_t>(gk) * ld + gc : src;
+// otherwise. Each of the THREADS threads issues kCount copies.
+template <int BK, bool VEC, int Stride, int THREADS>
+struct StraightCopy {
+  static constexpr int kCount = VEC ? BK * 128 / 4 / THREADS : BK * 128 / THREADS;
+  __device__ static __forceinline__ void one(int c, const float *src, int64_t ld,
+                                             float (*dst)[Stride], int k0, int c0, int k_valid,
+                                             int c_valid, int tid) {
+    const int e = tid + c * THREADS;
+    const int row = VEC ? e >> 5 : e >> 7;
+    const int col = VEC ? (e & 31) * 4 : e & 127;
+    const int gk = k0 + row, gc = c0 + col;
+    const bool ok = gk < k_valid && gc < c_valid;
+    const float *p = ok ? src + static_cast<int64_t>(gk) * ld + gc : src;
+    if constexpr (VEC)
       cp_async_16(smem_u32(&dst[row][col]), p, ok ? 16u : 0u);
-    }
-  } else {
-    constexpr int kPer = BK * 128 / kThreads;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int e = tid + i * kThreads;
-      const int row = e >> 7;
-      const int col = e & 127;
-      const int gk = k0 + row, gc = c0 + col;
-      const bool ok = gk < k_valid && gc < c_valid;
-      const float *p = ok ? src + static_cast<int64_t>(gk) * ld + gc : src;
+    else
       cp_async_4(smem_u32(&dst[row][col]), p, ok ? 4u : 0u);
-    }
   }
-}
+};
 
 // One BK-deep stage: the A tile (k-major, 128 rows of op(A)) and the B tile
 // (k rows x 128 columns of op(B)). A_T / B_T: the operand is stored
 // transposed; VEC_A / VEC_B: its straight copy may use 16-byte chunks.
-template <int BK, bool A_T, bool VEC_A, bool B_T, bool VEC_B, int BStride>
+template <int BK, int THREADS, bool A_T, bool VEC_A, bool B_T, bool VEC_B, int BStride>
 __device__ __forceinline__ void load_tile(const SimtArgs &p, const float *A, const float *B,
                                           float (*sa)[kAStride], float (*sb)[BStride], int m0,
                                           int n0, int k0, int tid) {
-  if constexpr (A_T) {
-    copy_straight<BK, VEC_A, kAStride>(A, p.lda, sa, k0, m0, p.K, p.M, tid);  // stored K x M
-  } else {
-    copy_transposing<BK>(A, p.lda, sa, m0, k0, p.M, p.K, tid);  // stored M x K
+  using CA = typename std::conditional<A_T, StraightCopy<BK, VEC_A, kAStride, THREADS>,
+                                       TransposingCopy<BK, THREADS>>::type;
+  using CB = typename std::conditional<B_T, TransposingCopy<BK, THREADS>,
+                                       StraightCopy<BK, VEC_B, BStride, THREADS>>::type;
+#pragma unroll
+  for (int c = 0; c < CA::kCount; ++c) {
+    if constexpr (A_T)
+      CA::one(c, A, p.lda, sa, k0, m0, p.K, p.M, tid);  // stored K x M
+    else
+      CA::one(c, A, p.lda, sa, m0, k0, p.M, p.K, tid);  // stored M x K
   }
-  if constexpr (B_T) {
-    copy_transposing<BK>(B, p.ldb, sb, n0, k0, p.N, p.K, tid);  // stored N x K
-  } else {
-    copy_straight<BK, VEC_B, BStride>(B, p.ldb, sb, k0, n0, p.K, p.N, tid);  // stored K x N
+#pragma unroll
+  for (int c = 0; c < CB::kCount; ++c) {
+    if constexpr (B_T)
+      CB::one(c, B, p.ldb, sb, n0, k0, p.N, p.K, tid);  // stored N x K
+    else
+      CB::one(c, B, p.ldb, sb, k0, n0, p.K, p.N, tid);  // stored K x N
   }
 }
 
 // The k-loop of one 128 x 128 tile at (m0, n0) over k-tiles [kt0, kt1):
 // acc += op(A) op(B) over those k. Leaves shared memory free for the next
-// tile (every copy waited for, every thread past its last read).
-template <int BK, int STAGES, bool A_T, bool VEC_A, bool B_T, bool VEC_B, int BStride>
+// tile (every copy waited for, every thread past its last read). The k-tile's
+// loop is unrolled whole, so the compiler schedules each k's shared loads
+// ahead of the previous k's FMAs.
+template <int TN, int BK, int STAGES, bool A_T, bool VEC_A, bool B_T, bool VEC_B, int BStride>
 __device__ __forceinline__ void tile_mainloop(const SimtArgs &p, const float *A, const float *B,
                                               SimtSmem<BK, STAGES, BStride> &sm, int m0, int n0,
                                               int kt0, int kt1, int tid, int rm, int cn,
-                                              float (&acc)[8][8]) {
+                                              float (&acc)[8][TN]) {
+  using Sh = SimtShape<TN>;
   const int KT = kt1 - kt0;
 #pragma unroll
   for (int s = 0; s < STAGES - 1; ++s) {
     if (s < KT)
-      load_tile<BK, A_T, VEC_A, B_T, VEC_B, BStride>(p, A, B, sm.a[s], sm.b[s], m0, n0,
-                                                      (kt0 + s) * BK, tid);
+      load_tile<BK, Sh::kThreads, A_T, VEC_A, B_T, VEC_B, BStride>(p, A, B, sm.a[s], sm.b[s], m0,
+                                                                  n0, (kt0 + s) * BK, tid);
     cp_async_commit();
   }
-
   for (int kt = 0; kt < KT; ++kt) {
     cp_async_wait<STAGES - 2>();
     __syncthreads();  // tile kt landed for everyone; tile kt-1 fully consumed
@@ -214,8 +232,8 @@ __device__ __forceinline__ void tile_mainloop(const SimtArgs &p, const float *A,
       const int nt = kt + STAGES - 1;
       if (nt < KT) {
         const int s = nt % STAGES;
-        load_tile<BK, A_T, VEC_A, B_T, VEC_B, BStride>(p, A, B, sm.a[s], sm.b[s], m0, n0,
-                                                        (kt0 + nt) * BK, tid);
+        load_tile<BK, Sh::kThreads, A_T, VEC_A, B_T, VEC_B, BStride>(
+            p, A, B, sm.a[s], sm.b[s], m0, n0, (kt0 + nt) * BK, tid);
       }
       cp_async_commit();
     }
@@ -224,20 +242,26 @@ __device__ __forceinline__ void tile_mainloop(const SimtArgs &p, const float *A,
     for (int k = 0; k < BK; ++k) {
       const float4 a_lo = *reinterpret_cast<const float4 *>(&sm.a[s][k][rm]);
       const float4 a_hi = *reinterpret_cast<const float4 *>(&sm.a[s][k][rm + 64]);
-      const float4 b_lo = *reinterpret_cast<const float4 *>(&sm.b[s][k][cn]);
-      const float4 b_hi = *reinterpret_cast<const float4 *>(&sm.b[s][k][cn + 64]);
       const float a[8] = {a_lo.x, a_lo.y, a_lo.z, a_lo.w, a_hi.x, a_hi.y, a_hi.z, a_hi.w};
-      const float b[8] = {b_lo.x, b_lo.y, b_lo.z, b_lo.w, b_hi.x, b_hi.y, b_hi.z, b_hi.w};
+      float b[TN];
+#pragma unroll
+      for (int q = 0; q < Sh::kColBlocks; ++q) {
+        const float4 v = *reinterpret_cast<const float4 *>(&sm.b[s][k][cn + q * Sh::kColStride]);
+        b[4 * q] = v.x;
+        b[4 * q + 1] = v.y;
+        b[4 * q + 2] = v.z;
+        b[4 * q + 3] = v.w;
+      }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
 #if DGR_SIMT_FFMA2
         // Two lanes of one row per instruction: (acc[i][j], acc[i][j+1]) +=
         // a[i] * (b[j], b[j+1]); one IEEE round-to-nearest per lane, as fmaf.
 #pragma unroll
-        for (int j = 0; j < 8; j += 2) ffma2(acc[i][j], acc[i][j + 1], a[i], b[j], b[j + 1]);
+        for (int j = 0; j < TN; j += 2) ffma2(acc[i][j], acc[i][j + 1], a[i], b[j], b[j + 1]);
 #else
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
 #endif
       }
     }
@@ -249,9 +273,11 @@ __device__ __forceinline__ void tile_mainloop(const SimtArgs &p, const float *A,
 // C[tile] = alpha * acc + beta * C (the C term only when use_c; beta = 1 when
 // a later k-part adds to what an earlier one stored). C is read through L2
 // (another CTA may have just written it).
+template <int TN>
 __device__ __forceinline__ void tile_epilogue(const SimtArgs &p, float *C, int m0, int n0, int rm,
-                                              int cn, const float (&acc)[8][8], float beta,
+                                              int cn, const float (&acc)[8][TN], float beta,
                                               bool use_c) {
+  using Sh = SimtShape<TN>;
   const float alpha = p.alpha;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -259,8 +285,8 @@ __device__ __forceinline__ void tile_epilogue(const SimtArgs &p, float *C, int m
     if (row >= p.M) continue;
     float *crow = C + static_cast<int64_t>(row) * p.ldc;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int col = n0 + cn + h * 64;
+    for (int h = 0; h < Sh::kColBlocks; ++h) {
+      const int col = n0 + cn + h * Sh::kColStride;
       const float *v = &acc[i][h * 4];
       if (p.c_vec_ok && col + 3 < p.N) {
         float4 out;
@@ -295,20 +321,22 @@ constexpr int kModeSplit = 2;    // one problem, persistent CTAs over a k-split 
 // split along k, parts added in order). For grids of fewer than two waves;
 // with more, one CTA per tile measures faster (CTAs that start together stay
 // in step, and their loads stop overlapping each other's arithmetic).
-template <int BK, int STAGES, bool A_T, bool VEC_A, bool B_T, bool VEC_B, int MODE>
-__global__ void __launch_bounds__(kThreads, 2) sgemm_simt_kernel(const SimtArgs p) {
+template <int TN, int BK, int STAGES, bool A_T, bool VEC_A, bool B_T, bool VEC_B, int MODE>
+__global__ void __launch_bounds__(SimtShape<TN>::kThreads, 2)
+    sgemm_simt_kernel(const SimtArgs p) {
+  using Sh = SimtShape<TN>;
   constexpr int kBStride = B_T ? kAStride : kBN;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   auto &sm = *reinterpret_cast<SimtSmem<BK, STAGES, kBStride> *>(smem_raw);
 
   const int tid = threadIdx.x;
-  // Thread -> 8x8 outputs. Warps form a 4 (rows) x 2 (cols) grid, lanes a
-  // 4 x 8 grid; rows rm..rm+3 and 64+rm..64+rm+3, cols cn..cn+3 and 64+cn..
+  // Thread -> 8 x TN outputs: rows rm..rm+3 and 64+rm..64+rm+3, columns
+  // cn..cn+3 plus multiples of the column-block stride (SimtShape).
   const int warp = tid >> 5, lane = tid & 31;
-  const int rm = (warp >> 1) * 16 + (lane >> 3) * 4;
-  const int cn = (warp & 1) * 32 + (lane & 7) * 4;
+  const int rm = (warp / Sh::kWarpsN) * 16 + (lane >> 3) * 4;
+  const int cn = (warp % Sh::kWarpsN) * 32 + (lane & 7) * 4;
   const int KT = (p.K + BK - 1) / BK;
-  float acc[8][8];
+  float acc[8][TN];
 
   if constexpr (MODE != kModeSplit) {
     // The operand addresses of a single problem stay in the parameter bank.
@@ -320,10 +348,11 @@ __global__ void __launch_bounds__(kThreads, 2) sgemm_simt_kernel(const SimtArgs 
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-    tile_mainloop<BK, STAGES, A_T, VEC_A, B_T, VEC_B, kBStride>(p, A, B, sm, tm * kBM, tn * kBN,
-                                                                0, KT, tid, rm, cn, acc);
-    tile_epilogue(p, C, tm * kBM, tn * kBN, rm, cn, acc, p.beta, p.beta != 0.f);
+      for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+    tile_mainloop<TN, BK, STAGES, A_T, VEC_A, B_T, VEC_B, kBStride>(p, A, B, sm, tm * kBM,
+                                                                    tn * kBN, 0, KT, tid, rm, cn,
+                                                                    acc);
+    tile_epilogue<TN>(p, C, tm * kBM, tn * kBN, rm, cn, acc, p.beta, p.beta != 0.f);
   } else {
     __shared__ int abort;
     if (tid == 0) abort = 0;
@@ -337,12 +366,11 @@ __global__ void __launch_bounds__(kThreads, 2) sgemm_simt_kernel(const SimtArgs 
 #pragma unroll
       for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-      tile_mainloop<BK, STAGES, A_T, VEC_A, B_T, VEC_B, kBStride>(p, p.A, p.B, sm, tm * kBM,
-                                                                  tn * kBN, w.kb0, w.kb1, tid, rm,
-                                                                  cn, acc);
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+      tile_mainloop<TN, BK, STAGES, A_T, VEC_A, B_T, VEC_B, kBStride>(
+          p, p.A, p.B, sm, tm * kBM, tn * kBN, w.kb0, w.kb1, tid, rm, cn, acc);
       if (w.parts == 1) {
-        tile_epilogue(p, p.C, tm * kBM, tn * kBN, rm, cn, acc, p.beta, p.beta != 0.f);
+        tile_epilogue<TN>(p, p.C, tm * kBM, tn * kBN, rm, cn, acc, p.beta, p.beta != 0.f);
         continue;
       }
       // k-split tile: part j adds after part j - 1 has stored (in order).
@@ -350,9 +378,9 @@ __global__ void __launch_bounds__(kThreads, 2) sgemm_simt_kernel(const SimtArgs 
       if (w.part > 0) {
         if (tid == 0) wait_flag(flag, static_cast<uint32_t>(w.part), &abort, p.err_word);
         __syncthreads();
-        tile_epilogue(p, p.C, tm * kBM, tn * kBN, rm, cn, acc, 1.f, true);
+        tile_epilogue<TN>(p, p.C, tm * kBM, tn * kBN, rm, cn, acc, 1.f, true);
       } else {
-        tile_epilogue(p, p.C, tm * kBM, tn * kBN, rm, cn, acc, p.beta, p.beta != 0.f);
+        tile_epilogue<TN>(p, p.C, tm * kBM, tn * kBN, rm, cn, acc, p.beta, p.beta != 0.f);
       }
       __threadfence();
       __syncthreads();  // every thread's part of the tile is stored and visible
@@ -361,17 +389,17 @@ __global__ void __launch_bounds__(kThreads, 2) sgemm_simt_kernel(const SimtArgs 
   }
 }
 
-// CTAs of `kern` that can be resident at once on the device (cached).
-int resident_ctas(const DeviceInfo &dev, const void *kern, size_t smem) {
+// CTAs of `kern` (blocks of `threads`) that can be resident at once on the
+// device (cached).
+int resident_ctas(const DeviceInfo &dev, const void *kern, int threads, size_t smem) {
   static std::mutex mu;
-  static std::map<std::pair<const void *, int>, int> cache;
+  static std::map<std::tuple<const void *, int>, int> cache;
   std::lock_guard<std::mutex> lock(mu);
-  const auto key = std::make_pair(kern, dev.device);
+  const auto key = std::make_tuple(kern, dev.device);
   auto it = cache.find(key);
   if (it != cache.end()) return it->second;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) !=
-      cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess)
     per_sm = 0;
   cudaGetLastError();
   const int n = per_sm * dev.sm_count;
@@ -381,11 +409,28 @@ int resident_ctas(const DeviceInfo &dev, const void *kern, size_t smem) {
 
 constexpr int kSimtMaxSplit = 4;  // parts per leftover tile (each adds one pass over its C)
 
-template <int BK, int STAGES, bool A_T, bool VEC_A, bool B_T, bool VEC_B, int MODE = kModeBatch>
+// The two kernel shapes: full grids (TN = 16, 8-deep k tiles, 6 stages) and
+// under-filled single problems on the k-split grid (TN = 8, 32-deep, 2 stages).
+#ifndef DGR_SIMT_WIDE_BK
+#define DGR_SIMT_WIDE_BK 8
+#endif
+#ifndef DGR_SIMT_WIDE_STAGES
+#define DGR_SIMT_WIDE_STAGES 6
+#endif
+struct SimtWide {
+  static constexpr int kTN = 16, kBK = DGR_SIMT_WIDE_BK, kStages = DGR_SIMT_WIDE_STAGES;
+};
+struct SimtNarrow {
+  static constexpr int kTN = 8, kBK = 32, kStages = 2;
+};
+
+template <class CFG, bool A_T, bool VEC_A, bool B_T, bool VEC_B, int MODE = kModeBatch>
 cudaError_t launch_variant(const SimtArgs &a_in, int batch, const DeviceInfo &dev,
                            cudaStream_t stream) {
-  constexpr size_t smem = sizeof(SimtSmem<BK, STAGES, B_T ? kAStride : kBN>);
-  auto kern = sgemm_simt_kernel<BK, STAGES, A_T, VEC_A, B_T, VEC_B, MODE>;
+  constexpr int kTN = CFG::kTN, kBK = CFG::kBK, kStages = CFG::kStages;
+  constexpr int kThreads = SimtShape<kTN>::kThreads;
+  constexpr size_t smem = sizeof(SimtSmem<kBK, kStages, B_T ? kAStride : kBN>);
+  auto kern = sgemm_simt_kernel<kTN, kBK, kStages, A_T, VEC_A, B_T, VEC_B, MODE>;
   cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void *>(kern),
                                        static_cast<int>(smem), dev.device);
   if (e != cudaSuccess) return e;
@@ -395,9 +440,9 @@ cudaError_t launch_variant(const SimtArgs &a_in, int batch, const DeviceInfo &de
   const int64_t blocks = static_cast<int64_t>(a.tiles_m) * a.tiles_n;
   if constexpr (MODE == kModeSplit) {
     // Persistent grid over the co-resident CTAs, the last wave split along k.
-    const int cap = resident_ctas(dev, reinterpret_cast<const void *>(kern), smem);
+    const int cap = resident_ctas(dev, reinterpret_cast<const void *>(kern), kThreads, smem);
     if (cap <= 0) return cudaErrorLaunchOutOfResources;
-    const int KT = (a.K + BK - 1) / BK;
+    const int KT = (a.K + kBK - 1) / kBK;
     int units = 0;
     plan_work(blocks, KT, 1, cap, kSimtMaxSplit, units, a.dp_tiles, a.tail_tiles, a.split);
     void *flags = nullptr;
@@ -436,23 +481,20 @@ cudaError_t launch_variant(const SimtArgs &a_in, int batch, const DeviceInfo &de
   return cudaSuccess;
 }
 
-#ifndef DGR_SIMT_BK
-#define DGR_SIMT_BK 32
-#endif
-#ifndef DGR_SIMT_STAGES
-#define DGR_SIMT_STAGES 2
-#endif
-constexpr int kSimtBK = DGR_SIMT_BK, kSimtStages = DGR_SIMT_STAGES;
-
-template <bool A_T, bool VEC_A>
+template <class CFG, bool A_T, bool VEC_A>
 cudaError_t launch_b(const SimtArgs &a, bool b_t, bool vec_b, int batch, const DeviceInfo &dev,
                      cudaStream_t stream) {
-  if (b_t)
-    return launch_variant<kSimtBK, kSimtStages, A_T, VEC_A, true, false>(a, batch, dev, stream);
-  return vec_b ? launch_variant<kSimtBK, kSimtStages, A_T, VEC_A, false, true>(a, batch, dev,
-                                                                               stream)
-               : launch_variant<kSimtBK, kSimtStages, A_T, VEC_A, false, false>(a, batch, dev,
-                                                                                stream);
+  if (b_t) return launch_variant<CFG, A_T, VEC_A, true, false>(a, batch, dev, stream);
+  return vec_b ? launch_variant<CFG, A_T, VEC_A, false, true>(a, batch, dev, stream)
+               : launch_variant<CFG, A_T, VEC_A, false, false>(a, batch, dev, stream);
+}
+
+template <class CFG>
+cudaError_t launch_ops(const SimtArgs &a, bool a_t, bool vec_a, bool b_t, bool vec_b, int batch,
+                       const DeviceInfo &dev, cudaStream_t stream) {
+  if (!a_t) return launch_b<CFG, false, false>(a, b_t, vec_b, batch, dev, stream);
+  return vec_a ? launch_b<CFG, true, true>(a, b_t, vec_b, batch, dev, stream)
+               : launch_b<CFG, true, false>(a, b_t, vec_b, batch, dev, stream);
 }
 
 // 16-byte chunks of a straight copy are safe when the stored matrix (and every
@@ -493,23 +535,25 @@ cudaError_t launch_sgemm_simt_ex(const DeviceInfo &dev, const BatchOps &ops, int
   if (static_cast<int64_t>(a.tiles_m) * a.tiles_n > 0x7fffffffLL) return cudaErrorInvalidValue;
   const bool vec_a = ops.a_t && vec_ok(A, lda, M, batch, a.stride_a);
   const bool vec_b = !ops.b_t && vec_ok(B, ldb, N, batch, a.stride_b);
+  // Fewer CTAs than two waves of resident CTAs (2 per SM): a single problem
+  // takes the persistent k-split form of the 256-thread shape, a batch or a
+  // transposed problem the 256-thread shape one CTA per tile. Otherwise the
+  // 128-thread shape, one CTA per tile.
+  const int64_t ctas = static_cast<int64_t>(a.tiles_m) * a.tiles_n * batch;
+  const bool full = ctas >= 4LL * dev.sm_count;
   if (ops.plain()) {  // one problem, no transposes
-    // Fewer tiles than two waves of resident CTAs (2 per SM): the persistent
-    // k-split form keeps every SM busy; otherwise one CTA per tile.
-    const int64_t tiles = static_cast<int64_t>(a.tiles_m) * a.tiles_n;
-    if (tiles < 4LL * dev.sm_count)
-      return vec_b ? launch_variant<kSimtBK, kSimtStages, false, false, false, true, kModeSplit>(
-                         a, 1, dev, stream)
-                   : launch_variant<kSimtBK, kSimtStages, false, false, false, false, kModeSplit>(
+    if (!full)
+      return vec_b ? launch_variant<SimtNarrow, false, false, false, true, kModeSplit>(a, 1, dev,
+                                                                                      stream)
+                   : launch_variant<SimtNarrow, false, false, false, false, kModeSplit>(
                          a, 1, dev, stream);
-    return vec_b ? launch_variant<kSimtBK, kSimtStages, false, false, false, true, kModeTile>(
-                       a, 1, dev, stream)
-                 : launch_variant<kSimtBK, kSimtStages, false, false, false, false, kModeTile>(
-                       a, 1, dev, stream);
+    return vec_b ? launch_variant<SimtWide, false, false, false, true, kModeTile>(a, 1, dev,
+                                                                                 stream)
+                 : launch_variant<SimtWide, false, false, false, false, kModeTile>(a, 1, dev,
+                                                                                  stream);
   }
-  if (!ops.a_t) return launch_b<false, false>(a, ops.b_t, vec_b, batch, dev, stream);
-  return vec_a ? launch_b<true, true>(a, ops.b_t, vec_b, batch, dev, stream)
-               : launch_b<true, false>(a, ops.b_t, vec_b, batch, dev, stream);
+  return full ? launch_ops<SimtWide>(a, ops.a_t, vec_a, ops.b_t, vec_b, batch, dev, stream)
+              : launch_ops<SimtNarrow>(a, ops.a_t, vec_a, ops.b_t, vec_b, batch, dev, stream);
 }
 
 cudaError_t launch_sgemm_simt(const DeviceInfo &dev, int M, int N, int K, float alpha,

@@ -138,6 +138,20 @@ def test_batched_transposed_multi_tile(gemm_mod, oracle_mod, dtype, ops):
     run_case(gemm_mod, oracle_mod, dtype, ops, 3, 300, 520, 200, seed=11)
 
 
+@pytest.mark.parametrize("aligned_ld", [False, True], ids=["ld_odd", "ld_mod4"])
+@pytest.mark.parametrize("ops", OPS)
+def test_f32_batch_full_grid(gemm_mod, oracle_mod, ops, aligned_ld):
+    """fp32 batches of at least two waves of resident CTAs (40 entries of 4 x 4
+    tiles) run the 128-thread SIMT shape, in every operand form: ragged sizes
+    with odd row strides (4-byte copies), and 512-wide operands with row and
+    matrix strides in whole 16-byte units (16-byte copies)."""
+    if aligned_ld:
+        run_case(gemm_mod, oracle_mod, torch.float32, ops, 40, 512, 512, 136, seed=23,
+                 gap=4, extra=4)
+    else:
+        run_case(gemm_mod, oracle_mod, torch.float32, ops, 40, 500, 510, 137, seed=29)
+
+
 @pytest.mark.parametrize("ops", OPS)
 @pytest.mark.parametrize("dtype", DTYPES, ids=str)
 def test_single_entry_transposed(gemm_mod, oracle_mod, dtype, ops):

@@ -272,6 +272,24 @@ def test_split_tail_shapes(gemm_mod, oracle_mod, dtype, shape):
         out.check_canaries()
 
 
+@pytest.mark.parametrize("shape,ldb", [((3203, 3202, 301), None), ((2560, 4100, 520), None),
+                                       ((3200, 3200, 200), 3201)],
+                         ids=["n_mod4_2", "vec_b_ragged_k", "ldb_odd"])
+def test_f32_full_grid_shapes(gemm_mod, oracle_mod, shape, ldb):
+    """fp32 grids of at least two waves of resident CTAs run the 128-thread
+    SIMT shape (8 x 16 outputs per thread, 8-deep k tiles): 16-byte and 4-byte
+    copies of B, ragged M, N and K, both C layouts; sampled rows."""
+    M, N, K = shape
+    for aligned in (True, False):
+        p = w.problem(M, N, K, torch.float32, "normal", 171 + M, alpha=-0.5, beta=1.5,
+                      c_dist="normal", ldb=ldb)
+        ldc = (N + 3) // 4 * 4 if aligned else N + 1
+        got, out = run_gpu(gemm_mod, p, ldc=ldc, aligned=aligned)
+        rows = sample_rows(M, 24, seed=M + 1)
+        assert_parity(got[rows], oracle_of(oracle_mod, p, rows), exact=False)
+        out.check_canaries()
+
+
 # ---------------------------------------------------------- short, wide shapes
 
 @pytest.mark.parametrize("dtype", ALL_DTYPES, ids=str)
