@@ -133,6 +133,30 @@ __device__ __forceinline__ int32_t axpby(int32_t a, int32_t x, int32_t b, int32_
   return static_cast<int32_t>(r);
 }
 
+__device__ __forceinline__ float add_parts(float a, float b) { return a + b; }
+__device__ __forceinline__ int32_t add_parts(int32_t a, int32_t b) {
+  return static_cast<int32_t>(static_cast<uint32_t>(a) + static_cast<uint32_t>(b));
+}
+
+// C[m][n] = alpha * w[j] + beta * C[m][n] for the rows m = g + j < M of column
+// n (a group of 16 rows). Every read of C is issued before the first store: as
+// far as the compiler knows a store may alias a later row's read, and
+// interleaving them would cost one load latency per row.
+template <bool kInt>
+__device__ __forceinline__ void write_rows16(const SkArgs<kInt> &p, int n, int g,
+                                             typename SkArgs<kInt>::Out (&w)[16]) {
+  using Out = typename SkArgs<kInt>::Out;
+  const bool use_c = p.beta != Out(0);
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if (g + j < p.M)
+      w[j] = axpby(p.alpha, w[j], p.beta,
+                   use_c ? p.C[static_cast<int64_t>(g + j) * p.ldc + n] : Out(0), use_c);
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if (g + j < p.M) p.C[static_cast<int64_t>(g + j) * p.ldc + n] = w[j];
+}
+
 template <bool kInt>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_skinny_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -305,15 +329,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         return facc[m];
       }
     };
-    const bool use_c = p.beta != Out(0);
     if (p.split == 1) {
       if (n < p.N && !*abort && kb1 > kb0) {
 #pragma unroll
-        for (int m = 0; m < kMaxM; ++m)
-          if (m < p.M) {
-            Out *cp = p.C + static_cast<int64_t>(m) * p.ldc + n;
-            *cp = axpby(p.alpha, value(m), p.beta, use_c ? *cp : Out(0), use_c);
+        for (int g = 0; g < kMaxM; g += 16) {
+          if (g < p.M) {
+            Out w[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) w[j] = value(g + j);
+            write_rows16<kInt>(p, n, g, w);
           }
+        }
       }
     } else {
       // Store this part's partial sums, count the part done; the last part of
@@ -330,19 +356,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (last) {
         __threadfence();
         if (n < p.N) {
+          // Parts in order (each element's sum in one fixed order); within a
+          // part 16 rows at once, so their loads overlap.
+#pragma unroll
+          for (int g = 0; g < kMaxM; g += 16) {
+            if (g < p.M) {
+              Out sum[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) sum[j] = Out(0);
 #pragma unroll 1
-          for (int m = 0; m < p.M; ++m) {
-            Out sum = Out(0);
-            for (int q = 0; q < p.split; ++q) {
-              const Out v = __ldcg(p.ws + (static_cast<int64_t>(q) * p.M + m) * p.ws_ld + n);
-              if constexpr (kInt) {
-                sum = static_cast<int32_t>(static_cast<uint32_t>(sum) + static_cast<uint32_t>(v));
-              } else {
-                sum += v;
+              for (int q = 0; q < p.split; ++q) {
+                const Out *src = p.ws + (static_cast<int64_t>(q) * p.M + g) * p.ws_ld + n;
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  if (g + j < p.M)
+                    sum[j] = add_parts(sum[j], __ldcg(src + static_cast<int64_t>(j) * p.ws_ld));
               }
+              write_rows16<kInt>(p, n, g, sum);
             }
-            Out *cp = p.C + static_cast<int64_t>(m) * p.ldc + n;
-            *cp = axpby(p.alpha, sum, p.beta, use_c ? *cp : Out(0), use_c);
           }
         }
       }
@@ -602,7 +633,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         return facc[m];
       }
     };
-    const bool use_c = p.beta != Out(0);
     if (!done) *abort = 1;  // a wait gave up: the error word says so
     epilogue_sync();
     if (warp == 2 && lane == 0) seg_skip = *abort;
@@ -611,11 +641,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!g.shared) {
       if (n < p.N) {
 #pragma unroll
-        for (int m = 0; m < kMaxM; ++m)
-          if (m < p.M) {
-            Out *cp = p.C + static_cast<int64_t>(m) * p.ldc + n;
-            *cp = axpby(p.alpha, value(m), p.beta, use_c ? *cp : Out(0), use_c);
+        for (int g = 0; g < kMaxM; g += 16) {
+          if (g < p.M) {
+            Out w[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) w[j] = value(g + j);
+            write_rows16<kInt>(p, n, g, w);
           }
+        }
       }
     } else {
       // Store this segment's partial sums in this CTA's slot, count the
@@ -645,23 +678,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int slot = q == 0 ? first_slot : 0;
             const Out *src = p.ws + (static_cast<int64_t>(cq) * 2 + slot) * p.M * kBN + lc;
 #pragma unroll
-            for (int m = 0; m < kMaxM; ++m) {
-              if (m < p.M) {
-                const Out v = __ldcg(src + static_cast<int64_t>(m) * kBN);
-                if constexpr (kInt) {
-                  sum[m] = static_cast<int32_t>(static_cast<uint32_t>(sum[m]) +
-                                                static_cast<uint32_t>(v));
-                } else {
-                  sum[m] += v;
-                }
-              }
-            }
+            for (int m = 0; m < kMaxM; ++m)
+              if (m < p.M) sum[m] = add_parts(sum[m], __ldcg(src + static_cast<int64_t>(m) * kBN));
           }
 #pragma unroll
-          for (int m = 0; m < kMaxM; ++m) {
-            if (m < p.M) {
-              Out *cp = p.C + static_cast<int64_t>(m) * p.ldc + n;
-              *cp = axpby(p.alpha, sum[m], p.beta, use_c ? *cp : Out(0), use_c);
+          for (int g = 0; g < kMaxM; g += 16) {
+            if (g < p.M) {
+              Out w[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) w[j] = sum[g + j];
+              write_rows16<kInt>(p, n, g, w);
             }
           }
         }
