@@ -62,6 +62,12 @@ WORKLOADS = {
                  "f32", "alu", 1),
     "s8_8192": ("int8 GEMM, row-major, M=N=K=8192, uniform -128..127, exact int32 accumulate "
                 "and int32 C, alpha=1, beta=0", "s8", "tensor", 3),
+    "f32_8192": ("fp32 SGEMM (SIMT, exact fp32), row-major, M=N=K=8192, N(0,1), alpha=1, beta=0",
+                 "f32", "alu", 1),
+    "bf16_4096": ("bf16 GEMM, row-major, M=N=K=4096, N(0,1) rounded to bf16, fp32 accumulate "
+                  "and fp32 C, alpha=1, beta=0", "bf16", "tensor", 1),
+    "s8_4096": ("int8 GEMM, row-major, M=N=K=4096, uniform -128..127, exact int32 accumulate "
+                "and int32 C, alpha=1, beta=0", "s8", "tensor", 3),
 }
 
 # Sources whose change invalidates recorded ncu traffic for a workload.
@@ -70,6 +76,9 @@ KERNEL_SOURCES = {
     "f16_8192": ["gemm_tc_kernel.cuh", "gemm_tc_f16.cu", "work_split.cuh", "ptx.cuh"],
     "s8_8192": ["gemm_tc_kernel.cuh", "gemm_tc_int.cu", "work_split.cuh", "ptx.cuh"],
     "f32_4096": ["sgemm_simt.cu", "work_split.cuh", "ptx.cuh"],
+    "f32_8192": ["sgemm_simt.cu", "work_split.cuh", "ptx.cuh"],
+    "bf16_4096": ["gemm_tc_kernel.cuh", "gemm_tc_f16.cu", "work_split.cuh", "ptx.cuh"],
+    "s8_4096": ["gemm_tc_kernel.cuh", "gemm_tc_int.cu", "work_split.cuh", "ptx.cuh"],
 }
 
 
@@ -223,6 +232,39 @@ def time_device(binding, torch, kind, p_dev, steps, warmup, stream, dist=None):
     return ms, t0, t1
 
 
+L2_BYTES = 129e6
+
+
+def time_device_flushed(binding, torch, kind, p_dev, steps, warmup, stream):
+    """For inputs that fit in L2: each timed call is preceded, outside its
+    event pair and on the same stream, by a 256 MB write that evicts L2.
+    Returns the summed device time of the calls and the wall window."""
+    A, B, C, alpha, beta = p_dev
+    M, K = A.shape
+    N = B.shape[1]
+    fn = entry(binding, kind)
+    args = (M, N, K, alpha, A, A.stride(0), B, B.stride(0), beta, C, C.stride(0), stream)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            fn(*args)
+    torch.cuda.synchronize()
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(steps)]
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        for e0, e1 in pairs:
+            flush.zero_()
+            e0.record(stream)
+            fn(*args)
+            e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in pairs)
+    del flush
+    return ms, t0, t1
+
+
 def time_e2e(binding, torch, kind, p_host, p_dev, steps, stream):
     """Host -> device copy of A and B, the C-ABI call, device -> host copy of C."""
     (Ah, Bh, Ch), (A, B, C, alpha, beta) = p_host, p_dev
@@ -339,6 +381,77 @@ def cpu_oracle_sample(p, seconds: float):
                       f"{flops_of(rows, N, K) / 1e9:.1f} GFLOP per sample"}
 
 
+def cpu_oracle_configs(w):
+    """The oracle on the small configs in full (fp32 128^3 integers, the
+    1023x777x513 ragged case, 4096^3) on all host threads, and 1024^3 on one
+    thread (a child process with OMP_NUM_THREADS=1: OpenMP fixes its thread
+    count at start-up)."""
+    from oracle import oracle as o
+    out = {}
+    for name in ("f32_int128", "f32_ragged", "f32_4096"):
+        q = w.config(name)
+        M, K = q.A.shape
+        N = q.B.shape[1]
+        t = time.perf_counter()
+        o.gemm(q.A, q.B, q.alpha, q.beta, q.C0 if q.beta != 0 else None)
+        dt = time.perf_counter() - t
+        out[name] = {"seconds": dt, "gflops": flops_of(M, N, K) / dt / 1e9,
+                     "cores": o.num_threads()}
+    code = ("import json, time, torch\n"
+            "from oracle import oracle as o\n"
+            "g = torch.Generator().manual_seed(9)\n"
+            "A = torch.randn(1024, 1024, generator=g); B = torch.randn(1024, 1024, generator=g)\n"
+            "t = time.perf_counter(); o.gemm(A, B, 1.0, 0.0); dt = time.perf_counter() - t\n"
+            "print(json.dumps({'seconds': dt, 'cores': o.num_threads()}))\n")
+    try:
+        r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
+                           timeout=600, env=dict(os.environ, OMP_NUM_THREADS="1"))
+        one = json.loads(r.stdout.strip().splitlines()[-1])
+        one["gflops"] = flops_of(1024, 1024, 1024) / one["seconds"] / 1e9
+        out["f32_1024_one_core"] = one
+    except (subprocess.SubprocessError, ValueError, IndexError) as e:
+        out["f32_1024_one_core"] = {"error": str(e)[:200]}
+    return out
+
+
+def measure_peaks(binding, torch, peaks, sm_count, stream, gpu_id):
+    """The build's own peak microbenchmarks: packed fp32 FMA and tcgen05
+    kind::f16 issue loops (best of 5 launches of about 10 ms each)."""
+    sink = torch.zeros(1, device="cuda")
+    runs = (("ffma", lambda it: binding.peak_ffma(it, sink, stream), 65536),
+            ("tc_f16", lambda it: binding.peak_tc_f16(it, stream), 40000))
+    out = {}
+    for name, fn, iters in runs:
+        fn(256)
+        torch.cuda.synchronize()
+        sampler = ClockSampler(gpu_id)
+        sampler.start()
+        times, flops = [], 0.0
+        t0 = time.time()
+        for _ in range(5):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            flops = fn(iters)
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+        t1 = time.time()
+        sampler.stop()
+        clocks = sampler.summary(t0, t1)
+        ms = min(times)
+        out[name] = {"tflops": flops / (ms / 1e3) / 1e12, "ms": ms, "iters": iters,
+                     "sm_mhz": clocks["sm_mhz"], "reasons": clocks["reasons"]}
+    max_mhz = peaks.get("sm_max_mhz", 2070.0)
+    nominal = sm_count * 128 * 2 * max_mhz * 1e6 / 1e12
+    out["ffma"]["nominal_at_max_clock"] = nominal
+    out["ffma"]["frac_of_nominal"] = out["ffma"]["tflops"] / nominal
+    out["tc_f16"]["cublas_burst"] = peaks.get("bf16_tflops")
+    out["tc_f16"]["dense_at_max_clock"] = sm_count * 8192 * max_mhz * 1e6 / 1e12
+    binding.check_device_error()
+    return out
+
+
 # ------------------------------------------------------------------ reference
 
 def run_reference(args, world, rank):
@@ -406,9 +519,13 @@ def measure_extra(binding, torch, w, name, peaks, sm_count, stream, gpu_id):
     M, K = q.A.shape
     N = q.B.shape[1]
     steps = 100 if kind != "f32" else 60
+    in_l2 = sum(t.numel() * t.element_size() for t in q_dev[:3]) < 1.5 * L2_BYTES
     sampler = ClockSampler(gpu_id)
     sampler.start()
-    ms, t0, t1 = time_device(binding, torch, kind, q_dev, steps, 5, stream)
+    if in_l2:
+        ms, t0, t1 = time_device_flushed(binding, torch, kind, q_dev, steps, 5, stream)
+    else:
+        ms, t0, t1 = time_device(binding, torch, kind, q_dev, steps, 5, stream)
     sampler.stop()
     clocks = sampler.summary(t0, t1)
     f = flops_of(M, N, K)
@@ -417,6 +534,8 @@ def measure_extra(binding, torch, w, name, peaks, sm_count, stream, gpu_id):
     out = {"workload": desc, "value": ach, "unit": "TOPS" if kind == "s8" else "TFLOP/s",
            "ms_per_step": ms / steps, "bound": bound, "peak": pk, "frac": ach / pk,
            "traffic": recorded_traffic(name),
+           "l2": ("flushed by a 256 MB write before each timed call" if in_l2
+                  else "no flush: A+B+C exceed 1.5 x the 129 MB L2"),
            "clocks": {"sm_mhz": clocks["sm_mhz"], "reasons": clocks["reasons"],
                       "samples": clocks["samples"]}}
     if kind == "f32" and clocks["sm_mhz"]:
@@ -661,7 +780,8 @@ def main():
 
     extras = {}
     if not args.no_extras:
-        for other in ("f32_4096", "f16_8192", "s8_8192", "bf16_8192"):
+        for other in ("f32_4096", "f16_8192", "s8_8192", "bf16_8192", "f32_8192", "bf16_4096",
+                      "s8_4096"):
             if other == name:
                 continue
             extras[other] = measure_extra(binding, torch, w, other, peaks, sm_count, stream,
@@ -676,12 +796,20 @@ def main():
         types = measure_types(binding, torch, peaks, stream)
         binding.check_device_error()
 
+    micro = {}
+    if not args.no_extras:
+        micro = measure_peaks(binding, torch, peaks, sm_count, stream, gpu_id)
+        roofline["microbench_peak"] = micro["ffma" if kind == "f32" else "tc_f16"]["tflops"]
+        roofline["frac_of_microbench_peak"] = achieved / roofline["microbench_peak"]
+
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cal = cpu_oracle_sample(p, args.cpu_seconds)
         cpu = {"value": cal["flops"] / cal["seconds"] / 1e12, "unit": unit,
                "cores": cal["cores"], "kind": "oracle", "sample": cal["sample"],
                "seconds": cal["seconds"]}
+        if not args.no_extras:
+            cpu["configs"] = cpu_oracle_configs(w)
 
     line = {
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
@@ -699,6 +827,7 @@ def main():
                    "reasons": clocks["reasons"], "samples": clocks["samples"],
                    "window": clocks["window"]},
         "extras": extras,
+        "peaks_microbench": micro,
         "skinny": skinny,
         "types": types,
     }

@@ -45,7 +45,7 @@ EXPORTED = ("gemm_f32", "gemm_bf16", "gemm_f16", "gemm_s8", "gemm_u8", "gemm_f16
             "gemm_bf16_bf16", "gemm_tf32", "gemm_f64", "gemm_f32_ex", "gemm_bf16_ex",
             "gemm_f16_ex", "gemm_s8_ex", "gemm_s8_noalloc", "gemm_status_string",
             "gemm_check_device_error", "gemm_selftest_wait_timeout", "gemm_last_launch_error",
-            "gemm_version")
+            "gemm_peak_ffma", "gemm_peak_tc_f16", "gemm_version")
 
 OP_N, OP_T = 0, 1  # gemm_op_t
 
@@ -92,6 +92,10 @@ def _load():
     lib.gemm_selftest_wait_timeout.restype = ctypes.c_int
     lib.gemm_last_launch_error.argtypes = []
     lib.gemm_last_launch_error.restype = ctypes.c_char_p
+    lib.gemm_peak_ffma.argtypes = [i32, vp, ctypes.POINTER(f64), vp]
+    lib.gemm_peak_ffma.restype = ctypes.c_int
+    lib.gemm_peak_tc_f16.argtypes = [i32, ctypes.POINTER(f64), vp]
+    lib.gemm_peak_tc_f16.restype = ctypes.c_int
     lib.gemm_version.argtypes = []
     lib.gemm_version.restype = ctypes.c_int
     return lib
@@ -192,6 +196,21 @@ gemm_f32_ex = _ex("gemm_f32_ex", float)
 gemm_bf16_ex = _ex("gemm_bf16_ex", float)
 gemm_f16_ex = _ex("gemm_f16_ex", float)
 gemm_s8_ex = _ex("gemm_s8_ex", int)
+
+
+def peak_ffma(iters, sink, stream=None) -> float:
+    """Enqueue the packed-FP32-FMA peak microbenchmark; returns its flop count."""
+    f = ctypes.c_double(0.0)
+    _check(lib.gemm_peak_ffma(int(iters), _addr(sink), ctypes.byref(f), _stream(stream)),
+           "gemm_peak_ffma")
+    return f.value
+
+
+def peak_tc_f16(iters, stream=None) -> float:
+    """Enqueue the tcgen05 kind::f16 peak microbenchmark; returns its flop count."""
+    f = ctypes.c_double(0.0)
+    _check(lib.gemm_peak_tc_f16(int(iters), ctypes.byref(f), _stream(stream)), "gemm_peak_tc_f16")
+    return f.value
 
 
 def check_device_error() -> int:

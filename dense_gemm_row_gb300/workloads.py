@@ -170,6 +170,8 @@ def config(name: str) -> Problem:
     bf16_8192    bf16 8192^3, N(0,1) rounded to bf16, fp32 C, alpha=1, beta=0
     f16_8192     fp16 8192^3, N(0,1) rounded to fp16, fp32 C, alpha=1, beta=0
     s8_8192      int8 8192^3, uniform -128..127, int32 C, alpha=1, beta=0
+    f32_8192, bf16_4096, s8_4096: the same recipes at the other size the
+                 throughput metric names
     """
     if name == "f32_int128":
         return problem(128, 128, 128, torch.float32, "int0_99", 1, name=name)
@@ -184,6 +186,12 @@ def config(name: str) -> Problem:
         return problem(8192, 8192, 8192, torch.float16, "normal", 4, name=name)
     if name == "s8_8192":
         return problem(8192, 8192, 8192, torch.int8, "int8", 5, alpha=1, beta=0, name=name)
+    if name == "f32_8192":
+        return problem(8192, 8192, 8192, torch.float32, "normal", 6, name=name)
+    if name == "bf16_4096":
+        return problem(4096, 4096, 4096, torch.bfloat16, "normal", 7, name=name)
+    if name == "s8_4096":
+        return problem(4096, 4096, 4096, torch.int8, "int8", 8, alpha=1, beta=0, name=name)
     raise KeyError(name)
 
 

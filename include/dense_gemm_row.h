@@ -278,6 +278,36 @@ GEMM_API gemm_status_t gemm_check_device_error(uint32_t *word);
 GEMM_API gemm_status_t gemm_selftest_wait_timeout(uint32_t limit_us, cudaStream_t stream);
 
 /*
+ * Peak-rate microbenchmarks: the measured denominators that the GEMM kernels'
+ * roofline fractions are cross-checked against. Neither reads or writes
+ * user data beyond `sink`; both are asynchronous on `stream` (time them with
+ * events around the call). *flops (a host pointer, may be NULL) receives the
+ * floating-point operations the launch performs (a multiply-add counts 2).
+ *
+ * gemm_peak_ffma: every SM runs 4 blocks of 256 threads; each thread issues
+ * `iters` rounds of 16 independent packed fp32 FMAs (fma.rn.f32x2, 32 lanes'
+ * worth of multiply-adds), the instruction the exact-fp32 GEMM uses. `sink` is
+ * a device float that is written only if the accumulated values happen to
+ * equal a fixed sentinel (never, in practice; it keeps the work observable).
+ * flops = SMs * 1024 * iters * 64.
+ *
+ * gemm_peak_tc_f16: one CTA per SM issues `iters` rounds of four
+ * tcgen05.mma.cta_group::1.kind::f16 (bf16 in, fp32 accumulate; M = 128,
+ * N = 256, K = 16) on operands held in shared memory, accumulating in TMEM;
+ * one thread issues, as in the GEMM kernel. flops = SMs * iters * 4 *
+ * 2 * 128 * 256 * 16. Its one wait (for the last MMA) is bounded like the
+ * GEMM kernels' waits.
+ *
+ * Both return GEMM_ERR_INVALID_VALUE for iters outside 1 .. 2^24 (or a NULL
+ * sink for gemm_peak_ffma), else the launch status. Source: the rooflines are
+ * bounded by these two pipes ("Sgemm [128,128,8]": FFMA-bound inner loop; the
+ * C++ warp-matrix-function page: tensor-core matrix multiply-accumulate).
+ */
+GEMM_API gemm_status_t gemm_peak_ffma(int32_t iters, float *sink, double *flops,
+                                      cudaStream_t stream);
+GEMM_API gemm_status_t gemm_peak_tc_f16(int32_t iters, double *flops, cudaStream_t stream);
+
+/*
  * The CUDA runtime's name for the error behind the calling thread's most
  * recent GEMM_ERR_LAUNCH (e.g. "cudaErrorLaunchOutOfResources"), or
  * "cudaSuccess" if there was none. A static string; never NULL.

@@ -152,3 +152,14 @@ def test_tf32_needs_aligned_elements(gemm_mod):
     f = gemm_mod.lib.gemm_tf32
     assert f(8, 8, 8, 1.0, FAKE + 2, 8, FAKE, 8, 0.0, FAKE, 8, None) == LAYOUT
     assert f(8, 8, 8, 1.0, FAKE, 8, FAKE + 1, 8, 0.0, FAKE, 8, None) == LAYOUT
+
+
+def test_peak_microbenchmarks_check_arguments_on_host(gemm_mod):
+    """Iteration counts outside 1 .. 2^24 and a missing sink are rejected before
+    any device work."""
+    lib = gemm_mod.lib
+    assert lib.gemm_peak_ffma(0, FAKE, None, None) == INVALID
+    assert lib.gemm_peak_ffma((1 << 24) + 1, FAKE, None, None) == INVALID
+    assert lib.gemm_peak_ffma(16, None, None, None) == INVALID
+    assert lib.gemm_peak_tc_f16(0, None, None) == INVALID
+    assert lib.gemm_peak_tc_f16(-5, None, None) == INVALID
