@@ -150,6 +150,32 @@ cudaError_t run_int_pooled(const DeviceInfo &dev, const BatchOps &ops, int M, in
   return e != cudaSuccess ? e : f;
 }
 
+}  // namespace
+
+// Short, wide int8 GEMM with B read as stored: A (M x K, a few rows) is
+// widened to fp16 in pool scratch; B goes straight to the transposed-role
+// kernel, whose converter warps widen each tile in shared memory.
+cudaError_t launch_gemm_s8_skinny_raw(const DeviceInfo &dev, int M, int N, int K, int32_t alpha,
+                                      const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
+                                      int32_t beta, int32_t *C, int64_t ldc,
+                                      cudaStream_t stream) {
+  const int64_t lda16 = (static_cast<int64_t>(K) + 7) / 8 * 8;
+  cudaMemPool_t pool = nullptr;
+  cudaError_t e = device_pool(dev, &pool);
+  if (e != cudaSuccess) return e;
+  void *scratch = nullptr;
+  e = cudaMallocFromPoolAsync(&scratch, static_cast<size_t>(M) * lda16 * 2, pool, stream);
+  if (e != cudaSuccess) return e;
+  __half *a16 = static_cast<__half *>(scratch);
+  e = widen8<int8_t>(dev, A, lda, a16, lda16, M, K, stream);
+  if (e == cudaSuccess)
+    e = launch_tc_skinny_i8(dev, M, N, K, alpha, a16, lda16, B, ldb, beta, C, ldc, stream);
+  cudaError_t f = cudaFreeAsync(scratch, stream);
+  return e != cudaSuccess ? e : f;
+}
+
+namespace {
+
 // row_corr[i] = 128 * sum_k A[i, k] (mod 2^32): one warp per row, lanes along
 // k, 16 bytes per lane per step when rows are 16-byte aligned (byte sums by
 // dp4a against 0x01010101), a shuffle reduction at the end.

@@ -68,6 +68,7 @@ constexpr uint32_t kABytes = kMaxM * kBK * 2;     // 8 KiB (room for 64 rows)
 constexpr int kMaxSplit = 16;
 
 struct __align__(1024) SkSmem {
+  static constexpr int kNumStages = kStages;
   uint8_t b[kStages][kBBytes];  // B tile, N-major: the MMA's A operand
   uint8_t a[kStages][kABytes];  // A tile, K-major: the MMA's B operand
   uint64_t full[kStages];
@@ -78,6 +79,68 @@ struct __align__(1024) SkSmem {
   uint32_t tmem_base;
   int abort;
 };
+
+// int8 B read as stored (the raw-B form of the per-block kernel): TMA brings a
+// 64(k) x 128(n) byte tile of B into `raw` (with the A tile into `a`); four
+// converter warps write it to `b` as fp16 in the layout TMA gives a 16-bit B
+// (two 64-column boxes, 128-byte swizzle) and arrive on `conv`; the MMA waits
+// on `conv`. B then crosses HBM once, as bytes, instead of being widened to a
+// 16-bit copy first.
+constexpr int kI8Stages = 6;
+constexpr int kConvWarps = 4;
+constexpr int kI8Threads = kThreads + 32 * kConvWarps;
+constexpr uint32_t kRawBytes = kBK * kBN;  // 8 KiB: 64 rows of 128 bytes
+struct __align__(1024) SkSmemI8 {
+  static constexpr int kNumStages = kI8Stages;
+  uint8_t b[kI8Stages][kBBytes];
+  uint8_t a[kI8Stages][kABytes];
+  uint8_t raw[kI8Stages][kRawBytes];
+  uint64_t full[kI8Stages];   // TMA: raw B and A landed
+  uint64_t conv[kI8Stages];   // converter warps: b written
+  uint64_t empty[kI8Stages];  // MMA: stage consumed
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// One converter thread's share of a stage (ct in [0, 128)): four 16-byte
+// pieces of the raw tile (row k = piece / 8, bytes 16 (piece % 8) ...), each
+// widened exactly to 16 fp16 values and stored as two 16-byte chunks of the
+// swizzled 16-bit tile: column n = 16 (piece % 8) + t sits in box n / 64, row
+// k, chunk (n % 64) / 8, placed at chunk position chunk ^ (k % 8).
+// Exact widening of a signed byte x: (x + 128) as the low byte under the fp16
+// pattern 0x64 is 1024 + x + 128; subtracting 1152 leaves x (every value
+// involved is an integer below 2^11, so fp16 holds it exactly).
+__device__ __forceinline__ void convert_stage(uint32_t raw, uint32_t b, int ct) {
+  const __half2 bias = __half2half2(__ushort_as_half(0x6480));  // 1152
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int piece = i * 128 + ct;
+    const int k = piece >> 3, c = piece & 7;
+    uint32_t w[4];
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                 : "r"(raw + static_cast<uint32_t>(k * 128 + c * 16)));
+    uint32_t h[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t t = w[q] ^ 0x80808080u;
+      const uint32_t lo = __byte_perm(t, 0x64646464u, 0x4140);
+      const uint32_t hi = __byte_perm(t, 0x64646464u, 0x4342);
+      const __half2 l = __hsub2(*reinterpret_cast<const __half2 *>(&lo), bias);
+      const __half2 u = __hsub2(*reinterpret_cast<const __half2 *>(&hi), bias);
+      h[2 * q] = *reinterpret_cast<const uint32_t *>(&l);
+      h[2 * q + 1] = *reinterpret_cast<const uint32_t *>(&u);
+    }
+    const int box = c >> 2;            // 64 columns per box
+    const int j0 = (c & 3) * 2;        // first 16-byte chunk of this piece in its row
+    const uint32_t row = b + static_cast<uint32_t>(box) * kBBox + static_cast<uint32_t>(k) * 128;
+    st_shared_v4(row + static_cast<uint32_t>(((j0) ^ (k & 7)) << 4), h[0], h[1], h[2], h[3]);
+    st_shared_v4(row + static_cast<uint32_t>(((j0 + 1) ^ (k & 7)) << 4), h[4], h[5], h[6], h[7]);
+  }
+}
 
 template <bool kInt>
 struct SkArgs {
@@ -157,22 +220,28 @@ __device__ __forceinline__ void write_rows16(const SkArgs<kInt> &p, int n, int g
     if (g + j < p.M) p.C[static_cast<int64_t>(g + j) * p.ldc + n] = w[j];
 }
 
-template <bool kInt>
-__global__ void __launch_bounds__(kThreads, 1)
+// kRawB (exact-int mode only): B is int8 as stored, converted to fp16 in
+// shared memory by kConvWarps extra warps (SkSmemI8).
+template <bool kInt, bool kRawB = false>
+__global__ void __launch_bounds__(kRawB ? kI8Threads : kThreads, 1)
     gemm_tc_skinny_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB, const SkArgs<kInt> p) {
+  static_assert(kInt || !kRawB, "int8 B as stored needs the exact-int mode");
   using Out = typename SkArgs<kInt>::Out;
+  using Smem = typename std::conditional<kRawB, SkSmemI8, SkSmem>::type;
+  constexpr int kS = Smem::kNumStages;
   extern __shared__ uint8_t smem_raw[];
-  SkSmem &sm = *reinterpret_cast<SkSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~uintptr_t(1023));
+  Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                       ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   volatile int *abort = &sm.abort;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kS; ++s) {
       mbar_init(smem_u32(&sm.full[s]), 1);
       mbar_init(smem_u32(&sm.empty[s]), 1);
+      if constexpr (kRawB) mbar_init(smem_u32(&sm.conv[s]), 32 * kConvWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sm.tmem_full[i]), 1);
@@ -207,7 +276,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    if constexpr (kRawB) {
+      // Raw B tiles (converted in shared memory) and their A tiles.
+      if (lane == 0) {
+        uint32_t stage = 0, phase = 0, issued = 0, issued_parity = 0;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&sm.empty[stage]), phase ^ 1u, abort, p.err_word,
+                                 kWaitEmpty))
+            break;
+          const uint32_t full_bar = smem_u32(&sm.full[stage]);
+          mbar_arrive_expect_tx(full_bar, kRawBytes + a_bytes);
+          tma_load_2d(smem_u32(sm.raw[stage]), &tmB, full_bar, n0, kb * kBK);
+          tma_load_2d(smem_u32(sm.a[stage]), &tmA, full_bar, kb * kBK, 0);
+          issued |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kS) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        for (int r = 0; r < kS; ++r)
+          if (issued & (1u << r))
+            drain_wait(smem_u32(&sm.full[r]), (issued_parity >> r) & 1u, p.err_word);
+      }
+    } else if (lane == 0) {
       uint32_t stage = 0, phase = 0, issued = 0, issued_parity = 0;
       for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait_bounded(smem_u32(&sm.empty[stage]), phase ^ 1u, abort, p.err_word,
@@ -220,12 +312,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(smem_u32(sm.a[stage]), &tmA, full_bar, kb * kBK, 0);
         issued |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == kStages) {
+        if (++stage == kS) {
           stage = 0;
           phase ^= 1u;
         }
       }
-      for (int s = 0; s < kStages; ++s)
+      for (int s = 0; s < kS; ++s)
         if (issued & (1u << s))
           drain_wait(smem_u32(&sm.full[s]), (issued_parity >> s) & 1u, p.err_word);
     }
@@ -245,8 +337,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + buf * kBufCols;
         for (int kb = c0; kb < c1; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&sm.full[stage]), phase, abort, p.err_word,
-                                 kWaitFull)) {
+          uint32_t ready;
+          if constexpr (kRawB)
+            ready = smem_u32(&sm.conv[stage]);  // converted by the converter warps
+          else
+            ready = smem_u32(&sm.full[stage]);
+          if (!mbar_wait_bounded(ready, phase, abort, p.err_word, kWaitFull)) {
             ok = false;
             break;
           }
@@ -264,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           any = true;
           tc_commit(smem_u32(&sm.empty[stage]));
-          if (++stage == kStages) {
+          if (++stage == kS) {
             stage = 0;
             phase ^= 1u;
           }
@@ -278,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else {
+  } else if (!kRawB || warp < 2 + kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     // Lanes are columns of C: lane -> column n0 + 32 * quarter + lane.
     const int quarter = warp & 3;
@@ -375,6 +471,27 @@ __global__ void __launch_bounds__(kThreads, 1)
               write_rows16<kInt>(p, n, g, sum);
             }
           }
+        }
+      }
+    }
+  }
+
+  if constexpr (kRawB) {
+    if (warp >= 2 + kEpiWarps) {
+      // --------------------------------------------------------- converter
+      // Each stage: wait for the raw tile, write its fp16 form, make the
+      // writes visible to the tensor core (async proxy), arrive.
+      const int ct = static_cast<int>(threadIdx.x) - 32 * (2 + kEpiWarps);
+      uint32_t stage = 0, phase = 0;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait_bounded(smem_u32(&sm.full[stage]), phase, abort, p.err_word, kWaitFull))
+          break;
+        convert_stage(smem_u32(sm.raw[stage]), smem_u32(sm.b[stage]), ct);
+        fence_proxy_async_shared();
+        mbar_arrive(smem_u32(&sm.conv[stage]));
+        if (++stage == kS) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
     }
@@ -776,6 +893,65 @@ cudaError_t launch_stream_k(const DeviceInfo &dev, SkArgs<kInt> p, const CUtenso
   return e != cudaSuccess ? e : f;
 }
 
+// One slice per CTA: column blocks times parts of k, at most one CTA per SM
+// when k is split (the per-block form of the kernel).
+template <bool kInt, bool kRawB>
+cudaError_t launch_per_block(const DeviceInfo &dev, SkArgs<kInt> p, const CUtensorMap &tmA,
+                             const CUtensorMap &tmB, int blocks, int nunits, cudaStream_t stream,
+                             uint32_t *flags_ws) {
+  const int M = p.M;
+  int split = blocks < dev.sm_count ? dev.sm_count / blocks : 1;
+  if (split > kMaxSplit) split = kMaxSplit;
+  if (split > nunits) split = nunits;
+  if (split < 1) split = 1;
+
+  // split > 1 needs a workspace for the partial sums (from the pool); a caller
+  // that provides its own memory gets whole column blocks instead.
+  if (flags_ws != nullptr) split = 1;
+  void *pool_ws = nullptr;
+  p.counters = nullptr;
+  p.ws = nullptr;
+  p.ws_ld = static_cast<int64_t>(blocks) * kBN;
+  if (split > 1) {
+    cudaMemPool_t pool;
+    cudaError_t e = device_pool(dev, &pool);
+    if (e != cudaSuccess) return e;
+    const size_t ws_bytes =
+        static_cast<size_t>(split) * M * p.ws_ld * sizeof(typename SkArgs<kInt>::Out);
+    const size_t cnt_off = (ws_bytes + 255) / 256 * 256;
+    e = cudaMallocFromPoolAsync(&pool_ws, cnt_off + static_cast<size_t>(blocks) * 4, pool,
+                                stream);
+    if (e != cudaSuccess) return e;
+    p.ws = static_cast<typename SkArgs<kInt>::Out *>(pool_ws);
+    p.counters = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(pool_ws) + cnt_off);
+    e = cudaMemsetAsync(p.counters, 0, static_cast<size_t>(blocks) * 4, stream);
+    if (e != cudaSuccess) {
+      cudaFreeAsync(pool_ws, stream);
+      return e;
+    }
+  }
+  p.split = split;
+
+  using Smem = typename std::conditional<kRawB, SkSmemI8, SkSmem>::type;
+  const size_t smem = sizeof(Smem) + 1024;
+  static_assert(sizeof(SkSmem) + 1024 <= 232448, "skinny kernel shared memory");
+  static_assert(sizeof(SkSmemI8) + 1024 <= 232448, "raw-int8 skinny kernel shared memory");
+  auto kern = gemm_tc_skinny_kernel<kInt, kRawB>;
+  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void *>(kern),
+                                       static_cast<int>(smem), dev.device);
+  if (e == cudaSuccess) {
+    kern<<<static_cast<unsigned>(blocks * split), kRawB ? kI8Threads : kThreads, smem, stream>>>(
+        tmA, tmB, p);
+    e = cudaGetLastError();
+  }
+  if (pool_ws) {
+    cudaError_t f = cudaFreeAsync(pool_ws, stream);
+    if (e == cudaSuccess) e = f;
+  }
+  return e;
+}
+
+
 template <bool kInt>
 cudaError_t launch(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf16, int M, int N,
                    int K, typename SkArgs<kInt>::Out alpha, const void *A, int64_t lda,
@@ -804,55 +980,23 @@ cudaError_t launch(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf16, 
   if (M > 8 && blocks >= 16 && blocks < dev.sm_count && flags_ws == nullptr &&
       static_cast<int64_t>(blocks) * nunits > dev.sm_count)
     return launch_stream_k<kInt>(dev, p, tmA, tmB, blocks, nunits, stream);
-  // One slice per CTA: column blocks times parts of k, at most one CTA per SM
-  // when k is split.
-  int split = blocks < dev.sm_count ? dev.sm_count / blocks : 1;
-  if (split > kMaxSplit) split = kMaxSplit;
-  if (split > nunits) split = nunits;
-  if (split < 1) split = 1;
-
-  // split > 1 needs a workspace for the partial sums (from the pool); a caller
-  // that provides its own memory gets whole column blocks instead.
-  if (flags_ws != nullptr) split = 1;
   (void)flags_words;
-  void *pool_ws = nullptr;
-  p.counters = nullptr;
-  p.ws = nullptr;
-  p.ws_ld = static_cast<int64_t>(blocks) * kBN;
-  if (split > 1) {
-    cudaMemPool_t pool;
-    cudaError_t e = device_pool(dev, &pool);
-    if (e != cudaSuccess) return e;
-    const size_t ws_bytes =
-        static_cast<size_t>(split) * M * p.ws_ld * sizeof(typename SkArgs<kInt>::Out);
-    const size_t cnt_off = (ws_bytes + 255) / 256 * 256;
-    e = cudaMallocFromPoolAsync(&pool_ws, cnt_off + static_cast<size_t>(blocks) * 4, pool,
-                                stream);
-    if (e != cudaSuccess) return e;
-    p.ws = static_cast<typename SkArgs<kInt>::Out *>(pool_ws);
-    p.counters = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(pool_ws) + cnt_off);
-    e = cudaMemsetAsync(p.counters, 0, static_cast<size_t>(blocks) * 4, stream);
-    if (e != cudaSuccess) {
-      cudaFreeAsync(pool_ws, stream);
-      return e;
-    }
-  }
-  p.split = split;
+  return launch_per_block<kInt, false>(dev, p, tmA, tmB, blocks, nunits, stream, flags_ws);
+}
 
-  const size_t smem = sizeof(SkSmem) + 1024;
-  static_assert(sizeof(SkSmem) + 1024 <= 232448, "skinny kernel shared memory");
-  auto kern = gemm_tc_skinny_kernel<kInt>;
-  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void *>(kern),
-                                       static_cast<int>(smem), dev.device);
-  if (e == cudaSuccess) {
-    kern<<<static_cast<unsigned>(blocks * split), kThreads, smem, stream>>>(tmA, tmB, p);
-    e = cudaGetLastError();
-  }
-  if (pool_ws) {
-    cudaError_t f = cudaFreeAsync(pool_ws, stream);
-    if (e == cudaSuccess) e = f;
-  }
-  return e;
+// Row-major rows x cols int8 matrix as bytes, boxes of 64 rows x 128 columns,
+// no swizzle (the raw tile the converter warps read).
+bool tmap8(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols, int64_t ld) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBN), static_cast<cuuint32_t>(kBK)};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -870,6 +1014,36 @@ cudaError_t launch_tc_skinny_float(const DeviceInfo &dev, bool is_bf16, int M, i
   return launch<false>(dev,
                        is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                        is_bf16, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, nullptr, 0);
+}
+
+bool tc_skinny_i8_supported(int M, const void *B, int64_t ldb) {
+  return M >= 1 && M <= kMaxM && reinterpret_cast<uintptr_t>(B) % 16 == 0 && ldb % 16 == 0;
+}
+
+cudaError_t launch_tc_skinny_i8(const DeviceInfo &dev, int M, int N, int K, int32_t alpha,
+                                const void *A16, int64_t lda, const int8_t *B, int64_t ldb,
+                                int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream) {
+  if (!tc_skinny_i8_supported(M, B, ldb)) return cudaErrorInvalidValue;
+  SkArgs<true> p;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.mp = (M + 15) / 16 * 16;
+  p.alpha = alpha;
+  p.beta = beta;
+  p.C = C;
+  p.ldc = ldc;
+  p.idesc = idesc_f16(false, /*a_mn_major=*/true, /*b_mn_major=*/false, kBN, p.mp);
+  p.err_word = dev.err_word;
+  CUtensorMap tmA, tmB;
+  if (!tmap16(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A16, M, K, lda,
+              static_cast<uint32_t>(p.mp)))
+    return cudaErrorInvalidValue;
+  if (!tmap8(&tmB, B, K, N, ldb)) return cudaErrorInvalidValue;
+  const int blocks = (N + kBN - 1) / kBN;
+  const int KB = (K + kBK - 1) / kBK;
+  const int nunits = (KB + kChunkKB - 1) / kChunkKB;
+  return launch_per_block<true, true>(dev, p, tmA, tmB, blocks, nunits, stream, nullptr);
 }
 
 cudaError_t launch_tc_skinny_int(const DeviceInfo &dev, int M, int N, int K, int32_t alpha,

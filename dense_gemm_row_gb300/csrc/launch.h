@@ -118,6 +118,22 @@ cudaError_t launch_tc_skinny_int(const DeviceInfo &dev, int M, int N, int K, int
                                  const void *A16, int64_t lda, const void *B16, int64_t ldb,
                                  int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream,
                                  uint32_t *flags, size_t flags_words);
+// The transposed-role kernel with int8 B read as stored (converted to fp16 in
+// shared memory; A already widened to fp16): M <= 64, B 16-byte aligned with
+// a row stride in whole 16-byte units (tc_skinny_i8_supported).
+bool tc_skinny_i8_supported(int M, const void *B, int64_t ldb);
+// gemm_s8 for short, wide problems through that kernel (gemm_tc_int.cu).
+cudaError_t launch_gemm_s8_skinny_raw(const DeviceInfo &dev, int M, int N, int K, int32_t alpha,
+                                      const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
+                                      int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream);
+// Rows from which gemm_s8 prefers it over the dp4a small-M kernel.
+#ifndef DGR_I8RAW_MIN_M
+#define DGR_I8RAW_MIN_M 10
+#endif
+constexpr int kI8RawMinM = DGR_I8RAW_MIN_M;
+cudaError_t launch_tc_skinny_i8(const DeviceInfo &dev, int M, int N, int K, int32_t alpha,
+                                const void *A16, int64_t lda, const int8_t *B, int64_t ldb,
+                                int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream);
 
 // Raises a kernel's dynamic shared-memory limit on the current device, once
 // per (kernel, device); later calls only look the pair up.

@@ -335,6 +335,36 @@ def test_skinny_stream_k(gemm_mod, oracle_mod, dtype, shape):
     out.check_canaries()
 
 
+@pytest.mark.parametrize("shape", [(9, 2048, 2048, 1000), (16, 4100, 4112, 3072),
+                                   (16, 8192, 8192, 4101), (33, 2048, 2064, 2049),
+                                   (48, 4096, 4096, 1024), (64, 8192, 8192, 3072),
+                                   (64, 4100, 4112, 4101), (12, 16384, 16384, 512)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_skinny_int8_b_as_stored(gemm_mod, oracle_mod, shape):
+    """int8 with 9..64 rows, at least 16 column blocks and B rows in whole
+    16-byte units: the transposed-role kernel reads B as stored and its
+    converter warps widen each tile to fp16 in shared memory. Ragged N under a
+    padded row stride, K not a multiple of the 64-deep tile (zero-filled
+    tail), beta != 0; every output bit-exact."""
+    M, N, ldb, K = shape
+    p = w.problem(M, N, K, torch.int8, "int8", 601 + M, alpha=-3, beta=2, c_dist="int", ldb=ldb)
+    got, out = run_gpu(gemm_mod, p)
+    assert_parity(got, oracle_of(oracle_mod, p), exact=True)
+    out.check_canaries()
+
+
+def test_skinny_int8_b_as_stored_extremes(gemm_mod, oracle_mod):
+    """All -128: every 1024-k chunk sums to 1024 * 16384 = 2^24, the largest
+    value the exact fp32 chunks must hold; K = 4096 spans four chunks."""
+    M, N, K = 32, 2048, 4096
+    A = torch.full((M, K), -128, dtype=torch.int8)
+    B = torch.full((K, N), -128, dtype=torch.int8)
+    C = torch.zeros(M, N, dtype=torch.int32, device="cuda")
+    gemm_mod.gemm(A.cuda(), B.cuda(), C)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(C.cpu().numpy(), oracle_mod.gemm_s8(A, B))
+
+
 @pytest.mark.parametrize("dtype", ALL_DTYPES, ids=str)
 @pytest.mark.parametrize("shape", [(8, 520, 8192), (32, 1024, 4096), (1, 128, 16384),
                                    (3, 4096, 2048)], ids=lambda s: "x".join(map(str, s)))
