@@ -335,17 +335,18 @@ def test_skinny_stream_k(gemm_mod, oracle_mod, dtype, shape):
     out.check_canaries()
 
 
-@pytest.mark.parametrize("shape", [(9, 2048, 2048, 1000), (16, 4100, 4112, 3072),
-                                   (16, 8192, 8192, 4101), (33, 2048, 2064, 2049),
+@pytest.mark.parametrize("shape", [(10, 2048, 2048, 1000), (16, 4100, 4112, 3072),
+                                   (16, 8192, 8192, 4101), (24, 4096, 4096, 2048),
+                                   (32, 2048, 2064, 3000), (33, 2048, 2064, 2049),
                                    (48, 4096, 4096, 1024), (64, 8192, 8192, 3072),
                                    (64, 4100, 4112, 4101), (12, 16384, 16384, 512)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_skinny_int8_b_as_stored(gemm_mod, oracle_mod, shape):
-    """int8 with 9..64 rows, at least 16 column blocks and B rows in whole
+    """int8 with 10..64 rows, at least 16 column blocks and B rows in whole
     16-byte units: the transposed-role kernel reads B as stored and its
-    converter warps widen each tile to fp16 in shared memory. Ragged N under a
-    padded row stride, K not a multiple of the 64-deep tile (zero-filled
-    tail), beta != 0; every output bit-exact."""
+    converter warps widen each tile to fp16 in shared memory (A slots for 16,
+    32 or 64 rows). Ragged N under a padded row stride, K not a multiple of
+    the 64-deep tile (zero-filled tail), beta != 0; every output bit-exact."""
     M, N, ldb, K = shape
     p = w.problem(M, N, K, torch.int8, "int8", 601 + M, alpha=-3, beta=2, c_dist="int", ldb=ldb)
     got, out = run_gpu(gemm_mod, p)
