@@ -71,6 +71,18 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace
 
+cudaError_t launch_transpose_f32(const DeviceInfo &dev, const float *src, int64_t lds, int rows,
+                                 int cols, float *dst, int64_t ldd, cudaStream_t stream) {
+  const int64_t tiles = (static_cast<int64_t>(rows) + 63) / 64 * ((cols + 63) / 64);
+  const int64_t blocks = tiles < static_cast<int64_t>(dev.sm_count) * 8 ? tiles : dev.sm_count * 8;
+  const int vec_src = (reinterpret_cast<uintptr_t>(src) % 16 == 0) && (lds % 4 == 0);
+  const int vec_dst = (reinterpret_cast<uintptr_t>(dst) % 16 == 0) && (ldd % 4 == 0);
+  if (blocks < 1) return cudaSuccess;
+  transpose_f32_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(src, lds, dst, ldd, rows,
+                                                                         cols, vec_src, vec_dst);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gemm_tf32(const DeviceInfo &dev, int M, int N, int K, float alpha,
                              const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
                              float *C, int64_t ldc, cudaStream_t stream) {
@@ -95,15 +107,7 @@ cudaError_t launch_gemm_tf32(const DeviceInfo &dev, int M, int N, int K, float a
     a = a_copy;
     lda_used = ldk;
   }
-  if (e == cudaSuccess) {
-    const int64_t tiles = (static_cast<int64_t>(K) + 63) / 64 * ((N + 63) / 64);
-    int64_t blocks = tiles < static_cast<int64_t>(dev.sm_count) * 8 ? tiles : dev.sm_count * 8;
-    const int vec_src = (reinterpret_cast<uintptr_t>(B) % 16 == 0) && (ldb % 4 == 0);
-    const int vec_dst = 1;  // bt: 256-byte aligned, ldk a multiple of 4
-    transpose_f32_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(B, ldb, bt, ldk, K,
-                                                                           N, vec_src, vec_dst);
-    e = cudaGetLastError();
-  }
+  if (e == cudaSuccess) e = launch_transpose_f32(dev, B, ldb, K, N, bt, ldk, stream);
   if (e == cudaSuccess) {
     BatchOps ops;
     ops.b_t = true;  // B is now the N x K copy

@@ -135,6 +135,12 @@ cudaError_t launch_tc_skinny_i8(const DeviceInfo &dev, int M, int N, int K, int3
                                 const void *A16, int64_t lda, const int8_t *B, int64_t ldb,
                                 int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream);
 
+// dst (cols x rows, row stride ldd) = transpose of the row-major rows x cols
+// fp32 matrix src (row stride lds): 64 x 64 tiles through shared memory
+// (gemm_tc_tf32.cu).
+cudaError_t launch_transpose_f32(const DeviceInfo &dev, const float *src, int64_t lds, int rows,
+                                 int cols, float *dst, int64_t ldd, cudaStream_t stream);
+
 // Raises a kernel's dynamic shared-memory limit on the current device, once
 // per (kernel, device); later calls only look the pair up.
 cudaError_t set_max_dynamic_smem(const void *kernel, int bytes, int device);

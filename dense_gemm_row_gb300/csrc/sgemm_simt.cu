@@ -408,6 +408,7 @@ int resident_ctas(const DeviceInfo &dev, const void *kern, int threads, size_t s
 }
 
 constexpr int kSimtMaxSplit = 4;  // parts per leftover tile (each adds one pass over its C)
+constexpr int kTransposeBMinM = 1024;  // rows from which a transposed B is transposed first
 
 // The two kernel shapes: full grids (TN = 16, 8-deep k tiles, 6 stages) and
 // under-filled single problems on the k-split grid (TN = 8, 32-deep, 2 stages).
@@ -541,6 +542,29 @@ cudaError_t launch_sgemm_simt_ex(const DeviceInfo &dev, const BatchOps &ops, int
   // 128-thread shape, one CTA per tile.
   const int64_t ctas = static_cast<int64_t>(a.tiles_m) * a.tiles_n * batch;
   const bool full = ctas >= 4LL * dev.sm_count;
+  // B stored N x K, one problem, a full grid and many rows: B is transposed
+  // once into pool scratch (N K values read and written, against the M N K
+  // product) and the problem runs with the straight, 16-byte B copy, which
+  // measures faster than the transposing one.
+  if (ops.b_t && batch == 1 && full && M >= kTransposeBMinM) {
+    const int64_t ldn = (static_cast<int64_t>(N) + 3) / 4 * 4;
+    cudaMemPool_t pool = nullptr;
+    cudaError_t e = device_pool(dev, &pool);
+    if (e != cudaSuccess) return e;
+    void *scratch = nullptr;
+    e = cudaMallocFromPoolAsync(&scratch, static_cast<size_t>(K) * ldn * 4, pool, stream);
+    if (e != cudaSuccess) return e;
+    float *bt = static_cast<float *>(scratch);
+    e = launch_transpose_f32(dev, B, ldb, N, K, bt, ldn, stream);  // stored N x K -> K x N
+    if (e == cudaSuccess) {
+      BatchOps straight = ops;
+      straight.b_t = false;
+      e = launch_sgemm_simt_ex(dev, straight, M, N, K, alpha, A, lda, bt, ldn, beta, C, ldc,
+                               stream);
+    }
+    cudaError_t f = cudaFreeAsync(scratch, stream);
+    return e != cudaSuccess ? e : f;
+  }
   if (ops.plain()) {  // one problem, no transposes
     if (!full)
       return vec_b ? launch_variant<SimtNarrow, false, false, false, true, kModeSplit>(a, 1, dev,

@@ -152,6 +152,20 @@ def test_f32_batch_full_grid(gemm_mod, oracle_mod, ops, aligned_ld):
         run_case(gemm_mod, oracle_mod, torch.float32, ops, 40, 500, 510, 137, seed=29)
 
 
+@pytest.mark.parametrize("aligned_ld", [False, True], ids=["ld_odd", "ld_mod4"])
+@pytest.mark.parametrize("ops", ["NT", "TT"])
+def test_f32_transposed_b_many_rows(gemm_mod, oracle_mod, ops, aligned_ld):
+    """fp32, B stored N x K, one problem of at least two waves of tiles and
+    >= 1024 rows: B is first transposed into scratch, then the straight-B
+    kernel runs. Ragged N with an odd row stride (4-byte transpose reads) and
+    16-byte-aligned strides."""
+    if aligned_ld:
+        run_case(gemm_mod, oracle_mod, torch.float32, ops, 1, 3200, 3200, 136, seed=31,
+                 gap=4, extra=4)
+    else:
+        run_case(gemm_mod, oracle_mod, torch.float32, ops, 1, 3200, 3203, 137, seed=37)
+
+
 @pytest.mark.parametrize("ops", OPS)
 @pytest.mark.parametrize("dtype", DTYPES, ids=str)
 def test_single_entry_transposed(gemm_mod, oracle_mod, dtype, ops):
