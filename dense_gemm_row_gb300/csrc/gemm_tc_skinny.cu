@@ -34,6 +34,11 @@
 // column blocks (many contributors per block). 33..64 rows take this kernel
 // only in the stream-K form (tc_skinny_route).
 //
+// int8 B as stored (the per-block form with kRawB, gemm_s8 with 10..64
+// rows): TMA brings raw byte tiles of B, and four converter warps widen each
+// tile exactly to fp16 in shared memory before the MMA reads it, so B crosses
+// HBM once as bytes instead of being widened to a 16-bit copy first.
+//
 // Sources: as gemm_tc_kernel.cuh (C = alpha*A*B + beta*C, "Sgemm [128,128,8]"; half /
 // bfloat16 x half / bfloat16 -> float and signed char -> int, C++ warp matrix
 // function page, type table). The pages have no skinny-shape kernel; this is a
