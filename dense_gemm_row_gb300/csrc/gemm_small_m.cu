@@ -65,6 +65,9 @@ template <bool kInt>
 struct __align__(128) SmSmem {
   uint8_t b[kStages][SmCfg<kInt>::kBBytes];  // b[s][k][n]
   uint8_t a[kStages][SmCfg<kInt>::kABytes];  // a[s][m][k] (rows of A)
+  // fp32: each consumer warp's k-major copy of the current stage's A tile
+  // (row stride kMaxM + 4: rows stay 16-byte aligned, stores spread over banks)
+  float at[8][16][kMaxM + 4];
   uint64_t full[kStages];
   uint64_t empty[kStages];
   int abort;
@@ -87,6 +90,14 @@ struct SmArgs {
 
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, 256;" ::: "memory");
+}
+
+// (c0, c1) = (a0 * b + c0, a1 * b + c1) with one packed fp32 FMA.
+__device__ __forceinline__ void ffma2_rows(float &c0, float &c1, float a0, float a1, float b) {
+  asm("{\n .reg .b64 ra, rb, rc;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %4};\n"
+      " mov.b64 rc, {%0, %1};\n fma.rn.f32x2 rc, ra, rb, rc;\n mov.b64 {%0, %1}, rc;\n}\n"
+      : "+f"(c0), "+f"(c1)
+      : "f"(a0), "f"(a1), "f"(b));
 }
 
 // (c0, c1) = (a * b0 + c0, a * b1 + c1) with one packed fp32 FMA.
@@ -194,7 +205,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       // B box j covers columns kBoxW*j .. of the block: KC rows of kBoxW.
       constexpr int W = Cf::kBoxW;
       const In *bcol = bs + (col / W) * (KC * W) + (col % W);
-      if constexpr (!kInt) {
+      if constexpr (!kInt && MP >= 4) {
+        // A tile to k-major (at[k][m]) so that rows m, m+1 of one k are a pair
+        // in one 16-byte load; then (acc[m][j], acc[m+1][j]) += (a[m], a[m+1])
+        // * b[j]: only b[j] is duplicated into a register pair, once per k and
+        // column for all rows (with A's rows paired the other way, every row's
+        // value needed its own pair).
+        // Each warp makes its own copy, so no barrier wider than the warp is
+        // needed (the __syncwarp ending the previous stage separates its reads
+        // from these writes).
+        static_assert(KC == 16, "the k-major copy holds 16 values of k");
+        float (*at)[kMaxM + 4] = sm.at[warp - 1];
+        for (int e = lane; e < MP * KC; e += 32) at[e % KC][e / KC] = as[e];
+        __syncwarp();
+#pragma unroll 4
+        for (int kq = 0; kq < KC; kq += 4) {
+          float4 b4[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            b4[u] = *reinterpret_cast<const float4 *>(bcol + (kq + u) * W);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float b[4] = {b4[u].x, b4[u].y, b4[u].z, b4[u].w};
+#pragma unroll
+            for (int m = 0; m < MP; m += 4) {
+              const float4 a4 = *reinterpret_cast<const float4 *>(&at[kq + u][m]);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                ffma2_rows(acc[m][j], acc[m + 1][j], a4.x, a4.y, b[j]);
+                ffma2_rows(acc[m + 2][j], acc[m + 3][j], a4.z, a4.w, b[j]);
+              }
+            }
+          }
+        }
+      } else if constexpr (!kInt) {
 #pragma unroll 4
         for (int kq = 0; kq < KC; kq += 4) {
           float4 b4[4];
