@@ -298,8 +298,9 @@ GEMM_API gemm_status_t gemm_selftest_wait_timeout(uint32_t limit_us, cudaStream_
  * 2 * 128 * 256 * 16. Its one wait (for the last MMA) is bounded like the
  * GEMM kernels' waits.
  *
- * Both return GEMM_ERR_INVALID_VALUE for iters outside 1 .. 2^24 (or a NULL
- * sink for gemm_peak_ffma), else the launch status. Source: the rooflines are
+ * Both return GEMM_ERR_INVALID_VALUE for iters outside 1 .. 2^24 (gemm_peak_ffma;
+ * also for a NULL sink) or 1 .. 2^20 (gemm_peak_tc_f16: at most about 0.3 s of
+ * MMAs, well inside the bound on its wait), else the launch status. Source: the rooflines are
  * bounded by these two pipes ("Sgemm [128,128,8]": FFMA-bound inner loop; the
  * C++ warp-matrix-function page: tensor-core matrix multiply-accumulate).
  */

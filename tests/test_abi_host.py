@@ -163,3 +163,4 @@ def test_peak_microbenchmarks_check_arguments_on_host(gemm_mod):
     assert lib.gemm_peak_ffma(16, None, None, None) == INVALID
     assert lib.gemm_peak_tc_f16(0, None, None) == INVALID
     assert lib.gemm_peak_tc_f16(-5, None, None) == INVALID
+    assert lib.gemm_peak_tc_f16((1 << 20) + 1, None, None) == INVALID
