@@ -59,11 +59,11 @@ WORKLOADS = {
     "f16_8192": ("fp16 GEMM, row-major, M=N=K=8192, N(0,1) rounded to fp16, fp32 accumulate "
                  "and fp32 C, alpha=1, beta=0", "f16", "tensor", 1),
     "f32_4096": ("fp32 SGEMM (SIMT, exact fp32), row-major, M=N=K=4096, N(0,1), alpha=1, beta=0",
-                 "f32", "alu", 1),
+                 "f32", "alu", 2),
     "s8_8192": ("int8 GEMM, row-major, M=N=K=8192, uniform -128..127, exact int32 accumulate "
                 "and int32 C, alpha=1, beta=0", "s8", "tensor", 3),
     "f32_8192": ("fp32 SGEMM (SIMT, exact fp32), row-major, M=N=K=8192, N(0,1), alpha=1, beta=0",
-                 "f32", "alu", 1),
+                 "f32", "alu", 2),
     "bf16_4096": ("bf16 GEMM, row-major, M=N=K=4096, N(0,1) rounded to bf16, fp32 accumulate "
                   "and fp32 C, alpha=1, beta=0", "bf16", "tensor", 1),
     "s8_4096": ("int8 GEMM, row-major, M=N=K=4096, uniform -128..127, exact int32 accumulate "
@@ -542,6 +542,8 @@ def measure_extra(binding, torch, w, name, peaks, sm_count, stream, gpu_id):
         out["frac_at_sampled_clock"] = ach / (sm_count * 128 * 2 * clocks["sm_mhz"] * 1e6 / 1e12)
     if kind == "s8":
         out["note"] = "step includes the two int8->fp16 widening launches"
+    elif kind == "f32":
+        out["note"] = "step includes the transposition of A ahead of the SIMT kernel"
     del q_dev
     torch.cuda.empty_cache()
     return out
@@ -753,6 +755,9 @@ def main():
                 "kernel_ms": kernel_ms}
     if kind == "s8":
         roofline["note"] = "step time includes the two int8->fp16 widening launches"
+    elif kind == "f32":
+        roofline["note"] = ("step time includes the transposition of A (M x K -> K x M) that "
+                            "lets the SIMT kernel copy A tiles in 16-byte chunks")
     if kind != "f32":
         # Context for a long timed loop: the measured sustained (power-capped)
         # peak, and the fraction of the dense rate at the clock sampled during

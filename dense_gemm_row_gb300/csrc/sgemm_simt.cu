@@ -409,6 +409,7 @@ int resident_ctas(const DeviceInfo &dev, const void *kern, int threads, size_t s
 
 constexpr int kSimtMaxSplit = 4;  // parts per leftover tile (each adds one pass over its C)
 constexpr int kTransposeBMinM = 1024;  // rows from which a transposed B is transposed first
+constexpr int kTransposeAMinN = 2048;  // columns from which A is transposed first
 
 // The two kernel shapes: full grids (TN = 16, 8-deep k tiles, 6 stages) and
 // under-filled single problems on the k-split grid (TN = 8, 32-deep, 2 stages).
@@ -560,6 +561,28 @@ cudaError_t launch_sgemm_simt_ex(const DeviceInfo &dev, const BatchOps &ops, int
       BatchOps straight = ops;
       straight.b_t = false;
       e = launch_sgemm_simt_ex(dev, straight, M, N, K, alpha, A, lda, bt, ldn, beta, C, ldc,
+                               stream);
+    }
+    cudaError_t f = cudaFreeAsync(scratch, stream);
+    return e != cudaSuccess ? e : f;
+  }
+  // Likewise A stored M x K with many columns: A transposed once (M K values,
+  // against the M N K product) lets the k-major A tile be filled by the straight
+  // 16-byte copy instead of the 4-byte transposing one.
+  if (!ops.a_t && batch == 1 && full && N >= kTransposeAMinN) {
+    const int64_t ldm = (static_cast<int64_t>(M) + 3) / 4 * 4;
+    cudaMemPool_t pool = nullptr;
+    cudaError_t e = device_pool(dev, &pool);
+    if (e != cudaSuccess) return e;
+    void *scratch = nullptr;
+    e = cudaMallocFromPoolAsync(&scratch, static_cast<size_t>(K) * ldm * 4, pool, stream);
+    if (e != cudaSuccess) return e;
+    float *at = static_cast<float *>(scratch);
+    e = launch_transpose_f32(dev, A, lda, M, K, at, ldm, stream);  // M x K -> K x M
+    if (e == cudaSuccess) {
+      BatchOps straight = ops;
+      straight.a_t = true;
+      e = launch_sgemm_simt_ex(dev, straight, M, N, K, alpha, at, ldm, B, ldb, beta, C, ldc,
                                stream);
     }
     cudaError_t f = cudaFreeAsync(scratch, stream);
