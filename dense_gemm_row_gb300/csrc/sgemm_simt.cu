@@ -510,10 +510,14 @@ bool vec_ok(const float *base, int64_t ld, int64_t cols, int batch, int64_t stri
 
 }  // namespace
 
-cudaError_t launch_sgemm_simt_ex(const DeviceInfo &dev, const BatchOps &ops, int M, int N, int K,
-                                 float alpha, const float *A, int64_t lda, const float *B,
-                                 int64_t ldb, float beta, float *C, int64_t ldc,
-                                 cudaStream_t stream) {
+namespace {
+
+// The fp32 GEMM; transpose_first enables the one-off transposition of a
+// stored-transposed B or a stored A into pool scratch on large problems.
+cudaError_t sgemm_simt_run(const DeviceInfo &dev, const BatchOps &ops, int M, int N, int K,
+                           float alpha, const float *A, int64_t lda, const float *B, int64_t ldb,
+                           float beta, float *C, int64_t ldc, cudaStream_t stream,
+                           bool transpose_first) {
   SimtArgs a;
   a.M = M;
   a.N = N;
@@ -547,21 +551,25 @@ cudaError_t launch_sgemm_simt_ex(const DeviceInfo &dev, const BatchOps &ops, int
   // once into pool scratch (N K values read and written, against the M N K
   // product) and the problem runs with the straight, 16-byte B copy, which
   // measures faster than the transposing one.
-  if (ops.b_t && batch == 1 && full && M >= kTransposeBMinM) {
+  if (transpose_first && ops.b_t && batch == 1 && full && M >= kTransposeBMinM) {
     const int64_t ldn = (static_cast<int64_t>(N) + 3) / 4 * 4;
     cudaMemPool_t pool = nullptr;
     cudaError_t e = device_pool(dev, &pool);
     if (e != cudaSuccess) return e;
     void *scratch = nullptr;
     e = cudaMallocFromPoolAsync(&scratch, static_cast<size_t>(K) * ldn * 4, pool, stream);
+    if (e == cudaErrorMemoryAllocation) {  // no room for the copy: the transposing copy path
+      cudaGetLastError();
+      return sgemm_simt_run(dev, ops, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, false);
+    }
     if (e != cudaSuccess) return e;
     float *bt = static_cast<float *>(scratch);
     e = launch_transpose_f32(dev, B, ldb, N, K, bt, ldn, stream);  // stored N x K -> K x N
     if (e == cudaSuccess) {
       BatchOps straight = ops;
       straight.b_t = false;
-      e = launch_sgemm_simt_ex(dev, straight, M, N, K, alpha, A, lda, bt, ldn, beta, C, ldc,
-                               stream);
+      e = sgemm_simt_run(dev, straight, M, N, K, alpha, A, lda, bt, ldn, beta, C, ldc, stream,
+                         true);
     }
     cudaError_t f = cudaFreeAsync(scratch, stream);
     return e != cudaSuccess ? e : f;
@@ -569,21 +577,25 @@ cudaError_t launch_sgemm_simt_ex(const DeviceInfo &dev, const BatchOps &ops, int
   // Likewise A stored M x K with many columns: A transposed once (M K values,
   // against the M N K product) lets the k-major A tile be filled by the straight
   // 16-byte copy instead of the 4-byte transposing one.
-  if (!ops.a_t && batch == 1 && full && N >= kTransposeAMinN) {
+  if (transpose_first && !ops.a_t && batch == 1 && full && N >= kTransposeAMinN) {
     const int64_t ldm = (static_cast<int64_t>(M) + 3) / 4 * 4;
     cudaMemPool_t pool = nullptr;
     cudaError_t e = device_pool(dev, &pool);
     if (e != cudaSuccess) return e;
     void *scratch = nullptr;
     e = cudaMallocFromPoolAsync(&scratch, static_cast<size_t>(K) * ldm * 4, pool, stream);
+    if (e == cudaErrorMemoryAllocation) {  // no room for the copy: the transposing copy path
+      cudaGetLastError();
+      return sgemm_simt_run(dev, ops, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, false);
+    }
     if (e != cudaSuccess) return e;
     float *at = static_cast<float *>(scratch);
     e = launch_transpose_f32(dev, A, lda, M, K, at, ldm, stream);  // M x K -> K x M
     if (e == cudaSuccess) {
       BatchOps straight = ops;
       straight.a_t = true;
-      e = launch_sgemm_simt_ex(dev, straight, M, N, K, alpha, at, ldm, B, ldb, beta, C, ldc,
-                               stream);
+      e = sgemm_simt_run(dev, straight, M, N, K, alpha, at, ldm, B, ldb, beta, C, ldc, stream,
+                         true);
     }
     cudaError_t f = cudaFreeAsync(scratch, stream);
     return e != cudaSuccess ? e : f;
@@ -601,6 +613,15 @@ cudaError_t launch_sgemm_simt_ex(const DeviceInfo &dev, const BatchOps &ops, int
   }
   return full ? launch_ops<SimtWide>(a, ops.a_t, vec_a, ops.b_t, vec_b, batch, dev, stream)
               : launch_ops<SimtNarrow>(a, ops.a_t, vec_a, ops.b_t, vec_b, batch, dev, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_sgemm_simt_ex(const DeviceInfo &dev, const BatchOps &ops, int M, int N, int K,
+                                 float alpha, const float *A, int64_t lda, const float *B,
+                                 int64_t ldb, float beta, float *C, int64_t ldc,
+                                 cudaStream_t stream) {
+  return sgemm_simt_run(dev, ops, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, true);
 }
 
 cudaError_t launch_sgemm_simt(const DeviceInfo &dev, int M, int N, int K, float alpha,
