@@ -671,6 +671,28 @@ def measure_types(binding, torch, peaks, stream):
     return out
 
 
+# ------------------------------------------------------------ compact summary
+
+def compact_configs(name, head, extras, skinny, types):
+    """One short entry per measured workload -- [value (TFLOP/s or TOPS),
+    fraction of its pipe's peak, ms per call, median SM MHz, throttle reasons]
+    -- plus the fraction of HBM bandwidth of each short, wide shape and the
+    batched many-small fraction."""
+    def entry(d):
+        c = d.get("clocks") or {}
+        mhz = c.get("sm_mhz")
+        return [round(d["value"], 1), round(d["frac"], 3), round(d["ms_per_step"], 4),
+                None if mhz is None else round(mhz), c.get("reasons", [])]
+    out = {"key": "[value, frac_of_peak, ms, sm_mhz, reasons]", name: entry(head)}
+    for k, d in extras.items():
+        out[k] = entry(d)
+    if skinny:
+        out["skinny_frac_hbm"] = {k: round(d["frac_hbm"], 3) for k, d in skinny.items()}
+    if "bf16_batched_64x1024" in types:
+        out["bf16_batched_64x1024_frac"] = round(types["bf16_batched_64x1024"]["frac"], 3)
+    return out
+
+
 # ----------------------------------------------------------------------- main
 
 def main():
@@ -836,7 +858,12 @@ def main():
         "skinny": skinny,
         "types": types,
     }
-    print(json.dumps(line), flush=True)
+    # Last, so that a reader keeping only the end of the line still has every
+    # config's throughput, roofline fraction and clock record.
+    line["configs"] = compact_configs(name, {"value": value, "ms_per_step": step_ms,
+                                             "frac": achieved / peak,
+                                             "clocks": clocks}, extras, skinny, types)
+    print(json.dumps(line, separators=(",", ":")), flush=True)
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()

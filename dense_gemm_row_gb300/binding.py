@@ -45,7 +45,7 @@ EXPORTED = ("gemm_f32", "gemm_bf16", "gemm_f16", "gemm_s8", "gemm_u8", "gemm_f16
             "gemm_bf16_bf16", "gemm_tf32", "gemm_f64", "gemm_f32_ex", "gemm_bf16_ex",
             "gemm_f16_ex", "gemm_s8_ex", "gemm_s8_noalloc", "gemm_status_string",
             "gemm_check_device_error", "gemm_selftest_wait_timeout", "gemm_last_launch_error",
-            "gemm_peak_ffma", "gemm_peak_tc_f16", "gemm_version")
+            "gemm_peak_ffma", "gemm_peak_tc_f16", "gemm_pool_usage", "gemm_version")
 
 OP_N, OP_T = 0, 1  # gemm_op_t
 
@@ -98,6 +98,8 @@ def _load():
     lib.gemm_peak_tc_f16.restype = ctypes.c_int
     lib.gemm_version.argtypes = []
     lib.gemm_version.restype = ctypes.c_int
+    lib.gemm_pool_usage.argtypes = [ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.c_int]
+    lib.gemm_pool_usage.restype = ctypes.c_int
     return lib
 
 
@@ -211,6 +213,16 @@ def peak_tc_f16(iters, stream=None) -> float:
     f = ctypes.c_double(0.0)
     _check(lib.gemm_peak_tc_f16(int(iters), ctypes.byref(f), _stream(stream)), "gemm_peak_tc_f16")
     return f.value
+
+
+def pool_usage(reset_high: bool = False) -> tuple[int, int]:
+    """(high-water mark of bytes in use, bytes reserved) of the library's memory
+    pool on the current device; reset_high clears the mark after reading."""
+    used = ctypes.c_int64(0)
+    reserved = ctypes.c_int64(0)
+    _check(lib.gemm_pool_usage(ctypes.byref(used), ctypes.byref(reserved), int(reset_high)),
+           "gemm_pool_usage")
+    return used.value, reserved.value
 
 
 def check_device_error() -> int:

@@ -195,10 +195,12 @@ cudaError_t set_max_dynamic_smem(const void *kernel, int bytes, int device) {
 // Library-owned stream-ordered memory pool of a device (scratch for the 8-bit
 // paths, the tf32 operand copies and split-k workspaces); freed blocks stay
 // mapped for reuse.
+std::mutex g_pool_mu;
+cudaMemPool_t g_pools[kMaxDevices] = {};
+
 cudaError_t device_pool(const DeviceInfo &dev, cudaMemPool_t *out) {
-  static std::mutex mu;
-  static cudaMemPool_t pools[kMaxDevices] = {};
-  std::lock_guard<std::mutex> lock(mu);
+  std::lock_guard<std::mutex> lock(g_pool_mu);
+  cudaMemPool_t *pools = g_pools;
   if (dev.device < 0 || dev.device >= kMaxDevices) return cudaErrorInvalidDevice;
   if (!pools[dev.device]) {
     cudaMemPoolProps props;
@@ -274,6 +276,35 @@ using dgr::DeviceInfo;
 using dgr::from_cuda;
 
 extern "C" {
+
+gemm_status_t gemm_pool_usage(int64_t *used_high_bytes, int64_t *reserved_bytes, int reset_high) {
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= dgr::kMaxDevices) {
+    cudaGetLastError();
+    return GEMM_ERR_DEVICE;
+  }
+  uint64_t used_high = 0, reserved = 0;
+  std::lock_guard<std::mutex> lock(dgr::g_pool_mu);
+  cudaMemPool_t pl = dgr::g_pools[device];
+  if (pl != nullptr) {  // no pool yet: nothing was ever taken from it
+    if (cudaMemPoolGetAttribute(pl, cudaMemPoolAttrUsedMemHigh, &used_high) != cudaSuccess ||
+        cudaMemPoolGetAttribute(pl, cudaMemPoolAttrReservedMemCurrent, &reserved) !=
+            cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_LAUNCH;
+    }
+    if (reset_high) {
+      uint64_t zero = 0;
+      if (cudaMemPoolSetAttribute(pl, cudaMemPoolAttrUsedMemHigh, &zero) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+      }
+    }
+  }
+  if (used_high_bytes) *used_high_bytes = static_cast<int64_t>(used_high);
+  if (reserved_bytes) *reserved_bytes = static_cast<int64_t>(reserved);
+  return GEMM_OK;
+}
 
 gemm_status_t gemm_f32(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
                        const float *B, int64_t ldb, float beta, float *C, int64_t ldc,

@@ -8,8 +8,12 @@ uniform -128..127 for int8; alpha = 1, beta = 0), runs the entry point a few
 times as warm-up, then times --iters back-to-back calls with CUDA events on
 one stream and prints one JSON line: milliseconds per call, TFLOP/s (TOPS for
 int8) and the GB/s of the algorithmic bytes (A and B read once, C written
-once). Used for the per-shape measurements in profiles/ (run it under ncu with
-a small --iters).
+once). Used for the per-shape measurements in profiles/. To profile it, run it
+with a small --iters under an ncu that leaves the GPU clocks alone and captures
+one kernel, e.g.
+    ncu --clock-control none --metrics gpu__time_duration.sum -k regex:gemm_tc -c 3 \
+        python -m dense_gemm_row_gb300.timing --dtype bf16 --shape 16,8192,8192 --iters 3
+(without --clock-control none, ncu locks the clocks of a GPU others share).
 
 --ops and --batch time the extended entry points (gemm_*_ex): a stack of B
 problems, each operand stored as op says (T: the transpose is stored); the

@@ -240,7 +240,11 @@ GEMM_API gemm_status_t gemm_s8_ex(gemm_op_t opA, gemm_op_t opB, int64_t M, int64
  * checks are those of gemm_s8.
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture begins. A failed look-up returns GEMM_ERR_DEVICE.
+ * any stream capture begins. A failed look-up returns GEMM_ERR_DEVICE, clears
+ * the CUDA runtime's last-error state of the calling thread (including an
+ * error an earlier asynchronous launch may have left there), and is
+ * remembered: every later call on that device returns GEMM_ERR_DEVICE too,
+ * for the life of the process (the look-up is not retried).
  * Concurrency: all calls on a device share the one array, and each call
  * overwrites every scratch element it later reads, so no state carries over
  * from the previous call; but calls that can overlap on the GPU (different
@@ -314,6 +318,23 @@ GEMM_API gemm_status_t gemm_peak_tc_f16(int32_t iters, double *flops, cudaStream
  * "cudaSuccess" if there was none. A static string; never NULL.
  */
 GEMM_API const char *gemm_last_launch_error(void);
+
+/*
+ * Usage of the library's own stream-ordered memory pool on the current device
+ * (the pool that gemm_s8, gemm_u8, gemm_tf32, the fp32 transposing paths and
+ * the split-k workspaces draw their scratch from). *used_high_bytes receives
+ * the most memory in use at one time since the pool was created or the mark
+ * was last reset; *reserved_bytes the device memory the pool holds now (freed
+ * blocks stay reserved for reuse). Either pointer may be NULL. reset_high != 0
+ * resets the high-water mark to zero after reading it. Before the first call
+ * that needs the pool, both values are 0. Host-only: nothing is enqueued.
+ * Returns GEMM_ERR_DEVICE when no device is current, GEMM_ERR_LAUNCH when the
+ * pool cannot be queried, else GEMM_OK. Source: none on the pages; a
+ * diagnostic of this library's memory use (it lets a test show that
+ * gemm_s8_noalloc takes nothing from the pool).
+ */
+GEMM_API gemm_status_t gemm_pool_usage(int64_t *used_high_bytes, int64_t *reserved_bytes,
+                                       int reset_high);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 GEMM_API int gemm_version(void);

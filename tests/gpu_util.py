@@ -65,9 +65,29 @@ def rel_frobenius(got: np.ndarray, ref: np.ndarray) -> float:
     return float(num / denom)
 
 
-def sample_rows(M: int, count: int, seed: int) -> list[int]:
-    """Rows that cover the first and last tiles, tile boundaries and random rows."""
-    fixed = [0, 1, 31, 32, 63, 64, 127, 128, 129, 255, 256, M // 2, M - 129, M - 128, M - 2, M - 1]
-    rng = np.random.default_rng(seed)
-    rand = rng.integers(0, M, size=max(0, count - len(fixed))).tolist()
-    return sorted({r for r in fixed + rand if 0 <= r < M})
+def fp32_accumulation_bound(oracle_mod, A: torch.Tensor, B: torch.Tensor, alpha: float,
+                            beta: float, C0) -> np.ndarray:
+    """Elementwise worst-case error of a GEMM whose products are exact in fp32
+    and whose sums are accumulated in fp32: (K + 2) * 2^-24 * (|alpha| (|A||B|)_ij
+    + |beta| |C0_ij|) -- K additions and the alpha / beta epilogue, each with a
+    relative error of at most one unit roundoff 2^-24. |A||B| comes from the
+    oracle on the absolute values (exact in every input format)."""
+    K = A.shape[1]
+    absprod = oracle_mod.gemm(A.abs(), B.abs(), 1.0, 0.0)
+    bound = abs(float(alpha)) * absprod
+    if beta != 0 and C0 is not None:
+        c0 = C0.detach().cpu().to(torch.float64).numpy() if isinstance(C0, torch.Tensor) \
+            else np.asarray(C0, dtype=np.float64)
+        bound += abs(float(beta)) * np.abs(c0)
+    return (K + 2) * 2.0 ** -24 * bound
+
+
+def assert_within(got, ref, bound, what=""):
+    """|got - ref| <= bound everywhere; names the worst element otherwise."""
+    got = np.asarray(got, dtype=np.float64)
+    err = np.abs(got - np.asarray(ref, dtype=np.float64))
+    bad = err > bound
+    if bad.any():
+        i, j = np.unravel_index(np.argmax(np.where(bad, err - bound, -np.inf)), err.shape)
+        raise AssertionError(f"{what}{int(bad.sum())} elements beyond the accumulation bound; "
+                             f"worst at ({i}, {j}): |err| {err[i, j]:.3e} > {bound[i, j]:.3e}")

@@ -25,7 +25,7 @@ import pytest
 import torch
 
 from dense_gemm_row_gb300 import workloads as w
-from tests.gpu_util import Banded, dev_copy, rel_frobenius, sample_rows
+from tests.gpu_util import Banded, dev_copy, rel_frobenius
 
 pytestmark = pytest.mark.gpu
 
@@ -74,14 +74,13 @@ def test_u8_extremes_exact_chunks_and_wrap(gemm_mod, oracle_mod):
         np.testing.assert_array_equal(C.cpu().numpy(), oracle_mod.gemm_u8(A, B))
 
 
-def test_u8_large_sampled_rows(gemm_mod, oracle_mod):
+def test_u8_large(gemm_mod, oracle_mod):
     M = N = K = 2048
     A, B = u8_matrix(M, K, 11), u8_matrix(K, N, 12)
     C = torch.empty(M, N, dtype=torch.int32, device="cuda")
     gemm_mod.gemm(A.cuda(), B.cuda(), C)
     torch.cuda.synchronize()
-    rows = sample_rows(M, 24, 5)
-    np.testing.assert_array_equal(C.cpu().numpy()[rows], oracle_mod.gemm_rows(A, B, rows, 1, 0))
+    np.testing.assert_array_equal(C.cpu().numpy(), oracle_mod.gemm_u8(A, B))
 
 
 # ------------------------------------------------------------------ 16-bit C
@@ -95,7 +94,7 @@ def check_out16(got, A, B, alpha, beta, C0, oracle_mod):
     got = got.contiguous()
     exp16 = oracle_mod.gemm_out16(A, B, alpha, beta, C0 if beta != 0 else None)
     ref = oracle_mod.gemm(A, B, alpha, beta, C0.double() if beta != 0 else None)
-    mag = abs(alpha) * (np.abs(A.double().numpy()) @ np.abs(B.double().numpy()))
+    mag = abs(alpha) * oracle_mod.gemm(A.abs(), B.abs())
     if beta != 0:
         mag = mag + abs(beta) * np.abs(C0.double().numpy())
     g = got.double().numpy()
@@ -166,17 +165,14 @@ def test_out16_beta_zero_and_k_zero(gemm_mod, oracle_mod, dtype):
 
 
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=str)
-def test_out16_large_sampled_rows(gemm_mod, oracle_mod, dtype):
+def test_out16_large(gemm_mod, oracle_mod, dtype):
     M, N, K = 2048, 2048, 4096
     A = w.matrix(M, K, dtype, "normal", 40)
     B = w.matrix(K, N, dtype, "normal", 41)
     C = torch.empty(M, N, dtype=dtype, device="cuda")
     gemm_mod.gemm(A.cuda(), B.cuda(), C, 1.0, 0.0)
     torch.cuda.synchronize()
-    rows = sample_rows(M, 16, 9)
-    idx = torch.tensor(rows)
-    check_out16(C.cpu()[idx], A[idx].contiguous(), B, 1.0, 0.0, torch.zeros(len(rows), N,
-                dtype=dtype), oracle_mod)
+    check_out16(C.cpu(), A, B, 1.0, 0.0, torch.zeros(M, N, dtype=dtype), oracle_mod)
 
 
 # ----------------------------------------------------------------------- tf32
@@ -223,17 +219,15 @@ def test_tf32_integer_inputs_bit_exact(gemm_mod, oracle_mod):
     np.testing.assert_array_equal(C.cpu().double().numpy(), oracle_mod.gemm(A, B, tf32=True))
 
 
-def test_tf32_large_sampled_rows(gemm_mod, oracle_mod):
+def test_tf32_large(gemm_mod, oracle_mod):
     M, N, K = 2048, 2048, 4096
     A = w.matrix(M, K, torch.float32, "normal", 61)
     B = w.matrix(K, N, torch.float32, "normal", 62)
     C = torch.empty(M, N, device="cuda")
     gemm_mod.gemm(A.cuda(), B.cuda(), C, tf32=True)
     torch.cuda.synchronize()
-    rows = sample_rows(M, 16, 10)
-    idx = torch.tensor(rows)
-    ref = oracle_mod.gemm(A[idx].contiguous(), B, tf32=True)
-    assert rel_frobenius(C.cpu().numpy()[rows], ref) <= 1e-5
+    ref = oracle_mod.gemm(A, B, tf32=True)
+    assert rel_frobenius(C.cpu().numpy(), ref) <= 1e-5
 
 
 # ----------------------------------------------------------------------- f64
