@@ -159,6 +159,9 @@ cudaError_t launch_gemm_s8_skinny_raw(const DeviceInfo &dev, int M, int N, int K
                                       const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
                                       int32_t beta, int32_t *C, int64_t ldc,
                                       cudaStream_t stream) {
+  // A read as stored too when its rows are whole 16-byte units: one launch.
+  if (tc_skinny_s8_supported(M, A, lda, B, ldb))
+    return launch_tc_skinny_s8(dev, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
   const int64_t lda16 = (static_cast<int64_t>(K) + 7) / 8 * 8;
   cudaMemPool_t pool = nullptr;
   cudaError_t e = device_pool(dev, &pool);

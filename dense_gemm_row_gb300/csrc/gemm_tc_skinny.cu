@@ -21,23 +21,22 @@
 // deterministic (and exact in the int8 mode, whose split points fall on
 // 1024-k chunks), and no part waits for another.
 //
-// Stream-K form (gemm_tc_skinny_sk_kernel), for 9..64 rows and 16..151 column
-// blocks: the (column block, k-unit) space is cut into one equal contiguous
-// range per SM, so no SM idles when #SMs is not a multiple of the number of
-// blocks. A range is a run of segments (a block and a k-range of it); a block
-// covered by one CTA is written directly, a block shared by several CTAs (only
-// a range's first and last segment can be) gets each share in a workspace
-// slot, and the block's last contributor adds them in CTA order. Measured on
-// GB300 (bf16, N = K = 8192): M = 16 35.3 vs 38.1 us, M = 32 36.1 vs 45.8 us,
-// 32 x 4096 x 4096 21.4 vs 26.5 us against the per-block split, which stays
-// faster for <= 8 rows (HBM-bound: 128 CTAs already saturate it) and for few
-// column blocks (many contributors per block). 33..64 rows take this kernel
-// only in the stream-K form (tc_skinny_route).
+// Cluster form (gemm_tc_skinny_cl_kernel), what every call without caller-
+// provided flags takes: the CTAs that split the k range of one column block
+// form a thread-block cluster and add their partial sums through distributed
+// shared memory, so a call is one launch with no workspace, counters or
+// atomics (details at the kernel). Measured on GB300 (bf16, N = K = 8192,
+// 50-call loops): M = 1 26.5 us, M = 16 27.1 us, M = 64 29.2 us, against 29.7,
+// 35.3 and 37.6 us for the per-block split and the stream-K form it replaces.
+// The per-block form remains for callers that supply their own flag memory
+// (whole column blocks, no split) and for int8 B as stored with an A whose rows
+// are not whole 16-byte units.
 //
-// int8 B as stored (the per-block form with kRawB, gemm_s8 with 10..64
-// rows): TMA brings raw byte tiles of B, and four converter warps widen each
-// tile exactly to fp16 in shared memory before the MMA reads it, so B crosses
-// HBM once as bytes instead of being widened to a 16-bit copy first.
+// int8 as stored (gemm_s8 with 10..64 rows): TMA brings raw byte tiles, and
+// converter warps widen each tile exactly to fp16 in shared memory before the
+// MMA reads it, so the operands cross HBM once as bytes instead of being
+// widened to 16-bit copies first. The cluster form reads A and B this way; the
+// per-block form (kRawB) reads B this way and takes a widened A.
 //
 // Sources: as gemm_tc_kernel.cuh (C = alpha*A*B + beta*C, "Sgemm [128,128,8]"; half /
 // bfloat16 x half / bfloat16 -> float and signed char -> int, C++ warp matrix
@@ -46,7 +45,9 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <tuple>
 #include <type_traits>
+#include <map>
 
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -118,8 +119,21 @@ struct __align__(1024) SkSmemI8 {
 // Exact widening of a signed byte x: (x + 128) as the low byte under the fp16
 // pattern 0x64 is 1024 + x + 128; subtracting 1152 leaves x (every value
 // involved is an integer below 2^11, so fp16 holds it exactly).
-__device__ __forceinline__ void convert_stage(uint32_t raw, uint32_t b, int ct) {
+__device__ __forceinline__ void widen_s8x16(const uint32_t (&w)[4], uint32_t (&h)[8]) {
   const __half2 bias = __half2half2(__ushort_as_half(0x6480));  // 1152
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t t = w[q] ^ 0x80808080u;
+    const uint32_t lo = __byte_perm(t, 0x64646464u, 0x4140);
+    const uint32_t hi = __byte_perm(t, 0x64646464u, 0x4342);
+    const __half2 l = __hsub2(*reinterpret_cast<const __half2 *>(&lo), bias);
+    const __half2 u = __hsub2(*reinterpret_cast<const __half2 *>(&hi), bias);
+    h[2 * q] = *reinterpret_cast<const uint32_t *>(&l);
+    h[2 * q + 1] = *reinterpret_cast<const uint32_t *>(&u);
+  }
+}
+
+__device__ __forceinline__ void convert_stage(uint32_t raw, uint32_t b, int ct) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int piece = i * 128 + ct;
@@ -129,16 +143,7 @@ __device__ __forceinline__ void convert_stage(uint32_t raw, uint32_t b, int ct) 
                  : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
                  : "r"(raw + static_cast<uint32_t>(k * 128 + c * 16)));
     uint32_t h[8];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint32_t t = w[q] ^ 0x80808080u;
-      const uint32_t lo = __byte_perm(t, 0x64646464u, 0x4140);
-      const uint32_t hi = __byte_perm(t, 0x64646464u, 0x4342);
-      const __half2 l = __hsub2(*reinterpret_cast<const __half2 *>(&lo), bias);
-      const __half2 u = __hsub2(*reinterpret_cast<const __half2 *>(&hi), bias);
-      h[2 * q] = *reinterpret_cast<const uint32_t *>(&l);
-      h[2 * q + 1] = *reinterpret_cast<const uint32_t *>(&u);
-    }
+    widen_s8x16(w, h);
     const int box = c >> 2;            // 64 columns per box
     const int j0 = (c & 3) * 2;        // first 16-byte chunk of this piece in its row
     const uint32_t row = b + static_cast<uint32_t>(box) * kBBox + static_cast<uint32_t>(k) * 128;
@@ -157,16 +162,11 @@ struct SkArgs {
   int64_t ldc;
   // Per-block split (gemm_tc_skinny_kernel): every CTA one part of one block.
   int split;           // parts of k per column block
-  uint32_t *counters;  // parts done, one per column block (split > 1), zero at launch;
-                       // stream-K: one per CTA, indexed by a shared block's first contributor
-  Out *ws;             // partial sums [split][M][ws_ld] (split > 1); stream-K:
-                       // [CTA][slot 0 (first segment) or 1 (last)][M][128]
+  uint32_t *counters;  // per-block form: parts done, one per column block (split > 1),
+                       // zero at launch
+  Out *ws;             // per-block form: partial sums [split][M][ws_ld] (split > 1)
   int64_t ws_ld;       // column blocks * 128
-  // Stream-K (gemm_tc_skinny_sk_kernel): `units` = column blocks * nunits
-  // k-units over gridDim.x CTAs.
-  int64_t units;
-  int nunits;
-  int small_index;  // (units + nunits + 1) * gridDim.x < 2^32: segment arithmetic in 32 bits
+  int nunits;          // k-units (k-blocks, or 1024-k chunks in the int mode)
   uint32_t idesc;
   uint32_t *err_word;
 };
@@ -510,80 +510,194 @@ __global__ void __launch_bounds__(kRawB ? kI8Threads : kThreads, 1)
   }
 }
 
-// The CTA whose range holds unit x: the largest c with c * U / G <= x. I is
-// the index type: 32 bits when U * G fits (integer division is a software
-// routine; the 64-bit one costs several times more).
-template <typename I>
-__device__ __forceinline__ int unit_owner(I x, I U, I G) {
-  return static_cast<int>(((x + 1) * G - 1) / U);
-}
+// ---------------------------------------------------------------- cluster form
+//
+// Cluster form (gemm_tc_skinny_cl_kernel): the k range of a column block is cut
+// into `cl` equal parts (cl = 1, 2, 4 or 8; in the exact-int mode on 1024-k
+// chunk boundaries), one per CTA of a thread-block cluster. Each CTA runs the
+// pipeline above over its part. Then every CTA puts its 128 x M partial sums in
+// its own shared memory, the cluster meets at a barrier, and CTA r adds the cl
+// partials of columns [r * 128 / cl, (r + 1) * 128 / cl) in CTA order, reading
+// the other CTAs' shared memory directly (distributed shared memory), and
+// writes alpha * sum + beta * C. A second barrier keeps every CTA's partials
+// in place until the others have read them. There is no workspace, counter or
+// atomic in global memory and no second launch: one kernel per call, with a
+// result that does not depend on timing (exact in the int mode).
+//
+// Two CTAs share an SM (shared memory, registers and TMEM are sized for it).
+// Measured on GB300, a CTA that streams from DRAM with TMA is capped at about
+// 200 box rows per microsecond whatever its ring depth (4 to 24 stages give the
+// same rate), while two co-resident CTAs double the SM's rate: the stream, not
+// the ring, sets the pace, so the rings here are short and the CTAs many.
+//
+// kRaw (exact-int mode, int8 A and B as stored): TMA brings byte tiles of A and
+// B into a ring of raw stages, and converter warps write their fp16 forms, in
+// the layouts TMA gives 16-bit operands, into a ring of 16-bit stages that the
+// MMA reads. The converters form kClConvGroups groups of kClGroupWarps warps;
+// group g converts k-blocks g, g + kClConvGroups, ..., so one group's fixed
+// per-stage costs (waits, the proxy fence, arrivals) overlap another group's
+// work. A raw stage is free again once converted, a 16-bit stage once the MMA
+// has read it. Neither operand is widened in global memory.
+constexpr int kClMaxCluster = 8;
+constexpr int kClCtasPerSm = 2;
+constexpr uint32_t kRawABytes = kMaxM * kBK;  // 4 KiB: up to 64 rows of 64 bytes
+constexpr int kClStages = 4;                  // 16-bit form
+constexpr int kClRawStages = 4;
+constexpr int kClWideStages = 2;
+constexpr int kClConvGroups = 2;
+constexpr int kClGroupWarps = 2;
+constexpr int kClConvWarps = kClConvGroups * kClGroupWarps;
+constexpr int kClRawThreads = 64 + 32 * kEpiWarps + 32 * kClConvWarps;
 
-// One segment of a CTA's range: block `blk`, k-blocks [kb0, kb1), and whether
-// another CTA also contributes to the block (then `first` is the block's
-// first contributor, `rank` this CTA's place among them, `count` their number
-// and `slot` this segment's workspace slot).
-struct Segment {
-  int blk, kb0, kb1;
-  bool shared;
-  int first, rank, count, slot;
+template <bool kRaw>
+struct __align__(1024) ClSmem {
+  static constexpr int kNumStages = kRaw ? kClWideStages : kClStages;  // 16-bit stages
+  static constexpr int kNumRaw = kRaw ? kClRawStages : 1;             // byte stages
+  uint8_t b[kNumStages][kBBytes];  // 16-bit B tile: the MMA's A operand
+  uint8_t a[kNumStages][kABytes];  // 16-bit A tile: the MMA's B operand
+  uint8_t rawb[kNumRaw][kRaw ? kRawBytes : 128];
+  uint8_t rawa[kNumRaw][kRaw ? kRawABytes : 128];
+  uint64_t full[kRaw ? kNumRaw : kNumStages];  // TMA: the stage's tiles landed
+  uint64_t raw_free[kNumRaw];                   // kRaw: the converters have read the bytes
+  uint64_t conv[kNumStages];                    // kRaw: the converters wrote b and a
+  uint64_t empty[kNumStages];                   // MMA: the 16-bit stage consumed
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
 };
+// The partial sums of a CTA (M x 128 values of 4 bytes, row m at m * 512 bytes)
+// reuse the first two B stages once the pipeline is done.
+static_assert(2 * kBBytes >= kMaxM * kBN * 4, "partial sums fit in two B stages");
 
-// Segment number `s` of CTA c (false past its range's end). `first_slot` is
-// the workspace slot in which the block's first contributor keeps its share:
-// 0 if the block is that CTA's first segment, else 1 (every later contributor
-// starts inside the block, so its share is in its slot 0).
-template <typename I>
-__device__ __forceinline__ bool get_segment_t(int c, int s, I G, I U, I nunits, int kb_unit,
-                                              int KB, Segment &g, int &first_slot) {
-  const I u0 = static_cast<I>(c) * U / G, u1 = (static_cast<I>(c) + 1) * U / G;
-  I u = u0;
-  for (int i = 0; i < s && u < u1; ++i) {
-    const I blk_end = (u / nunits + 1) * nunits;
-    u = blk_end < u1 ? blk_end : u1;
+// One raw stage into the 16-bit tiles TMA would give, by converter thread ct of
+// a group (kClGroupThreads threads):
+//   * B: 64 rows of k x 128 bytes of n, 128-byte swizzled (16-byte chunk c of
+//     row k at c ^ (k % 8)). A piece is one chunk: 16 values of n = 16 c ...; it
+//     goes to box c / 4 of the 16-bit tile, row k, chunks 2 (c % 4) and the next,
+//     each at chunk ^ (k % 8). Eight consecutive pieces cover chunks 0..3 of an
+//     even row k and 4..7 of row k + 1, or the other halves: in every group of
+//     eight threads the loads and each of the two stores touch eight different
+//     16-byte bank groups.
+//   * A: mp rows x 64 bytes of k, unswizzled; piece q = row q / 4, bytes 16 (q %
+//     4) ...; it goes to row r at r * 128 bytes, chunks 2 (q % 4) and the next
+//     at chunk ^ (r % 8).
+// All the thread's loads are issued before the first conversion, so their
+// latencies overlap.
+constexpr int kClGroupThreads = 32 * kClGroupWarps;
+// pieces per thread and round (a stage takes kClRounds rounds of loads, then stores)
+constexpr int kClRounds = 2;
+constexpr int kClBPieces = kRawBytes / 16 / kClGroupThreads / kClRounds;    // 4
+constexpr int kClAPieces = kMaxM * kBK / 16 / kClGroupThreads / kClRounds;  // 2
+__device__ __forceinline__ void cl_b_piece(int q, int &k, int &c) {
+  const int oct = q >> 3, i = q & 7, v = oct & 1;
+  k = 2 * (oct >> 1) + (i >> 2);
+  c = (i & 3) + 4 * ((i >> 2) ^ v);
+}
+// Piece numbers of round `rd`: B pieces (rd * kClBPieces + i) * kClGroupThreads +
+// ct, A pieces (rd * kClAPieces + i) * kClGroupThreads + ct.
+__device__ __forceinline__ void cl_load_raw(uint32_t rawb, uint32_t rawa, int mp, int ct, int rd,
+                                            uint32_t (&wb)[kClBPieces][4],
+                                            uint32_t (&wa)[kClAPieces][4]) {
+#pragma unroll
+  for (int i = 0; i < kClBPieces; ++i) {
+    int k, c;
+    cl_b_piece((rd * kClBPieces + i) * kClGroupThreads + ct, k, c);
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(wb[i][0]), "=r"(wb[i][1]), "=r"(wb[i][2]), "=r"(wb[i][3])
+                 : "r"(rawb + static_cast<uint32_t>(k * 128 + ((c ^ (k & 7)) << 4))));
   }
-  if (u >= u1) return false;
-  g.blk = static_cast<int>(u / nunits);
-  const I base = static_cast<I>(g.blk) * nunits;
-  const I end = base + nunits < u1 ? base + nunits : u1;
-  g.kb0 = static_cast<int>(u - base) * kb_unit;
-  g.kb1 = min(KB, static_cast<int>(end - base) * kb_unit);
-  g.first = unit_owner<I>(base, U, G);
-  const int last = unit_owner<I>(base + nunits - 1, U, G);
-  g.count = last - g.first + 1;
-  g.shared = g.count > 1;
-  g.rank = c - g.first;
-  g.slot = (u == u0) ? 0 : 1;
-  first_slot = (static_cast<I>(g.first) * U / G == base) ? 0 : 1;
-  return true;
+#pragma unroll
+  for (int i = 0; i < kClAPieces; ++i) {
+    const int q = (rd * kClAPieces + i) * kClGroupThreads + ct;
+    wa[i][0] = wa[i][1] = wa[i][2] = wa[i][3] = 0;
+    if (q < mp * 4)
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
+                   : "=r"(wa[i][0]), "=r"(wa[i][1]), "=r"(wa[i][2]), "=r"(wa[i][3])
+                   : "r"(rawa + static_cast<uint32_t>(q * 16)));
+  }
+}
+__device__ __forceinline__ void cl_store_wide(uint32_t b, uint32_t a, int mp, int ct, int rd,
+                                              const uint32_t (&wb)[kClBPieces][4],
+                                              const uint32_t (&wa)[kClAPieces][4]) {
+#pragma unroll
+  for (int i = 0; i < kClBPieces; ++i) {
+    int k, c;
+    cl_b_piece((rd * kClBPieces + i) * kClGroupThreads + ct, k, c);
+    uint32_t h[8];
+    widen_s8x16(wb[i], h);
+    const uint32_t row = b + static_cast<uint32_t>(c >> 2) * kBBox + static_cast<uint32_t>(k) * 128;
+    const int j0 = (c & 3) * 2;
+    st_shared_v4(row + static_cast<uint32_t>((j0 ^ (k & 7)) << 4), h[0], h[1], h[2], h[3]);
+    st_shared_v4(row + static_cast<uint32_t>(((j0 + 1) ^ (k & 7)) << 4), h[4], h[5], h[6], h[7]);
+  }
+#pragma unroll
+  for (int i = 0; i < kClAPieces; ++i) {
+    const int q = (rd * kClAPieces + i) * kClGroupThreads + ct;
+    if (q < mp * 4) {
+      const int r = q >> 2, c = q & 3;
+      uint32_t h[8];
+      widen_s8x16(wa[i], h);
+      const uint32_t row = a + static_cast<uint32_t>(r) * 128u;
+      st_shared_v4(row + static_cast<uint32_t>(((2 * c) ^ (r & 7)) << 4), h[0], h[1], h[2],
+                   h[3]);
+      st_shared_v4(row + static_cast<uint32_t>(((2 * c + 1) ^ (r & 7)) << 4), h[4], h[5], h[6],
+                   h[7]);
+    }
+  }
+}
+static_assert(kClRounds * kClBPieces * kClGroupThreads * 16 == kRawBytes,
+              "B pieces cover the raw tile");
+static_assert(kClRounds * kClAPieces * kClGroupThreads * 16 == kRawABytes,
+              "A pieces cover the raw tile");
+
+__device__ __forceinline__ void ld_dsmem_v4(uint32_t cluster_addr, uint32_t (&v)[4]) {
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+               : "r"(cluster_addr)
+               : "memory");
 }
 
-__device__ __forceinline__ bool get_segment(int c, int s, int G, int64_t U, int nunits,
-                                            int kb_unit, int KB, bool small, Segment &g,
-                                            int &first_slot) {
-  if (small)
-    return get_segment_t<uint32_t>(c, s, static_cast<uint32_t>(G), static_cast<uint32_t>(U),
-                                   static_cast<uint32_t>(nunits), kb_unit, KB, g, first_slot);
-  return get_segment_t<int64_t>(c, s, G, U, nunits, kb_unit, KB, g, first_slot);
+__device__ __forceinline__ float out_from_bits(uint32_t b, float) { return __uint_as_float(b); }
+__device__ __forceinline__ int32_t out_from_bits(uint32_t b, int32_t) {
+  return static_cast<int32_t>(b);
 }
+__device__ __forceinline__ uint32_t out_to_bits(float v) { return __float_as_uint(v); }
+__device__ __forceinline__ uint32_t out_to_bits(int32_t v) { return static_cast<uint32_t>(v); }
 
-// Stream-K form: the same pipeline over a CTA's run of segments (see the
-// work-split comment at the top of the file).
-template <bool kInt>
-__global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_skinny_sk_kernel(const __grid_constant__ CUtensorMap tmA,
-                          const __grid_constant__ CUtensorMap tmB, const SkArgs<kInt> p) {
+template <bool kInt, bool kRaw>
+__global__ void __launch_bounds__(kRaw ? kClRawThreads : kThreads, kClCtasPerSm)
+    gemm_tc_skinny_cl_kernel(const __grid_constant__ CUtensorMap tmA,
+                             const __grid_constant__ CUtensorMap tmB, const SkArgs<kInt> p) {
+  static_assert(kInt || !kRaw, "int8 operands as stored need the exact-int mode");
   using Out = typename SkArgs<kInt>::Out;
+  using Smem = ClSmem<kRaw>;
+  constexpr int kS = Smem::kNumStages;
   extern __shared__ uint8_t smem_raw[];
-  SkSmem &sm = *reinterpret_cast<SkSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~uintptr_t(1023));
+  Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                       ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   volatile int *abort = &sm.abort;
+  const int cl = p.split;  // CTAs per cluster = parts of k
+  const int rank = cl > 1 ? static_cast<int>(cluster_ctarank()) : 0;
 
+  constexpr int kR = Smem::kNumRaw;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&sm.full[s]), 1);
+    for (int s = 0; s < kS; ++s) {
       mbar_init(smem_u32(&sm.empty[s]), 1);
+      if constexpr (kRaw) {
+        mbar_init(smem_u32(&sm.conv[s]), kClGroupWarps);
+      } else {
+        mbar_init(smem_u32(&sm.full[s]), 1);
+      }
+    }
+    if constexpr (kRaw) {
+      for (int s = 0; s < kR; ++s) {
+        mbar_init(smem_u32(&sm.full[s]), 1);
+        mbar_init(smem_u32(&sm.raw_free[s]), kClGroupWarps);
+      }
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sm.tmem_full[i]), 1);
@@ -604,44 +718,49 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = sm.tmem_base;
 
-  // This CTA's range of the (column block, k-unit) space, as segments.
-  const int c = static_cast<int>(blockIdx.x);
-  const int G = static_cast<int>(gridDim.x);
+  // This CTA's part: column block `blk`, k-blocks [kb0, kb1).
+  const int blk = static_cast<int>(blockIdx.x) / cl;
+  const int n0 = blk * kBN;
   const int KB = (p.K + kBK - 1) / kBK;
   const int kb_unit = kInt ? kChunkKB : 1;
+  const int nunits = (KB + kb_unit - 1) / kb_unit;
+  const int kb0 = min(KB, (rank * nunits / cl) * kb_unit);
+  const int kb1 = min(KB, ((rank + 1) * nunits / cl) * kb_unit);
   const int chunk_kb = kInt ? kChunkKB : KB;
-  const uint32_t a_bytes = static_cast<uint32_t>(p.mp) * kBK * 2;
-  const bool small = p.small_index != 0;
-  Segment g;
-  int first_slot = 0;
+  // bytes per stage of the A tile: mp rows of 64 values
+  const uint32_t a_bytes = static_cast<uint32_t>(p.mp) * kBK * (kRaw ? 1 : 2);
+  bool have_sums = false;  // epilogue threads: this CTA's partial sums are complete
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      // kRaw: the ring of byte stages (freed by the converters); otherwise the
+      // ring of 16-bit stages (freed by the MMA).
+      constexpr int kRing = kRaw ? kR : kS;
       uint32_t stage = 0, phase = 0, issued = 0, issued_parity = 0;
-      bool ok = true;
-      for (int s = 0; ok && get_segment(c, s, G, p.units, p.nunits, kb_unit, KB, small, g, first_slot); ++s) {
-        const int n0 = g.blk * kBN;
-        for (int kb = g.kb0; kb < g.kb1; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&sm.empty[stage]), phase ^ 1u, abort, p.err_word,
-                                 kWaitEmpty)) {
-            ok = false;
-            break;
-          }
-          const uint32_t full_bar = smem_u32(&sm.full[stage]);
+      for (int kb = kb0; kb < kb1; ++kb) {
+        const uint32_t free_bar =
+            kRaw ? smem_u32(&sm.raw_free[stage]) : smem_u32(&sm.empty[stage]);
+        if (!mbar_wait_bounded(free_bar, phase ^ 1u, abort, p.err_word, kWaitEmpty)) break;
+        const uint32_t full_bar = smem_u32(&sm.full[stage]);
+        if constexpr (kRaw) {
+          mbar_arrive_expect_tx(full_bar, kRawBytes + a_bytes);
+          tma_load_2d(smem_u32(sm.rawb[stage]), &tmB, full_bar, n0, kb * kBK);
+          tma_load_2d(smem_u32(sm.rawa[stage]), &tmA, full_bar, kb * kBK, 0);
+        } else {
           mbar_arrive_expect_tx(full_bar, kBBytes + a_bytes);
           tma_load_2d(smem_u32(sm.b[stage]), &tmB, full_bar, n0, kb * kBK);
           tma_load_2d(smem_u32(sm.b[stage] + kBBox), &tmB, full_bar, n0 + 64, kb * kBK);
           tma_load_2d(smem_u32(sm.a[stage]), &tmA, full_bar, kb * kBK, 0);
-          issued |= 1u << stage;
-          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+        }
+        issued |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == kRing) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
-      for (int s = 0; s < kStages; ++s)
+      for (int s = 0; s < kRing; ++s)
         if (issued & (1u << s))
           drain_wait(smem_u32(&sm.full[s]), (issued_parity >> s) & 1u, p.err_word);
     }
@@ -651,9 +770,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, chunk = 0;
       bool ok = true, any = false;
-      for (int s = 0; ok && get_segment(c, s, G, p.units, p.nunits, kb_unit, KB, small, g, first_slot); ++s)
-      for (int c0 = g.kb0; ok && c0 < g.kb1; c0 += chunk_kb) {
-        const int c1 = min(g.kb1, c0 + chunk_kb);
+      for (int c0 = kb0; ok && c0 < kb1; c0 += chunk_kb) {
+        const int c1 = min(kb1, c0 + chunk_kb);
         const uint32_t buf = chunk & 1u, use = (chunk >> 1) & 1u;
         ++chunk;
         if (!mbar_wait_bounded(smem_u32(&sm.tmem_empty[buf]), use ^ 1u, abort, p.err_word,
@@ -662,8 +780,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + buf * kBufCols;
         for (int kb = c0; kb < c1; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&sm.full[stage]), phase, abort, p.err_word,
-                                 kWaitFull)) {
+          const uint32_t ready = kRaw ? smem_u32(&sm.conv[stage]) : smem_u32(&sm.full[stage]);
+          if (!mbar_wait_bounded(ready, phase, abort, p.err_word, kWaitFull)) {
             ok = false;
             break;
           }
@@ -672,16 +790,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a_addr = smem_u32(sm.a[stage]);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            // MMA A operand = B tile, N-major: LBO = one 64-column box, SBO = 1 KiB
-            // between groups of 8 k-rows; 16 k = 16 rows of 128 B further.
+            // descriptors as in the per-block form
             const uint64_t adesc = smem_desc(b_addr + kk * 2048, kBBox, 1024, 2u);
-            // MMA B operand = A tile, K-major: SBO = 8 rows of 128 B; 16 k = 32 B.
             const uint64_t bdesc = smem_desc(a_addr + kk * 32, 16, 1024, 2u);
             tc_mma_f16(d_tmem, adesc, bdesc, p.idesc, (kb > c0 || kk > 0) ? 1u : 0u);
           }
           any = true;
           tc_commit(smem_u32(&sm.empty[stage]));
-          if (++stage == kStages) {
+          if (++stage == kS) {
             stage = 0;
             phase ^= 1u;
           }
@@ -695,26 +811,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp < 2 + kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     // Lanes are columns of C: lane -> column n0 + 32 * quarter + lane.
     const int quarter = warp & 3;
+    const int col = quarter * 32 + lane;
+    const int n = n0 + col;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    // Every epilogue warp walks every segment and meets the same named
-    // barriers whatever its waits return; whether a segment is written is
-    // decided once (seg_skip, read after a barrier) so all warps agree.
-    __shared__ int last, seg_skip;
-    uint32_t chunk = 0;
-    for (int s = 0; get_segment(c, s, G, p.units, p.nunits, kb_unit, KB, small, g, first_slot); ++s) {
-    const int n = g.blk * kBN + quarter * 32 + lane;
     uint32_t acc[kInt ? kMaxM : 1];
     if constexpr (kInt) {
 #pragma unroll
       for (int j = 0; j < kMaxM; ++j) acc[j] = 0;
     }
     float facc[kInt ? 1 : kMaxM];
-    bool done = true;  // every chunk of the segment arrived
-    for (int c0 = g.kb0; c0 < g.kb1; c0 += chunk_kb) {
+    if constexpr (!kInt) {
+#pragma unroll
+      for (int j = 0; j < kMaxM; ++j) facc[j] = 0.f;
+    }
+    bool done = true;
+    uint32_t chunk = 0;
+    for (int c0 = kb0; c0 < kb1; c0 += chunk_kb) {
       const uint32_t buf = chunk & 1u, use = (chunk >> 1) & 1u;
       ++chunk;
       int got = 0;
@@ -755,13 +871,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         return facc[m];
       }
     };
-    if (!done) *abort = 1;  // a wait gave up: the error word says so
-    epilogue_sync();
-    if (warp == 2 && lane == 0) seg_skip = *abort;
-    epilogue_sync();
-    if (seg_skip) continue;  // uniform across the epilogue warps
-    if (!g.shared) {
-      if (n < p.N) {
+    have_sums = done && !*abort;
+    if (cl == 1) {
+      if (n < p.N && have_sums) {
 #pragma unroll
         for (int g = 0; g < kMaxM; g += 16) {
           if (g < p.M) {
@@ -772,51 +884,93 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-    } else {
-      // Store this segment's partial sums in this CTA's slot, count the
-      // contribution; the block's last contributor adds all of them in CTA
-      // order.
-      const int lc = n - g.blk * kBN;  // column within the block
+    } else if (have_sums) {
+      // Every MMA has completed (the last accumulator was committed after
+      // them) and every TMA copy was consumed by one, so the B stages are free.
+      uint32_t *red = reinterpret_cast<uint32_t *>(sm.b[0]);
 #pragma unroll
       for (int m = 0; m < kMaxM; ++m)
-        if (m < p.M) p.ws[((static_cast<int64_t>(c) * 2 + g.slot) * p.M + m) * kBN + lc] = value(m);
-      __threadfence();
-      epilogue_sync();
-      if (warp == 2 && lane == 0)
-        last = (atomicAdd(p.counters + g.first, 1u) == static_cast<uint32_t>(g.count - 1));
-      epilogue_sync();
-      if (last) {
-        __threadfence();
-        if (n < p.N) {
-          // Contributors in CTA order (each element's sum in one fixed order);
-          // within a contributor all rows at once, so the loads overlap.
-          Out sum[kMaxM];
+        if (m < p.M) red[m * kBN + col] = out_to_bits(value(m));
+    }
+  } else {
+    if constexpr (kRaw) {
+      // --------------------------------------------------------- converter
+      // Group g, per k-block kb = kb0 + g, kb0 + g + kClConvGroups, ...: wait
+      // for its bytes (raw stage r) and for its 16-bit stage w to be free; load
+      // this thread's pieces, release r, write w's fp16 tiles, make them
+      // visible to the tensor core (async proxy), arrive on conv[w].
+      const int cw = warp - (2 + kEpiWarps);
+      const int grp = cw / kClGroupWarps;
+      const int ct = (cw % kClGroupWarps) * 32 + lane;
+      for (int kb = kb0 + grp; kb < kb1; kb += kClConvGroups) {
+        const int i = kb - kb0;
+        const int r = i % kR, w = i % kS;
+        const uint32_t rphase = static_cast<uint32_t>(i / kR) & 1u;
+        const uint32_t wphase = static_cast<uint32_t>(i / kS) & 1u;
+        int ok = 1;
+        if (!mbar_wait_bounded(smem_u32(&sm.full[r]), rphase, abort, p.err_word, kWaitFull) ||
+            !mbar_wait_bounded(smem_u32(&sm.empty[w]), wphase ^ 1u, abort, p.err_word,
+                               kWaitEmpty))
+          ok = 0;
+        if (!__all_sync(0xffffffffu, ok)) break;
+        uint32_t wb[kClBPieces][4], wa[kClAPieces][4];
 #pragma unroll
-          for (int m = 0; m < kMaxM; ++m) sum[m] = Out(0);
-          for (int q = 0; q < g.count; ++q) {
-            // contributor first + q holds its share in slot 0, except the
-            // first contributor when the block is not its first segment
-            const int cq = g.first + q;
-            const int slot = q == 0 ? first_slot : 0;
-            const Out *src = p.ws + (static_cast<int64_t>(cq) * 2 + slot) * p.M * kBN + lc;
-#pragma unroll
-            for (int m = 0; m < kMaxM; ++m)
-              if (m < p.M) sum[m] = add_parts(sum[m], __ldcg(src + static_cast<int64_t>(m) * kBN));
+        for (int rd = 0; rd < kClRounds; ++rd) {
+          cl_load_raw(smem_u32(sm.rawb[r]), smem_u32(sm.rawa[r]), p.mp, ct, rd, wb, wa);
+          if (rd == kClRounds - 1) {  // every byte of the raw stage is in registers
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sm.raw_free[r]));
           }
-#pragma unroll
-          for (int g = 0; g < kMaxM; g += 16) {
-            if (g < p.M) {
-              Out w[16];
-#pragma unroll
-              for (int j = 0; j < 16; ++j) w[j] = sum[g + j];
-              write_rows16<kInt>(p, n, g, w);
-            }
-          }
+          cl_store_wide(smem_u32(sm.b[w]), smem_u32(sm.a[w]), p.mp, ct, rd, wb, wa);
         }
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm.conv[w]));
       }
-      epilogue_sync();  // `last` is read before the next segment writes it
     }
+  }
+
+  __syncwarp();
+  if (cl > 1) {
+    // ---------------------------------------------------- cluster reduction
+    cluster_sync();  // every CTA's partial sums are in its shared memory
+    if (warp >= 2 && warp < 2 + kEpiWarps) {
+      // All CTAs must have their sums; a CTA whose waits gave up has recorded
+      // the error and flags the cluster through its own abort word.
+      int bad = 0;
+      const uint32_t abort_local = smem_u32(&sm.abort);
+      for (int q = 0; q < cl; ++q) {
+        uint32_t v;
+        asm volatile("ld.shared::cluster.u32 %0, [%1];\n"
+                     : "=r"(v)
+                     : "r"(mapa_shared(abort_local, static_cast<uint32_t>(q)))
+                     : "memory");
+        bad |= static_cast<int>(v);
+      }
+      const int W = kBN / cl;              // columns this CTA finishes
+      const int wq = W / 4;                // 4-column groups per row
+      const int t = static_cast<int>(threadIdx.x) - 64;
+      const uint32_t red_local = smem_u32(sm.b[0]);
+      const bool use_c = p.beta != Out(0);
+      for (int idx = t; !bad && idx < p.M * wq; idx += 32 * kEpiWarps) {
+        const int m = idx / wq;
+        const int c = rank * W + (idx - m * wq) * 4;
+        const uint32_t off = static_cast<uint32_t>((m * kBN + c) * 4);
+        Out s[4] = {Out(0), Out(0), Out(0), Out(0)};
+        for (int q = 0; q < cl; ++q) {  // CTA order: one fixed order per element
+          uint32_t v[4];
+          ld_dsmem_v4(mapa_shared(red_local + off, static_cast<uint32_t>(q)), v);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) s[j] = add_parts(s[j], out_from_bits(v[j], Out(0)));
+        }
+        Out *crow = p.C + static_cast<int64_t>(m) * p.ldc + n0 + c;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (n0 + c + j < p.N)
+            crow[j] = axpby(p.alpha, s[j], p.beta, use_c ? crow[j] : Out(0), use_c);
+      }
     }
+    cluster_sync();  // no CTA leaves while another may still read its sums
   }
 
   tc_fence_before_sync();
@@ -825,6 +979,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, kTmemCols);
   }
+  (void)have_sums;
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -861,41 +1016,74 @@ bool tmap16(CUtensorMap *tm, CUtensorMapDataType dt, const void *base, int64_t r
          CUDA_SUCCESS;
 }
 
-// Stream-K launch: one CTA per SM over equal shares of the (column block,
-// k-unit) space; two partial-sum slots and one counter per CTA.
-template <bool kInt>
-cudaError_t launch_stream_k(const DeviceInfo &dev, SkArgs<kInt> p, const CUtensorMap &tmA,
-                            const CUtensorMap &tmB, int blocks, int nunits, cudaStream_t stream) {
-  using Out = typename SkArgs<kInt>::Out;
-  const int64_t units = static_cast<int64_t>(blocks) * nunits;
-  const int G = units < dev.sm_count ? static_cast<int>(units) : dev.sm_count;
-  p.units = units;
-  p.nunits = nunits;
-  p.small_index = (units + nunits + 1) * static_cast<int64_t>(G) < (int64_t(1) << 32);
-  p.split = 1;
+// Whether clusters of cl CTAs of this kernel can be resident on the device
+// (queried once per kernel, device and cluster size).
+bool clusters_fit(const DeviceInfo &dev, const void *kern, size_t smem, int threads, int cl) {
+  static std::mutex mu;
+  static std::map<std::tuple<const void *, int, int>, bool> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_tuple(kern, dev.device, cl);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(cl), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cl);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  cudaGetLastError();
+  cache[key] = n >= 1;
+  return n >= 1;
+}
+
+// Cluster-form launch: cl = the largest of 1, 2, 4, 8 with blocks * cl CTAs
+// at most kClCtasPerSm per SM, at least one k-unit per part, and clusters of
+// that size schedulable.
+template <bool kInt, bool kRaw>
+cudaError_t launch_cluster(const DeviceInfo &dev, SkArgs<kInt> p, const CUtensorMap &tmA,
+                           const CUtensorMap &tmB, int blocks, int nunits, cudaStream_t stream) {
+  // kClCtasPerSm CTAs per SM: 228 KiB of shared memory, 1 KiB of it reserved per CTA
+  static_assert(kClCtasPerSm * (sizeof(ClSmem<kRaw>) + 1024 + 1024) <= 228 * 1024,
+                "cluster-form shared memory");
+  auto kern = gemm_tc_skinny_cl_kernel<kInt, kRaw>;
+  const void *kp = reinterpret_cast<const void *>(kern);
+  const size_t smem = sizeof(ClSmem<kRaw>) + 1024;
+  const int threads = kRaw ? kClRawThreads : kThreads;
+  cudaError_t e = set_max_dynamic_smem(kp, static_cast<int>(smem), dev.device);
+  if (e != cudaSuccess) return e;
+  int cl = 1;
+  while (cl < kClMaxCluster &&
+         static_cast<int64_t>(blocks) * cl * 2 <= static_cast<int64_t>(kClCtasPerSm) * dev.sm_count &&
+         cl * 2 <= nunits)
+    cl *= 2;
+  while (cl > 1 && !clusters_fit(dev, kp, smem, threads, cl)) cl /= 2;
+  p.split = cl;
+  p.counters = nullptr;
+  p.ws = nullptr;
   p.ws_ld = 0;
-  cudaMemPool_t pool;
-  cudaError_t e = device_pool(dev, &pool);
-  if (e != cudaSuccess) return e;
-  const size_t ws_bytes = static_cast<size_t>(G) * 2 * p.M * kBN * sizeof(Out);
-  const size_t cnt_off = (ws_bytes + 255) / 256 * 256;
-  void *pool_ws = nullptr;
-  e = cudaMallocFromPoolAsync(&pool_ws, cnt_off + static_cast<size_t>(G) * 4, pool, stream);
-  if (e != cudaSuccess) return e;
-  p.ws = static_cast<Out *>(pool_ws);
-  p.counters = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(pool_ws) + cnt_off);
-  e = cudaMemsetAsync(p.counters, 0, static_cast<size_t>(G) * 4, stream);
-  const size_t smem = sizeof(SkSmem) + 1024;
-  auto kern = gemm_tc_skinny_sk_kernel<kInt>;
-  if (e == cudaSuccess)
-    e = set_max_dynamic_smem(reinterpret_cast<const void *>(kern), static_cast<int>(smem),
-                             dev.device);
-  if (e == cudaSuccess) {
-    kern<<<static_cast<unsigned>(G), kThreads, smem, stream>>>(tmA, tmB, p);
-    e = cudaGetLastError();
-  }
-  cudaError_t f = cudaFreeAsync(pool_ws, stream);
-  return e != cudaSuccess ? e : f;
+  p.nunits = nunits;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks * cl), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cl);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = cl > 1 ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return e;
 }
 
 // One slice per CTA: column blocks times parts of k, at most one CTA per SM
@@ -982,27 +1170,30 @@ cudaError_t launch(const DeviceInfo &dev, CUtensorMapDataType dt, bool is_bf16, 
   const int blocks = (N + kBN - 1) / kBN;
   const int KB = (K + kBK - 1) / kBK;
   const int nunits = kInt ? (KB + kChunkKB - 1) / kChunkKB : KB;
-  if (M > 8 && blocks >= 16 && blocks < dev.sm_count && flags_ws == nullptr &&
-      static_cast<int64_t>(blocks) * nunits > dev.sm_count)
-    return launch_stream_k<kInt>(dev, p, tmA, tmB, blocks, nunits, stream);
+  if (flags_ws == nullptr)
+    return launch_cluster<kInt, false>(dev, p, tmA, tmB, blocks, nunits, stream);
   (void)flags_words;
   return launch_per_block<kInt, false>(dev, p, tmA, tmB, blocks, nunits, stream, flags_ws);
 }
 
-// Row-major rows x cols int8 matrix as bytes, boxes of 64 rows x 128 columns,
-// no swizzle (the raw tile the converter warps read).
-bool tmap8(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols, int64_t ld) {
+// Row-major rows x cols int8 matrix as bytes, boxes of box_rows rows x
+// box_cols columns (by default 64 x 128), unswizzled or with the 128-byte
+// swizzle (box_cols = 128): the raw tiles the converter warps read.
+bool tmap8(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols, int64_t ld,
+           uint32_t box_rows = kBK, uint32_t box_cols = kBN, bool swizzle128 = false) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBN), static_cast<cuuint32_t>(kBK)};
+  cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
          CUDA_SUCCESS;
 }
+
 
 }  // namespace
 
@@ -1057,6 +1248,35 @@ cudaError_t launch_tc_skinny_int(const DeviceInfo &dev, int M, int N, int K, int
                                  uint32_t *flags, size_t flags_words) {
   return launch<true>(dev, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, false, M, N, K, alpha, A16, lda, B16,
                       ldb, beta, C, ldc, stream, flags, flags_words);
+}
+
+bool tc_skinny_s8_supported(int M, const void *A, int64_t lda, const void *B, int64_t ldb) {
+  return M >= 1 && M <= kMaxM && reinterpret_cast<uintptr_t>(A) % 16 == 0 && lda % 16 == 0 &&
+         reinterpret_cast<uintptr_t>(B) % 16 == 0 && ldb % 16 == 0;
+}
+
+cudaError_t launch_tc_skinny_s8(const DeviceInfo &dev, int M, int N, int K, int32_t alpha,
+                                const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
+                                int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream) {
+  if (!tc_skinny_s8_supported(M, A, lda, B, ldb)) return cudaErrorInvalidValue;
+  SkArgs<true> p;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.mp = (M + 15) / 16 * 16;
+  p.alpha = alpha;
+  p.beta = beta;
+  p.C = C;
+  p.ldc = ldc;
+  p.idesc = idesc_f16(false, /*a_mn_major=*/true, /*b_mn_major=*/false, kBN, p.mp);
+  p.err_word = dev.err_word;
+  CUtensorMap tmA, tmB;
+  if (!tmap8(&tmA, A, M, K, lda, static_cast<uint32_t>(p.mp), kBK)) return cudaErrorInvalidValue;
+  if (!tmap8(&tmB, B, K, N, ldb, kBK, kBN, /*swizzle128=*/true)) return cudaErrorInvalidValue;
+  const int blocks = (N + kBN - 1) / kBN;
+  const int KB = (K + kBK - 1) / kBK;
+  const int nunits = (KB + kChunkKB - 1) / kChunkKB;
+  return launch_cluster<true, true>(dev, p, tmA, tmB, blocks, nunits, stream);
 }
 
 }  // namespace dgr

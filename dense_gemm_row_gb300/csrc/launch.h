@@ -105,10 +105,10 @@ cudaError_t launch_gemm_s8_scratch(const DeviceInfo &dev, int M, int N, int K, i
 // limit of the small-M SIMT kernel (gemm_small_m.cu).
 constexpr int kSkinnyMaxM = 32;
 // Whether the 16-bit / int8 tensor-core paths take the transposed-role kernel
-// for an M x N problem: up to 32 rows always; 33..64 rows when its stream-K
-// form applies (16..sm_count-1 column blocks of 128). Measured on GB300 at
-// 33..64 rows against the 256-row pair tiles: bf16 N = K = 8192 36.4-38.6 vs
-// 38.5-39.1 us, 64 x 4096 x 4096 23.4 vs 31.3 us; int8 77 vs 97 us.
+// for an M x N problem: up to 32 rows always; 33..64 rows when its k range is
+// split across a cluster (16..sm_count-1 column blocks of 128). Measured on
+// GB300 at 64 rows against the 256-row pair tiles: bf16 N = K = 8192 29.2 vs
+// 38.5 us, 64 x 4096 x 4096 12.6 vs 31.3 us.
 bool tc_skinny_route(int M, int N, int sm_count);
 cudaError_t launch_tc_skinny_float(const DeviceInfo &dev, bool is_bf16, int M, int N, int K,
                                    float alpha, const void *A, int64_t lda, const void *B,
@@ -131,6 +131,13 @@ cudaError_t launch_gemm_s8_skinny_raw(const DeviceInfo &dev, int M, int N, int K
 #define DGR_I8RAW_MIN_M 10
 #endif
 constexpr int kI8RawMinM = DGR_I8RAW_MIN_M;
+// int8 A and B read as stored by the cluster form of the transposed-role
+// kernel (gemm_tc_skinny.cu; up to 64 rows): both operands 16-byte aligned
+// with row strides in whole 16-byte units (tc_skinny_s8_supported).
+bool tc_skinny_s8_supported(int M, const void *A, int64_t lda, const void *B, int64_t ldb);
+cudaError_t launch_tc_skinny_s8(const DeviceInfo &dev, int M, int N, int K, int32_t alpha,
+                                const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
+                                int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream);
 cudaError_t launch_tc_skinny_i8(const DeviceInfo &dev, int M, int N, int K, int32_t alpha,
                                 const void *A16, int64_t lda, const int8_t *B, int64_t ldb,
                                 int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream);

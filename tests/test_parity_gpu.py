@@ -331,12 +331,12 @@ def test_skinny_shapes(gemm_mod, oracle_mod, dtype, M):
 @pytest.mark.parametrize("shape", [(9, 2048, 4096), (24, 4160, 8200), (32, 8192, 2048),
                                    (16, 19200, 1024), (40, 3000, 3000), (64, 4096, 4096)],
                          ids=lambda s: "x".join(map(str, s)))
-def test_skinny_stream_k(gemm_mod, oracle_mod, dtype, shape):
-    """9..64 rows and 16..151 column blocks of 128: the stream-K form of the
-    transposed-role kernel (equal shares of the (block, k) space per SM; blocks
-    shared by several CTAs are summed by their last contributor in CTA order).
-    int8 with K not a multiple of 16 takes the same kernel on widened operands
-    (1024-k units). Every output checked (M is small)."""
+def test_skinny_cluster_split(gemm_mod, oracle_mod, dtype, shape):
+    """9..64 rows and 16..151 column blocks of 128: the cluster form of the
+    transposed-role kernel (the CTAs that split one column block's k range form
+    a cluster and add their partial sums in CTA order through distributed
+    shared memory). int8 with K not a multiple of 16 takes the same kernel on
+    widened operands (1024-k units). Every output checked (M is small)."""
     M, N, K = shape
     if dtype == torch.int8:
         K = K + 3  # rows not 16-byte multiples: not the small-M kernel
