@@ -26,7 +26,7 @@
 // form a thread-block cluster and add their partial sums through distributed
 // shared memory, so a call is one launch with no workspace, counters or
 // atomics (details at the kernel). Measured on GB300 (bf16, N = K = 8192,
-// 50-call loops): M = 1 26.5 us, M = 16 27.1 us, M = 64 29.2 us, against 29.7,
+// 50-call loops): M = 1 23.8 us, M = 16 24.7 us, M = 64 26.7 us, against 29.7,
 // 35.3 and 37.6 us for the per-block split and the stream-K form it replaces.
 // The per-block form remains for callers that supply their own flag memory
 // (whole column blocks, no split) and for int8 B as stored with an A whose rows
@@ -717,6 +717,11 @@ __global__ void __launch_bounds__(kRaw ? kClRawThreads : kThreads, kClCtasPerSm)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = sm.tmem_base;
+  // Launched as a programmatic dependent of the previous kernel on the stream:
+  // the set-up above overlaps that kernel's tail; nothing in global memory is
+  // touched before it has completed and its writes are visible.
+  grid_dependency_wait();
+  grid_launch_dependents();
 
   // This CTA's part: column block `blk`, k-blocks [kb0, kb1).
   const int blk = static_cast<int>(blockIdx.x) / cl;
@@ -1074,13 +1079,17 @@ cudaError_t launch_cluster(const DeviceInfo &dev, SkArgs<kInt> p, const CUtensor
   cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(cl);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  // Programmatic dependent launch (the kernel waits for its predecessor before
+  // touching global memory), and the cluster shape when k is split.
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(cl);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = cl > 1 ? 1 : 0;
+  cfg.numAttrs = cl > 1 ? 2 : 1;
   e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   return e;

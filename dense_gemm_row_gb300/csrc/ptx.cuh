@@ -126,6 +126,20 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// --------------------------------------------- programmatic dependent launch
+
+// Waits until the grids this one depends on (the previous kernel on the
+// stream, when launched with programmatic stream serialization) have completed
+// and their memory operations are visible; returns at once otherwise.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Allows the next kernel on the stream, if launched as a programmatic
+// dependent, to be scheduled before this grid has finished.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------- TMA
 
 // 2-D tiled bulk tensor copy global -> shared, completing on `bar`.
