@@ -538,25 +538,37 @@ __global__ void __launch_bounds__(kRawB ? kI8Threads : kThreads, 1)
 // per-stage costs (waits, the proxy fence, arrivals) overlap another group's
 // work. A raw stage is free again once converted, a 16-bit stage once the MMA
 // has read it. Neither operand is widened in global memory.
+//
+// The int8 form is built for a bound kMP on the rows (16, 32 or 64): its A
+// tiles and accumulators are sized for kMP rows, so that more stages fit. Both
+// rings matter: a raw stage is held from its TMA issue through the
+// conversion's loads, a 16-bit stage from its conversion until the MMAs that
+// read it complete (measured: with 2 of them the MMA round trip, not the
+// stream, set the pace at 0.45 us per k-block; without MMAs 0.22 us).
+static_assert(kBK / 16 == 4, "four MMAs of k = 16 per stage");
 constexpr int kClMaxCluster = 8;
 constexpr int kClCtasPerSm = 2;
-constexpr uint32_t kRawABytes = kMaxM * kBK;  // 4 KiB: up to 64 rows of 64 bytes
 constexpr int kClStages = 4;                  // 16-bit form
-constexpr int kClRawStages = 4;
-constexpr int kClWideStages = 2;
+template <int kMP>
+struct ClRaw {
+  static constexpr int kStages = kMP <= 16 ? 4 : 3;  // raw (byte) stages
+  static constexpr int kWide = kMP <= 32 ? 4 : 3;    // 16-bit stages
+  static constexpr uint32_t kABytes = kMP * kBK;          // raw A tile: kMP rows of 64 bytes
+  static constexpr uint32_t kWideABytes = kMP * kBK * 2;  // fp16 A tile
+};
 constexpr int kClConvGroups = 2;
 constexpr int kClGroupWarps = 2;
 constexpr int kClConvWarps = kClConvGroups * kClGroupWarps;
 constexpr int kClRawThreads = 64 + 32 * kEpiWarps + 32 * kClConvWarps;
 
-template <bool kRaw>
+template <bool kRaw, int kMP>
 struct __align__(1024) ClSmem {
-  static constexpr int kNumStages = kRaw ? kClWideStages : kClStages;  // 16-bit stages
-  static constexpr int kNumRaw = kRaw ? kClRawStages : 1;             // byte stages
+  static constexpr int kNumStages = kRaw ? ClRaw<kMP>::kWide : kClStages;  // 16-bit stages
+  static constexpr int kNumRaw = kRaw ? ClRaw<kMP>::kStages : 1;      // byte stages
   uint8_t b[kNumStages][kBBytes];  // 16-bit B tile: the MMA's A operand
-  uint8_t a[kNumStages][kABytes];  // 16-bit A tile: the MMA's B operand
+  uint8_t a[kNumStages][kRaw ? ClRaw<kMP>::kWideABytes : kABytes];  // 16-bit A tile: B operand
   uint8_t rawb[kNumRaw][kRaw ? kRawBytes : 128];
-  uint8_t rawa[kNumRaw][kRaw ? kRawABytes : 128];
+  uint8_t rawa[kNumRaw][kRaw ? ClRaw<kMP>::kABytes : 128];
   uint64_t full[kRaw ? kNumRaw : kNumStages];  // TMA: the stage's tiles landed
   uint64_t raw_free[kNumRaw];                   // kRaw: the converters have read the bytes
   uint64_t conv[kNumStages];                    // kRaw: the converters wrote b and a
@@ -589,7 +601,11 @@ constexpr int kClGroupThreads = 32 * kClGroupWarps;
 // pieces per thread and round (a stage takes kClRounds rounds of loads, then stores)
 constexpr int kClRounds = 2;
 constexpr int kClBPieces = kRawBytes / 16 / kClGroupThreads / kClRounds;    // 4
-constexpr int kClAPieces = kMaxM * kBK / 16 / kClGroupThreads / kClRounds;  // 2
+// A pieces per thread and round for kMP rows (kMP * 4 pieces of 16 bytes)
+template <int kMP>
+constexpr int cl_a_pieces() {
+  return (kMP * 4 + kClGroupThreads * kClRounds - 1) / (kClGroupThreads * kClRounds);
+}
 __device__ __forceinline__ void cl_b_piece(int q, int &k, int &c) {
   const int oct = q >> 3, i = q & 7, v = oct & 1;
   k = 2 * (oct >> 1) + (i >> 2);
@@ -597,9 +613,10 @@ __device__ __forceinline__ void cl_b_piece(int q, int &k, int &c) {
 }
 // Piece numbers of round `rd`: B pieces (rd * kClBPieces + i) * kClGroupThreads +
 // ct, A pieces (rd * kClAPieces + i) * kClGroupThreads + ct.
+template <int kAP>
 __device__ __forceinline__ void cl_load_raw(uint32_t rawb, uint32_t rawa, int mp, int ct, int rd,
                                             uint32_t (&wb)[kClBPieces][4],
-                                            uint32_t (&wa)[kClAPieces][4]) {
+                                            uint32_t (&wa)[kAP][4]) {
 #pragma unroll
   for (int i = 0; i < kClBPieces; ++i) {
     int k, c;
@@ -609,8 +626,8 @@ __device__ __forceinline__ void cl_load_raw(uint32_t rawb, uint32_t rawa, int mp
                  : "r"(rawb + static_cast<uint32_t>(k * 128 + ((c ^ (k & 7)) << 4))));
   }
 #pragma unroll
-  for (int i = 0; i < kClAPieces; ++i) {
-    const int q = (rd * kClAPieces + i) * kClGroupThreads + ct;
+  for (int i = 0; i < kAP; ++i) {
+    const int q = (rd * kAP + i) * kClGroupThreads + ct;
     wa[i][0] = wa[i][1] = wa[i][2] = wa[i][3] = 0;
     if (q < mp * 4)
       asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
@@ -618,9 +635,10 @@ __device__ __forceinline__ void cl_load_raw(uint32_t rawb, uint32_t rawa, int mp
                    : "r"(rawa + static_cast<uint32_t>(q * 16)));
   }
 }
+template <int kAP>
 __device__ __forceinline__ void cl_store_wide(uint32_t b, uint32_t a, int mp, int ct, int rd,
                                               const uint32_t (&wb)[kClBPieces][4],
-                                              const uint32_t (&wa)[kClAPieces][4]) {
+                                              const uint32_t (&wa)[kAP][4]) {
 #pragma unroll
   for (int i = 0; i < kClBPieces; ++i) {
     int k, c;
@@ -633,8 +651,8 @@ __device__ __forceinline__ void cl_store_wide(uint32_t b, uint32_t a, int mp, in
     st_shared_v4(row + static_cast<uint32_t>(((j0 + 1) ^ (k & 7)) << 4), h[4], h[5], h[6], h[7]);
   }
 #pragma unroll
-  for (int i = 0; i < kClAPieces; ++i) {
-    const int q = (rd * kClAPieces + i) * kClGroupThreads + ct;
+  for (int i = 0; i < kAP; ++i) {
+    const int q = (rd * kAP + i) * kClGroupThreads + ct;
     if (q < mp * 4) {
       const int r = q >> 2, c = q & 3;
       uint32_t h[8];
@@ -649,7 +667,8 @@ __device__ __forceinline__ void cl_store_wide(uint32_t b, uint32_t a, int mp, in
 }
 static_assert(kClRounds * kClBPieces * kClGroupThreads * 16 == kRawBytes,
               "B pieces cover the raw tile");
-static_assert(kClRounds * kClAPieces * kClGroupThreads * 16 == kRawABytes,
+static_assert(kClRounds * cl_a_pieces<64>() * kClGroupThreads >= 64 * 4 &&
+                  kClRounds * cl_a_pieces<16>() * kClGroupThreads >= 16 * 4,
               "A pieces cover the raw tile");
 
 __device__ __forceinline__ void ld_dsmem_v4(uint32_t cluster_addr, uint32_t (&v)[4]) {
@@ -666,13 +685,14 @@ __device__ __forceinline__ int32_t out_from_bits(uint32_t b, int32_t) {
 __device__ __forceinline__ uint32_t out_to_bits(float v) { return __float_as_uint(v); }
 __device__ __forceinline__ uint32_t out_to_bits(int32_t v) { return static_cast<uint32_t>(v); }
 
-template <bool kInt, bool kRaw>
+template <bool kInt, bool kRaw, int kMP = kMaxM>
 __global__ void __launch_bounds__(kRaw ? kClRawThreads : kThreads, kClCtasPerSm)
     gemm_tc_skinny_cl_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB, const SkArgs<kInt> p) {
   static_assert(kInt || !kRaw, "int8 operands as stored need the exact-int mode");
   using Out = typename SkArgs<kInt>::Out;
-  using Smem = ClSmem<kRaw>;
+  using Smem = ClSmem<kRaw, kMP>;
+  constexpr int kAccM = kMP;  // rows held per epilogue thread
   constexpr int kS = Smem::kNumStages;
   extern __shared__ uint8_t smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -775,6 +795,14 @@ __global__ void __launch_bounds__(kRaw ? kClRawThreads : kThreads, kClCtasPerSm)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, chunk = 0;
       bool ok = true, any = false;
+      // Descriptors of stage 0 (as in the per-block form); a stage or a k-step
+      // of 16 only moves the start address, the descriptor's low 14 bits
+      // (address / 16), so each MMA's descriptors are one add away. A single
+      // thread's MMA issue rate is what paces the small-N MMAs here.
+      const uint64_t adesc0 = smem_desc(smem_u32(sm.b[0]), kBBox, 1024, 2u);
+      const uint64_t bdesc0 = smem_desc(smem_u32(sm.a[0]), 16, 1024, 2u);
+      constexpr uint32_t kAStep = sizeof(sm.b[0]) >> 4, kBStep = sizeof(sm.a[0]) >> 4;
+      uint32_t a_off = 0, b_off = 0;  // stage offsets in descriptor units
       for (int c0 = kb0; ok && c0 < kb1; c0 += chunk_kb) {
         const int c1 = min(kb1, c0 + chunk_kb);
         const uint32_t buf = chunk & 1u, use = (chunk >> 1) & 1u;
@@ -791,20 +819,22 @@ __global__ void __launch_bounds__(kRaw ? kClRawThreads : kThreads, kClCtasPerSm)
             break;
           }
           tc_fence_after_sync();
-          const uint32_t b_addr = smem_u32(sm.b[stage]);
-          const uint32_t a_addr = smem_u32(sm.a[stage]);
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            // descriptors as in the per-block form
-            const uint64_t adesc = smem_desc(b_addr + kk * 2048, kBBox, 1024, 2u);
-            const uint64_t bdesc = smem_desc(a_addr + kk * 32, 16, 1024, 2u);
-            tc_mma_f16(d_tmem, adesc, bdesc, p.idesc, (kb > c0 || kk > 0) ? 1u : 0u);
-          }
+          const uint64_t ad = adesc0 + a_off, bd = bdesc0 + b_off;
+          const uint32_t first = kb == c0 ? 0u : 1u;
+          // k-step 16: 16 rows of 128 bytes further in the B tile (N-major),
+          // 32 bytes further along the A tile's rows (K-major)
+          tc_mma_f16(d_tmem, ad, bd, p.idesc, first);
+          tc_mma_f16(d_tmem, ad + 128, bd + 2, p.idesc, 1u);
+          tc_mma_f16(d_tmem, ad + 256, bd + 4, p.idesc, 1u);
+          tc_mma_f16(d_tmem, ad + 384, bd + 6, p.idesc, 1u);
           any = true;
           tc_commit(smem_u32(&sm.empty[stage]));
+          a_off += kAStep;
+          b_off += kBStep;
           if (++stage == kS) {
             stage = 0;
             phase ^= 1u;
+            a_off = b_off = 0;
           }
         }
         if (!ok) break;
@@ -823,15 +853,15 @@ __global__ void __launch_bounds__(kRaw ? kClRawThreads : kThreads, kClCtasPerSm)
     const int col = quarter * 32 + lane;
     const int n = n0 + col;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    uint32_t acc[kInt ? kMaxM : 1];
+    uint32_t acc[kInt ? kAccM : 1];
     if constexpr (kInt) {
 #pragma unroll
-      for (int j = 0; j < kMaxM; ++j) acc[j] = 0;
+      for (int j = 0; j < kAccM; ++j) acc[j] = 0;
     }
-    float facc[kInt ? 1 : kMaxM];
+    float facc[kInt ? 1 : kAccM];
     if constexpr (!kInt) {
 #pragma unroll
-      for (int j = 0; j < kMaxM; ++j) facc[j] = 0.f;
+      for (int j = 0; j < kAccM; ++j) facc[j] = 0.f;
     }
     bool done = true;
     uint32_t chunk = 0;
@@ -850,7 +880,7 @@ __global__ void __launch_bounds__(kRaw ? kClRawThreads : kThreads, kClCtasPerSm)
       tc_fence_after_sync();
       const uint32_t taddr = tmem_base + lane_base + buf * 64;
 #pragma unroll
-      for (int c = 0; c < kMaxM; c += 16) {
+      for (int c = 0; c < kAccM; c += 16) {
         if (c < p.mp) {
           uint32_t r[16];
           tmem_ld_32x32b_x16(taddr + c, r);
@@ -880,7 +910,7 @@ __global__ void __launch_bounds__(kRaw ? kClRawThreads : kThreads, kClCtasPerSm)
     if (cl == 1) {
       if (n < p.N && have_sums) {
 #pragma unroll
-        for (int g = 0; g < kMaxM; g += 16) {
+        for (int g = 0; g < kAccM; g += 16) {
           if (g < p.M) {
             Out w[16];
 #pragma unroll
@@ -894,7 +924,7 @@ __global__ void __launch_bounds__(kRaw ? kClRawThreads : kThreads, kClCtasPerSm)
       // them) and every TMA copy was consumed by one, so the B stages are free.
       uint32_t *red = reinterpret_cast<uint32_t *>(sm.b[0]);
 #pragma unroll
-      for (int m = 0; m < kMaxM; ++m)
+      for (int m = 0; m < kAccM; ++m)
         if (m < p.M) red[m * kBN + col] = out_to_bits(value(m));
     }
   } else {
@@ -918,7 +948,8 @@ __global__ void __launch_bounds__(kRaw ? kClRawThreads : kThreads, kClCtasPerSm)
                                kWaitEmpty))
           ok = 0;
         if (!__all_sync(0xffffffffu, ok)) break;
-        uint32_t wb[kClBPieces][4], wa[kClAPieces][4];
+        constexpr int kAP = cl_a_pieces<kMP>();
+        uint32_t wb[kClBPieces][4], wa[kAP][4];
 #pragma unroll
         for (int rd = 0; rd < kClRounds; ++rd) {
           cl_load_raw(smem_u32(sm.rawb[r]), smem_u32(sm.rawa[r]), p.mp, ct, rd, wb, wa);
@@ -1051,15 +1082,16 @@ bool clusters_fit(const DeviceInfo &dev, const void *kern, size_t smem, int thre
 // Cluster-form launch: cl = the largest of 1, 2, 4, 8 with blocks * cl CTAs
 // at most kClCtasPerSm per SM, at least one k-unit per part, and clusters of
 // that size schedulable.
-template <bool kInt, bool kRaw>
+template <bool kInt, bool kRaw, int kMP = kMaxM>
 cudaError_t launch_cluster(const DeviceInfo &dev, SkArgs<kInt> p, const CUtensorMap &tmA,
                            const CUtensorMap &tmB, int blocks, int nunits, cudaStream_t stream) {
   // kClCtasPerSm CTAs per SM: 228 KiB of shared memory, 1 KiB of it reserved per CTA
-  static_assert(kClCtasPerSm * (sizeof(ClSmem<kRaw>) + 1024 + 1024) <= 228 * 1024,
+  static_assert(kClCtasPerSm * (sizeof(ClSmem<kRaw, kMP>) + 1024 + 1024) <= 228 * 1024,
                 "cluster-form shared memory");
-  auto kern = gemm_tc_skinny_cl_kernel<kInt, kRaw>;
+  static_assert(2 * kBBytes >= kMP * kBN * 4, "partial sums fit in two B stages");
+  auto kern = gemm_tc_skinny_cl_kernel<kInt, kRaw, kMP>;
   const void *kp = reinterpret_cast<const void *>(kern);
-  const size_t smem = sizeof(ClSmem<kRaw>) + 1024;
+  const size_t smem = sizeof(ClSmem<kRaw, kMP>) + 1024;
   const int threads = kRaw ? kClRawThreads : kThreads;
   cudaError_t e = set_max_dynamic_smem(kp, static_cast<int>(smem), dev.device);
   if (e != cudaSuccess) return e;
@@ -1285,7 +1317,9 @@ cudaError_t launch_tc_skinny_s8(const DeviceInfo &dev, int M, int N, int K, int3
   const int blocks = (N + kBN - 1) / kBN;
   const int KB = (K + kBK - 1) / kBK;
   const int nunits = (KB + kChunkKB - 1) / kChunkKB;
-  return launch_cluster<true, true>(dev, p, tmA, tmB, blocks, nunits, stream);
+  if (p.mp <= 16) return launch_cluster<true, true, 16>(dev, p, tmA, tmB, blocks, nunits, stream);
+  if (p.mp <= 32) return launch_cluster<true, true, 32>(dev, p, tmA, tmB, blocks, nunits, stream);
+  return launch_cluster<true, true, 64>(dev, p, tmA, tmB, blocks, nunits, stream);
 }
 
 }  // namespace dgr

@@ -348,6 +348,48 @@ def test_skinny_cluster_split(gemm_mod, oracle_mod, dtype, shape):
     out.check_canaries()
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=str)
+@pytest.mark.parametrize("shape", [(1, 128, 8192), (16, 2056, 1000), (32, 39000, 256),
+                                   (64, 4096, 64), (5, 640, 4104)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_skinny_cluster_edges(gemm_mod, oracle_mod, dtype, shape):
+    """Cluster form of the transposed-role kernel at its edges: one column
+    block whose k range is split eight ways (1 x 128 x 8192), a ragged N and K
+    (17 blocks, 16 k-blocks of which the last is partial, clusters of 8), more
+    column blocks than fit on the device at once (305 blocks: no split, several
+    waves), a single k-block (no split) and a ragged k split into parts of
+    unequal length. beta != 0 with C read through an unaligned row stride;
+    every output checked, and a second call gives the same bits."""
+    M, N, K = shape
+    p = w.problem(M, N, K, dtype, "normal", 701 + M + N, alpha=0.75, beta=-1.25,
+                  c_dist="normal", lda=ld_for(dtype, K), ldb=ld_for(dtype, N))
+    got, out = run_gpu(gemm_mod, p, ldc=N + 1, aligned=False)
+    assert_parity(got, oracle_of(oracle_mod, p), exact=False)
+    out.check_canaries()
+    again, _ = run_gpu(gemm_mod, p, ldc=N + 1, aligned=False)
+    assert torch.equal(got, again)
+
+
+@pytest.mark.parametrize("shape", [(10, 2048, 1024), (16, 2064, 8192), (16, 39040, 1024),
+                                   (48, 4096, 3072), (12, 2048, 4112), (64, 2048, 2048),
+                                   (33, 2080, 5120)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_skinny_int8_cluster(gemm_mod, oracle_mod, shape):
+    """int8 with A and B rows in whole 16-byte units and 10..64 rows: the
+    cluster form reads both operands as bytes and widens them in shared memory
+    (row bounds 16, 32 and 64), splitting k on 1024-k chunks across a cluster:
+    one chunk (no split), a ragged N, more column blocks than fit at once,
+    three chunks (clusters of 2), a ragged last chunk, 64 rows; beta != 0,
+    every output bit-exact, and a second call gives the same bits."""
+    M, N, K = shape
+    p = w.problem(M, N, K, torch.int8, "int8", 801 + M, alpha=-5, beta=3, c_dist="int")
+    got, out = run_gpu(gemm_mod, p, ldc=N + 3, aligned=False)
+    assert_parity(got, oracle_of(oracle_mod, p), exact=True)
+    out.check_canaries()
+    again, _ = run_gpu(gemm_mod, p, ldc=N + 3, aligned=False)
+    assert torch.equal(got, again)
+
+
 @pytest.mark.parametrize("shape", [(10, 2048, 2048, 1000), (16, 4100, 4112, 3072),
                                    (16, 8192, 8192, 4101), (24, 4096, 4096, 2048),
                                    (32, 2048, 2064, 3000), (33, 2048, 2064, 2049),
