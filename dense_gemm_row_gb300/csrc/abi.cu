@@ -376,7 +376,9 @@ gemm_status_t gemm_s8(int64_t M, int64_t N, int64_t K, int32_t alpha, const int8
   if (K == 0) return from_cuda(dgr::launch_scale_s32(int(M), int(N), beta, C, ldc, stream));
   // Short and wide with at least 16 column blocks of 128: the tensor-core
   // kernel that reads int8 B once, as stored.
-  if (M >= dgr::kI8RawMinM && N >= 16 * 128 && dgr::tc_skinny_i8_supported(int(M), B, ldb))
+  if (N >= 16 * 128 && dgr::tc_skinny_i8_supported(int(M), B, ldb) &&
+      (M >= dgr::kI8RawMinM ||
+       (M >= dgr::kI8ClusterMinM && dgr::tc_skinny_s8_supported(int(M), A, lda, B, ldb))))
     return from_cuda(dgr::launch_gemm_s8_skinny_raw(*dev, int(M), int(N), int(K), alpha, A, lda,
                                                     B, ldb, beta, C, ldc, stream));
   if (dgr::small_m_supported(int(M), A, lda, B, ldb, 1))  // few rows: int8 B read once, dp4a

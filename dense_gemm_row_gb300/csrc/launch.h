@@ -126,11 +126,16 @@ bool tc_skinny_i8_supported(int M, const void *B, int64_t ldb);
 cudaError_t launch_gemm_s8_skinny_raw(const DeviceInfo &dev, int M, int N, int K, int32_t alpha,
                                       const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
                                       int32_t beta, int32_t *C, int64_t ldc, cudaStream_t stream);
-// Rows from which gemm_s8 prefers it over the dp4a small-M kernel.
+// Rows from which gemm_s8 prefers it over the dp4a small-M kernel: with A and
+// B read as stored (the cluster form) from 5 rows, with a widened A from 10.
+// Measured on GB300 at N = K = 8192: dp4a 19.1 us at 4 rows and 26.3 us at 6;
+// the cluster form about 19.5 us for any row count up to 16; the widened-A
+// form tied with dp4a at 10 rows.
 #ifndef DGR_I8RAW_MIN_M
 #define DGR_I8RAW_MIN_M 10
 #endif
 constexpr int kI8RawMinM = DGR_I8RAW_MIN_M;
+constexpr int kI8ClusterMinM = 5;
 // int8 A and B read as stored by the cluster form of the transposed-role
 // kernel (gemm_tc_skinny.cu; up to 64 rows): both operands 16-byte aligned
 // with row strides in whole 16-byte units (tc_skinny_s8_supported).

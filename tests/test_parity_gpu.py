@@ -372,15 +372,16 @@ def test_skinny_cluster_edges(gemm_mod, oracle_mod, dtype, shape):
 
 @pytest.mark.parametrize("shape", [(10, 2048, 1024), (16, 2064, 8192), (16, 39040, 1024),
                                    (48, 4096, 3072), (12, 2048, 4112), (64, 2048, 2048),
-                                   (33, 2080, 5120)],
+                                   (33, 2080, 5120), (5, 2048, 2048), (9, 4096, 1040)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_skinny_int8_cluster(gemm_mod, oracle_mod, shape):
-    """int8 with A and B rows in whole 16-byte units and 10..64 rows: the
+    """int8 with A and B rows in whole 16-byte units and 5..64 rows: the
     cluster form reads both operands as bytes and widens them in shared memory
     (row bounds 16, 32 and 64), splitting k on 1024-k chunks across a cluster:
     one chunk (no split), a ragged N, more column blocks than fit at once,
-    three chunks (clusters of 2), a ragged last chunk, 64 rows; beta != 0,
-    every output bit-exact, and a second call gives the same bits."""
+    three chunks (clusters of 2), a ragged last chunk, 64 rows, and the 5- and
+    9-row problems it takes from the dp4a kernel; beta != 0, every output
+    bit-exact, and a second call gives the same bits."""
     M, N, K = shape
     p = w.problem(M, N, K, torch.int8, "int8", 801 + M, alpha=-5, beta=3, c_dist="int")
     got, out = run_gpu(gemm_mod, p, ldc=N + 3, aligned=False)
