@@ -666,6 +666,18 @@ def measure_types(binding, torch, peaks, stream):
     run("bf16_batched_64x1024", binding.gemm_bf16_ex,
         (binding.OP_N, binding.OP_N, E, E, E, 1.0, A, E, E * E, B, E, E * E, 0.0, C, E, E * E,
          nb, stream), 20, nb * flops_of(E, E, E), bf16, "TFLOP/s")
+    # 137 GFLOP against 537 MB (A and B read once, fp32 C written once): the
+    # problem sits at the roofline's ridge, and at the measured peaks the bytes
+    # take longer than the flops. Its bound is the slower of the two.
+    d = out["bf16_batched_64x1024"]
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    nbytes = nb * (2 * E * E * 2 + E * E * 4)
+    t = d["ms"] / 1e3
+    t_bound = max(nb * flops_of(E, E, E) / (bf16 * 1e12), nbytes / (hbm * 1e9))
+    d["gbs"] = nbytes / t / 1e9
+    d["frac_hbm"] = d["gbs"] / hbm
+    d["roofline_bound"] = "hbm" if nbytes / (hbm * 1e9) >= t_bound else "tensor"
+    d["frac_of_roofline"] = t_bound / t
     del A, B, C
     torch.cuda.empty_cache()
     return out
@@ -677,7 +689,8 @@ def compact_configs(name, head, extras, skinny, types):
     """One short entry per measured workload -- [value (TFLOP/s or TOPS),
     fraction of its pipe's peak, ms per call, median SM MHz, throttle reasons]
     -- plus the fraction of HBM bandwidth of each short, wide shape and the
-    batched many-small fraction."""
+    batched many-small fraction (of the tensor peak, and of its roofline bound:
+    the slower of its flops at the tensor peak and its bytes at HBM speed)."""
     def entry(d):
         c = d.get("clocks") or {}
         mhz = c.get("sm_mhz")
@@ -689,7 +702,11 @@ def compact_configs(name, head, extras, skinny, types):
     if skinny:
         out["skinny_frac_hbm"] = {k: round(d["frac_hbm"], 3) for k, d in skinny.items()}
     if "bf16_batched_64x1024" in types:
-        out["bf16_batched_64x1024_frac"] = round(types["bf16_batched_64x1024"]["frac"], 3)
+        d = types["bf16_batched_64x1024"]
+        out["bf16_batched_64x1024_frac"] = round(d["frac"], 3)
+        if "frac_of_roofline" in d:
+            out["bf16_batched_64x1024_frac_of_roofline"] = [round(d["frac_of_roofline"], 3),
+                                                           d["roofline_bound"]]
     return out
 
 
