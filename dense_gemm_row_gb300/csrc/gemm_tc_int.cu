@@ -78,6 +78,76 @@ cudaError_t widen8(const DeviceInfo &dev, const T8 *src, int64_t lds, __half *ds
   return cudaGetLastError();
 }
 
+// Both operands of one GEMM in a single launch (one grid-stride loop over A's
+// chunks, then B's), which also zeroes `nflags` words of split-k tail flags
+// for the tensor-core kernel that follows; it lets that kernel start as a
+// programmatic dependent once every thread here is done.
+struct WidenJob {
+  const void *src;
+  int64_t lds, src_stride;
+  __half *dst;
+  int64_t ldd;
+  int rows, cols, count;
+  int vec_ok;
+};
+template <typename T8, int kOffset = 0>
+__device__ __forceinline__ void widen_chunk(const WidenJob &j, int64_t i) {
+  const int64_t chunks_per_row = (j.ldd + 15) / 16;
+  const int64_t r = i / chunks_per_row;
+  const int c0 = static_cast<int>((i - r * chunks_per_row) * 16);
+  const int64_t m = r / j.rows;
+  const T8 *s = static_cast<const T8 *>(j.src) + m * j.src_stride + (r - m * j.rows) * j.lds;
+  __align__(16) __half h[16];
+  if (j.vec_ok && c0 + 16 <= j.cols) {
+    const int4 v = *reinterpret_cast<const int4 *>(s + c0);
+    const int w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+      h[q] = __int2half_rn(
+          static_cast<int>(static_cast<T8>(static_cast<uint32_t>(w[q >> 2]) >> (8 * (q & 3)))) -
+          kOffset);
+  } else {
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int c = c0 + q;
+      h[q] = __int2half_rn(c < j.cols ? static_cast<int>(s[c]) - kOffset : 0);
+    }
+  }
+  uint4 *d = reinterpret_cast<uint4 *>(j.dst + r * j.ldd + c0);
+  d[0] = *reinterpret_cast<const uint4 *>(h);
+  if (c0 + 16 <= j.ldd) d[1] = *reinterpret_cast<const uint4 *>(h + 8);
+}
+template <typename T8>
+__global__ void widen8x2_kernel(WidenJob a, WidenJob b, uint32_t *flags, int nflags) {
+  const int64_t tid = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = tid; i < nflags; i += step) flags[i] = 0;
+  const int64_t ta = static_cast<int64_t>(a.rows) * a.count * ((a.ldd + 15) / 16);
+  const int64_t tb = static_cast<int64_t>(b.rows) * b.count * ((b.ldd + 15) / 16);
+  for (int64_t i = tid; i < ta + tb; i += step) {
+    if (i < ta) {
+      widen_chunk<T8>(a, i);
+    } else {
+      widen_chunk<T8>(b, i - ta);
+    }
+  }
+  grid_launch_dependents();
+}
+
+template <typename T8>
+cudaError_t widen8x2(const DeviceInfo &dev, const WidenJob &a, const WidenJob &b,
+                     uint32_t *flags, int nflags, cudaStream_t stream) {
+  const int64_t total = static_cast<int64_t>(a.rows) * a.count * ((a.ldd + 15) / 16) +
+                        static_cast<int64_t>(b.rows) * b.count * ((b.ldd + 15) / 16);
+  const int threads = 256;
+  int64_t blocks = (total + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(dev.sm_count) * 16;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  widen8x2_kernel<T8><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(a, b, flags, nflags);
+  return cudaGetLastError();
+}
+
 // The widened operands of an 8-bit GEMM in one scratch block: A's copies at
 // offset 0, B's at b_off (256-byte aligned); each copy packed (row stride
 // rounded up to 8 values, matrices back to back).
@@ -109,26 +179,48 @@ template <int kKind, bool kAllForms, typename T8>
 cudaError_t run_int(const DeviceInfo &dev, const BatchOps &ops, int M, int N, int K,
                     int32_t alpha, const T8 *A, int64_t lda, const T8 *B, int64_t ldb,
                     int32_t beta, int32_t *C, int64_t ldc, void *scratch, uint32_t *flags,
-                    size_t flags_words, cudaStream_t stream) {
+                    size_t flags_words, cudaStream_t stream, bool caller_flags) {
   const WideLayout w(ops, M, N, K);
   __half *a16 = static_cast<__half *>(scratch);
   __half *b16 = reinterpret_cast<__half *>(static_cast<uint8_t *>(scratch) + w.b_off);
-  cudaError_t e = widen8<T8>(dev, A, lda, a16, w.lda16, w.a_rows, w.a_cols, stream, w.na,
-                             ops.stride_a);
-  if (e == cudaSuccess)
-    e = widen8<T8>(dev, B, ldb, b16, w.ldb16, w.b_rows, w.b_cols, stream, w.nb, ops.stride_b);
+  auto job = [](const T8 *src, int64_t ld, int64_t stride, __half *dst, int64_t ldd, int rows,
+                int cols, int count) {
+    WidenJob j;
+    j.src = src;
+    j.lds = ld;
+    j.src_stride = stride;
+    j.dst = dst;
+    j.ldd = ldd;
+    j.rows = rows;
+    j.cols = cols;
+    j.count = count;
+    j.vec_ok = (reinterpret_cast<uintptr_t>(src) % 16 == 0) && (ld % 16 == 0) &&
+               (count == 1 || stride % 16 == 0);
+    return j;
+  };
+  // The flags for the tensor-core kernel's split-k tail are zeroed by the
+  // same launch (at most kTailFlagWords of them are ever used).
+  const int nflags = flags != nullptr ? static_cast<int>(flags_words < kTailFlagWords
+                                                             ? flags_words
+                                                             : kTailFlagWords)
+                                      : 0;
+  cudaError_t e = widen8x2<T8>(dev,
+                               job(A, lda, ops.stride_a, a16, w.lda16, w.a_rows, w.a_cols, w.na),
+                               job(B, ldb, ops.stride_b, b16, w.ldb16, w.b_rows, w.b_cols, w.nb),
+                               flags, nflags, stream);
   if (e != cudaSuccess) return e;
   // Short, wide int8 problems: the transposed-role kernel (1024-k chunks).
   if (kKind == kKindS8 && tc_skinny_route(M, N, dev.sm_count) && ops.plain())
     return launch_tc_skinny_int(dev, M, N, K, alpha, a16, w.lda16, b16, w.ldb16, beta, C, ldc,
-                                stream, flags, flags_words);
+                                stream, caller_flags ? flags : nullptr, flags_words);
   BatchOps wide = ops;
   wide.stride_a = w.na > 1 ? w.a_mat : 0;
   wide.stride_b = w.nb > 1 ? w.b_mat : 0;
   return launch_tc<kKind, kAllForms>(dev, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, kFmtF16,
                                      CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wide, M, N, K, alpha, a16,
                                      w.lda16, b16, w.ldb16, beta, C, ldc, stream, flags,
-                                     flags_words);
+                                     static_cast<size_t>(nflags), nullptr, nullptr, 0,
+                                     /*flags_zeroed=*/true);
 }
 
 // The same on scratch drawn from the library's stream-ordered pool and
@@ -142,10 +234,13 @@ cudaError_t run_int_pooled(const DeviceInfo &dev, const BatchOps &ops, int M, in
   cudaError_t e = device_pool(dev, &pool);
   if (e != cudaSuccess) return e;
   void *scratch = nullptr;
-  e = cudaMallocFromPoolAsync(&scratch, w.total, pool, stream);
+  const size_t flags_off = (w.total + 255) / 256 * 256;
+  e = cudaMallocFromPoolAsync(&scratch, flags_off + kTailFlagWords * 4, pool, stream);
   if (e != cudaSuccess) return e;
+  uint32_t *flags =
+      reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(scratch) + flags_off);
   e = run_int<kKind, kAllForms, T8>(dev, ops, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
-                                    scratch, nullptr, 0, stream);
+                                    scratch, flags, kTailFlagWords, stream, false);
   cudaError_t f = cudaFreeAsync(scratch, stream);
   return e != cudaSuccess ? e : f;
 }
@@ -329,7 +424,7 @@ cudaError_t launch_gemm_s8_scratch(const DeviceInfo &dev, int M, int N, int K, i
                                    int32_t beta, int32_t *C, int64_t ldc, void *scratch,
                                    uint32_t *flags, size_t flags_words, cudaStream_t stream) {
   return run_int<kKindS8, true, int8_t>(dev, BatchOps(), M, N, K, alpha, A, lda, B, ldb, beta, C,
-                                         ldc, scratch, flags, flags_words, stream);
+                                         ldc, scratch, flags, flags_words, stream, true);
 }
 
 }  // namespace dgr

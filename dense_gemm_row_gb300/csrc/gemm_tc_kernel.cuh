@@ -437,6 +437,12 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tmA, const CUten
   }
   tc_fence_after_sync();
   const uint32_t tmem_base = sm.tmem_base;
+  // Launched as a programmatic dependent of the previous kernel on the stream
+  // (for instance the int8 path's widening pass): the set-up above overlaps
+  // that kernel's tail; nothing in global memory is touched before it has
+  // completed and its writes are visible.
+  grid_dependency_wait();
+  grid_launch_dependents();
 
   const int KB = (p.K + kBK - 1) / kBK;
   // int mode: exact fp32 chunks of kChunkK values of k; float mode: one chunk per item
@@ -880,6 +886,9 @@ inline int pair_capacity(const DeviceInfo &dev, const void *kern, size_t smem) {
 }
 
 constexpr int kMaxSplit = DGR_TC_MAX_SPLIT;  // parts per tail tile (each adds one pass over C)
+// Tail flags any one launch can need: two per split tile, and fewer tiles are
+// split than there are units (at most one per SM).
+constexpr size_t kTailFlagWords = 1024;
 
 // The kernel for an operand form (only the forms a kind is built with).
 template <int kKind, bool kPair, bool kAT, bool kBT>
@@ -898,7 +907,8 @@ cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, uint32_t ab
                       const void *B, int64_t ldb, typename TcKind<kKind>::Scale beta,
                       typename TcKind<kKind>::Out *C, int64_t ldc, cudaStream_t stream,
                       uint32_t *flags_ws, size_t flags_words, const int32_t *row_corr = nullptr,
-                      const int32_t *col_corr = nullptr, int32_t corr_const = 0) {
+                      const int32_t *col_corr = nullptr, int32_t corr_const = 0,
+                      bool flags_zeroed = false) {
   using K_ = TcKind<kKind>;
   constexpr int kEs = K_::kInBytes;
   constexpr int kBK = K_::kBK;
@@ -1034,7 +1044,7 @@ cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, uint32_t ab
       if (e != cudaSuccess) return e;
       p.tail_flags = static_cast<uint32_t *>(pool_flags);
     }
-    if (p.split > 1) {
+    if (p.split > 1 && !(flags_zeroed && p.tail_flags == flags_ws)) {
       cudaError_t e = cudaMemsetAsync(p.tail_flags, 0, need * 4, stream);
       if (e != cudaSuccess) {
         if (pool_flags) cudaFreeAsync(pool_flags, stream);
@@ -1050,21 +1060,33 @@ cudaError_t launch_tc(const DeviceInfo &dev, CUtensorMapDataType dt, uint32_t ab
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem_pair;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, kern_pair, tmA, tmB, tmC, p);
     if (e == cudaSuccess) e = cudaGetLastError();
   } else {
     e = set_max_dynamic_smem(reinterpret_cast<const void *>(kern_single),
                              static_cast<int>(smem_single), dev.device);
     if (e == cudaSuccess) {
-      kern_single<<<units, kThreads, smem_single, stream>>>(tmA, tmB, tmC, p);
-      e = cudaGetLastError();
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(units), 1, 1);
+      cfg.blockDim = dim3(kThreads, 1, 1);
+      cfg.dynamicSmemBytes = smem_single;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      e = cudaLaunchKernelEx(&cfg, kern_single, tmA, tmB, tmC, p);
+      if (e == cudaSuccess) e = cudaGetLastError();
     }
   }
   if (pool_flags) {
