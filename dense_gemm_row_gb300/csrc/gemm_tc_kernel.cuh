@@ -535,6 +535,16 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tmA, const CUten
       uint32_t stage = 0, phase = 0, chunk = 0;
       bool ok = true;
       bool any = false;
+      // Descriptors of stage 0 (layouts below); a stage or a k-step only moves
+      // the start address, the descriptor's low 14 bits (address / 16), so each
+      // MMA's descriptors are one add away from these.
+      const uint64_t adesc0 = kAT ? smem_desc(smem_u32(sm.a[0]), kMNBoxBytes, kAtomBytes, 2u)
+                                  : smem_desc(smem_u32(sm.a[0]), 16, kAtomBytes, 2u);
+      const uint64_t bdesc0 = kBT ? smem_desc(smem_u32(sm.b[0]), 16, kAtomBytes, 2u)
+                                  : smem_desc(smem_u32(sm.b[0]), kMNBoxBytes, kAtomBytes, 2u);
+      constexpr uint32_t kAStage = sizeof(sm.a[0]) >> 4, kBStage = sizeof(sm.b[0]) >> 4;
+      constexpr uint32_t kAStepK = (kAT ? kMNStep : 32u) >> 4;  // one MMA's k, in 16 B
+      constexpr uint32_t kBStepK = (kBT ? 32u : kMNStep) >> 4;
       for (int n = 0; ok && get_work(unit, n, units, p.dp_tiles, p.tail_tiles, p.split, KB,
                                      kb_unit, wi);
            ++n) {
@@ -563,8 +573,8 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tmA, const CUten
               break;
             }
             tc_fence_after_sync();
-            const uint32_t a_addr = smem_u32(sm.a[stage]);
-            const uint32_t b_addr = smem_u32(sm.b[stage]);
+            const uint64_t ad = adesc0 + stage * kAStage, bd = bdesc0 + stage * kBStage;
+            const uint32_t first = kb > kb0 ? 1u : 0u;
 #pragma unroll
             for (int kk = 0; kk < kBK / K_::kMmaK; ++kk) {
               // K-major operand: 128-byte swizzled rows of k; one MMA's k is 32 B
@@ -572,14 +582,8 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tmA, const CUten
               // MN-major operand: 128-byte swizzled rows of m or n, one row per
               // k; one MMA's k is kMmaK rows further; LBO = one box of
               // kMNElems values, SBO = 1 KiB between groups of 8 k-rows.
-              const uint64_t adesc =
-                  kAT ? smem_desc(a_addr + kk * kMNStep, kMNBoxBytes, kAtomBytes, 2u)
-                      : smem_desc(a_addr + kk * 32, 16, kAtomBytes, 2u);
-              const uint64_t bdesc =
-                  kBT ? smem_desc(b_addr + kk * 32, 16, kAtomBytes, 2u)
-                      : smem_desc(b_addr + kk * kMNStep, kMNBoxBytes, kAtomBytes, 2u);
-              const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
-              issue_mma<kKind, kPair>(d_tmem, adesc, bdesc, p.idesc, acc);
+              issue_mma<kKind, kPair>(d_tmem, ad + kk * kAStepK, bd + kk * kBStepK, p.idesc,
+                                      kk > 0 ? 1u : first);
             }
             any = true;
             // This stage's shared memory is free again in both CTAs.
