@@ -330,6 +330,9 @@ gemm_status_t gemm_f32(int64_t M, int64_t N, int64_t K, float alpha, const float
                                   B, ldb, beta, C + int64_t(m1) * ldc, ldc, stream);
     return from_cuda(e);
   }
+  if (dgr::small_n_supported(int(M), int(N), A, lda, 4))  // few columns: stream A once
+    return from_cuda(dgr::launch_small_n_f32(int(M), int(N), int(K), alpha, A, lda, B, ldb, beta,
+                                             C, ldc, stream));
   return from_cuda(dgr::launch_sgemm_simt(*dev, int(M), int(N), int(K), alpha, A, lda, B, ldb,
                                           beta, C, ldc, stream));
 }
@@ -349,6 +352,9 @@ static gemm_status_t gemm_half(bool is_bf16, int64_t M, int64_t N, int64_t K, fl
   const DeviceInfo *dev = nullptr;
   if ((st = current_device(&dev)) != GEMM_OK) return st;
   if (K == 0) return from_cuda(dgr::launch_scale_f32(int(M), int(N), beta, C, ldc, stream));
+  if (dgr::small_n_supported(int(M), int(N), A, lda, 2))  // few columns: stream A once
+    return from_cuda(dgr::launch_small_n_half(is_bf16, int(M), int(N), int(K), alpha, A, lda, B,
+                                              ldb, beta, C, ldc, stream));
   return from_cuda(dgr::launch_gemm_tc_f16(*dev, is_bf16, int(M), int(N), int(K), alpha, A, lda,
                                            B, ldb, beta, C, ldc, stream));
 }
@@ -384,6 +390,9 @@ gemm_status_t gemm_s8(int64_t M, int64_t N, int64_t K, int32_t alpha, const int8
   if (dgr::small_m_supported(int(M), A, lda, B, ldb, 1))  // few rows: int8 B read once, dp4a
     return from_cuda(dgr::launch_small_m_s8(*dev, int(M), int(N), int(K), alpha, A, lda, B, ldb,
                                             beta, C, ldc, stream));
+  if (dgr::small_n_supported(int(M), int(N), A, lda, 1))  // few columns: stream A once
+    return from_cuda(dgr::launch_small_n_s8(int(M), int(N), int(K), alpha, A, lda, B, ldb, beta,
+                                            C, ldc, stream));
   return from_cuda(dgr::launch_gemm_s8(*dev, int(M), int(N), int(K), alpha, A, lda, B, ldb, beta,
                                        C, ldc, stream));
 }

@@ -157,6 +157,23 @@ cudaError_t launch_transpose_f32(const DeviceInfo &dev, const float *src, int64_
 // per (kernel, device); later calls only look the pair up.
 cudaError_t set_max_dynamic_smem(const void *kernel, int bytes, int device);
 
+// Tall, narrow problems (gemm_small_n.cu): N <= 8 columns (16-bit inputs:
+// N <= 2) and at least
+// kSmallNMinM rows; A read once with 16-byte loads (A 16-byte aligned, rows a
+// whole number of 16-byte units: small_n_supported), B staged in shared
+// memory. fp32, bf16 / fp16 (fp32 accumulation, fp32 C) and int8 (int32 C).
+constexpr int kSmallNMinM = 512;
+bool small_n_supported(int M, int N, const void *A, int64_t lda, int esize);
+cudaError_t launch_small_n_f32(int M, int N, int K, float alpha, const float *A, int64_t lda,
+                               const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
+                               cudaStream_t stream);
+cudaError_t launch_small_n_half(bool is_bf16, int M, int N, int K, float alpha, const void *A,
+                                int64_t lda, const void *B, int64_t ldb, float beta, float *C,
+                                int64_t ldc, cudaStream_t stream);
+cudaError_t launch_small_n_s8(int M, int N, int K, int32_t alpha, const int8_t *A, int64_t lda,
+                              const int8_t *B, int64_t ldb, int32_t beta, int32_t *C, int64_t ldc,
+                              cudaStream_t stream);
+
 // fp32 and int8 GEMM for M <= 32 (gemm_small_m.cu): streams B once with TMA,
 // 4 columns x all rows per thread (packed fp32 FMA / dp4a). Usable when
 // small_m_supported(): A and B 16-byte aligned with row strides that are whole

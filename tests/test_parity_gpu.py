@@ -422,6 +422,39 @@ def test_skinny_int8_b_as_stored_extremes(gemm_mod, oracle_mod):
     np.testing.assert_array_equal(C.cpu().numpy(), oracle_mod.gemm_s8(A, B))
 
 
+def _ld16(dtype, cols):
+    """A row stride in whole 16-byte units (the narrow-N kernel's condition on A)."""
+    per = {torch.float32: 4, torch.bfloat16: 8, torch.float16: 8, torch.int8: 16}[dtype]
+    return (cols + per - 1) // per * per
+
+
+@pytest.mark.parametrize("dtype", ALL_DTYPES, ids=str)
+@pytest.mark.parametrize("shape", [(512, 1, 1000), (4097, 3, 3001), (2048, 8, 8192),
+                                   (600, 5, 4100), (8192, 1, 8192), (1111, 2, 37)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_narrow_n_shapes(gemm_mod, oracle_mod, dtype, shape):
+    """Tall, narrow problems (N <= 8, at least 512 rows; 16-bit inputs N <= 2,
+    wider ones take the tiled tensor-core kernel) on the narrow-N kernel:
+    A streamed once with 16-byte loads (its row stride padded to 16 bytes),
+    B staged in shared memory in 1024-k chunks (a ragged last chunk, a K
+    shorter than one 16-byte load of a lane's slice), N rounded up to 1, 2, 4 or
+    8, rows that do not fill the last CTA; beta != 0 with an unaligned C; every
+    element checked, and a second call gives the same bits."""
+    M, N, K = shape
+    ldb = 8 if dtype in (torch.bfloat16, torch.float16) else None  # 16-bit: ldb % 8 == 0
+    if dtype == torch.int8:
+        p = w.problem(M, N, K, dtype, "int8", 951 + M, alpha=-3, beta=2, c_dist="int",
+                      lda=_ld16(dtype, K))
+    else:
+        p = w.problem(M, N, K, dtype, "normal", 951 + M, alpha=0.5, beta=-1.5, c_dist="normal",
+                      lda=_ld16(dtype, K), ldb=ldb)
+    got, out = run_gpu(gemm_mod, p, ldc=N + 1, aligned=False)
+    assert_parity(got, oracle_of(oracle_mod, p), exact=(dtype == torch.int8))
+    out.check_canaries()
+    again, _ = run_gpu(gemm_mod, p, ldc=N + 1, aligned=False)
+    assert torch.equal(got, again)
+
+
 @pytest.mark.parametrize("dtype", ALL_DTYPES, ids=str)
 @pytest.mark.parametrize("shape", [(8, 520, 8192), (32, 1024, 4096), (1, 128, 16384),
                                    (3, 4096, 2048)], ids=lambda s: "x".join(map(str, s)))
