@@ -584,31 +584,33 @@ def measure_skinny(binding, torch, peaks, stream):
                                    "tflops": flops_of(M, N, K) / t / 1e12}
         del B
         torch.cuda.empty_cache()
-    # Tall and narrow, matrix times vector (N = 1): A (M x K) streamed once. A
-    # 16-bit B keeps its row stride at 8 (the tensor-map layout rule of the
-    # 16-bit entry points), one column used.
+    # Tall and narrow: matrix times vector (N = 1), and 16 columns for fp32 and
+    # int8; A (M x K) streamed once. A 16-bit B keeps its row stride at 8 (the
+    # tensor-map layout rule of the 16-bit entry points), one column used.
     M = 8192
-    for kind, dt, cdt in (("bf16", torch.bfloat16, torch.float32),
-                          ("f32", torch.float32, torch.float32),
-                          ("s8", torch.int8, torch.int32)):
+    for kind, dt, cdt, widths in (("bf16", torch.bfloat16, torch.float32, (1,)),
+                                  ("f32", torch.float32, torch.float32, (1, 16)),
+                                  ("s8", torch.int8, torch.int32, (1, 16))):
         if kind == "s8":
             A = torch.randint(-128, 128, (M, K), device="cuda", dtype=torch.int8, generator=g)
-            Bw = torch.randint(-128, 128, (K, 8), device="cuda", dtype=torch.int8, generator=g)
+            Bw = torch.randint(-128, 128, (K, 16), device="cuda", dtype=torch.int8, generator=g)
             alpha, beta = 1, 0
         else:
             A = torch.randn(M, K, device="cuda", generator=g).to(dt)
-            Bw = torch.randn(K, 8, device="cuda", generator=g).to(dt)
+            Bw = torch.randn(K, 16 if kind == "f32" else 8, device="cuda", generator=g).to(dt)
             alpha, beta = 1.0, 0.0
-        B = Bw[:, :1] if kind == "bf16" else Bw[:, :1].contiguous()
-        C = torch.zeros(M, 1, device="cuda", dtype=cdt)
-        ms, _, _ = time_device(binding, torch, kind, (A, B, C, alpha, beta), 20, 3, stream)
-        t = ms / 20 / 1e3
-        nbytes = (A.numel() * A.element_size() + K * B.element_size()
-                  + C.numel() * C.element_size())
-        out[f"{kind}_N1"] = {"M": M, "N": 1, "K": K, "ms": t * 1e3,
-                             "gbs": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / hbm,
-                             "tflops": flops_of(M, 1, K) / t / 1e12}
-        del A, Bw, B, C
+        for n in widths:
+            B = Bw[:, :n] if kind == "bf16" else Bw[:, :n].contiguous()
+            C = torch.zeros(M, n, device="cuda", dtype=cdt)
+            ms, _, _ = time_device(binding, torch, kind, (A, B, C, alpha, beta), 20, 3, stream)
+            t = ms / 20 / 1e3
+            nbytes = (A.numel() * A.element_size() + K * n * B.element_size()
+                      + C.numel() * C.element_size())
+            out[f"{kind}_N{n}"] = {"M": M, "N": n, "K": K, "ms": t * 1e3,
+                                   "gbs": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / hbm,
+                                   "tflops": flops_of(M, n, K) / t / 1e12}
+            del B, C
+        del A, Bw
     torch.cuda.empty_cache()
     return out
 

@@ -1,4 +1,4 @@
-// gemm_small_n.cu -- GEMM for tall, narrow problems (N <= 8), including the
+// gemm_small_n.cu -- GEMM for tall, narrow problems (N <= 16), including the
 // matrix-vector product (N = 1):
 //
 //     C = alpha * A * B + beta * C       A: M x K, B: K x N, C: M x N, row-major
@@ -40,8 +40,7 @@ constexpr int kSnThreads = 256;
 constexpr int kSnWarps = kSnThreads / 32;
 constexpr int kRows = 4;                   // rows of A per warp
 constexpr int kSnRowsPerCta = kSnWarps * kRows;
-constexpr int kKC = 1024;                  // values of k per staged chunk of B
-constexpr int kMaxNP = 8;
+constexpr int kMaxNP = 16;
 
 template <typename In>
 struct SnType {
@@ -50,9 +49,21 @@ struct SnType {
   static constexpr bool kInt = std::is_same<In, int8_t>::value;
   using Acc = typename std::conditional<kInt, int32_t, float>::type;
   using Bt = typename std::conditional<kInt, int8_t, float>::type;  // staged B element
-  // staged row (one column of B) stride: 16 bytes of padding, so the
-  // transposing stores of one k spread over the banks
-  static constexpr int kBtStride = kKC + 16 / static_cast<int>(sizeof(Bt));
+};
+
+// Per column count: KC values of k per staged chunk of B (at most 32 staged
+// values per thread, so that all loads of a chunk are in flight at once: 512
+// for 16 columns), S the staged row (one column of B) stride, with 16 bytes
+// of padding so that the transposing stores of one k spread over the banks,
+// and G the steps of A loaded ahead (kRows x NP accumulators and G x kRows
+// 16-byte loads per lane must fit the 128 registers of two CTAs per SM).
+template <typename In, int NP>
+struct SnShape {
+  using Bt = typename SnType<In>::Bt;
+  static constexpr int KC = NP * 1024 > 32 * kSnThreads ? 512 : 1024;
+  static constexpr int S = KC + 16 / static_cast<int>(sizeof(Bt));
+  static constexpr int kSteps = KC / (32 * SnType<In>::kVec);
+  static constexpr int G = (NP >= 16 ? 2 : 4) < kSteps ? (NP >= 16 ? 2 : 4) : kSteps;
 };
 
 __device__ __forceinline__ float to_float(float x) { return x; }
@@ -89,7 +100,7 @@ template <typename In, int NP>
 __device__ __forceinline__ void sn_step(const uint4 (&a)[kRows],
                                         const typename SnType<In>::Bt *bt, int kk,
                                         typename SnType<In>::Acc (&acc)[kRows][NP]) {
-  constexpr int S = SnType<In>::kBtStride;
+  constexpr int S = SnShape<In, NP>::S;
   if constexpr (std::is_same<In, int8_t>::value) {
 #pragma unroll
     for (int n = 0; n < NP; ++n) {
@@ -171,14 +182,16 @@ __device__ __forceinline__ int32_t sn_add(int32_t a, int32_t b) {
   return static_cast<int32_t>(static_cast<uint32_t>(a) + static_cast<uint32_t>(b));
 }
 
-// NP: N rounded up to 1, 2, 4 or 8 (every per-column loop runs NP times).
+// NP: N rounded up to 1, 2, 4, 8 or 16 (every per-column loop runs NP times).
 template <typename In, int NP>
 __global__ void __launch_bounds__(kSnThreads, 2)
     gemm_small_n_kernel(const SnArgs<In> p) {
   using T = SnType<In>;
   using Acc = typename T::Acc;
   using Bt = typename T::Bt;
-  constexpr int S = T::kBtStride;
+  using Sh = SnShape<In, NP>;
+  constexpr int S = Sh::S;
+  constexpr int KC = Sh::KC;
   constexpr int V = T::kVec;
   __shared__ __align__(16) Bt bt[NP * S];
   const int warp = threadIdx.x >> 5;
@@ -196,27 +209,39 @@ __global__ void __launch_bounds__(kSnThreads, 2)
 #pragma unroll
     for (int n = 0; n < NP; ++n) acc[r][n] = Acc(0);
 
-  for (int kc0 = 0; kc0 < p.K; kc0 += kKC) {
-    // Stage B[kc0 .. kc0 + kKC) x NP, column by column (zeros beyond K and N).
-    for (int idx = threadIdx.x; idx < kKC * NP; idx += kSnThreads) {
-      const int k = idx / NP, n = idx - (idx / NP) * NP;
-      const int gk = kc0 + k;
-      Bt v = Bt(0);
-      if (gk < p.K && n < p.N) {
-        if constexpr (T::kInt) {
-          v = p.B[static_cast<int64_t>(gk) * p.ldb + n];
-        } else {
-          v = to_float(p.B[static_cast<int64_t>(gk) * p.ldb + n]);
+  for (int kc0 = 0; kc0 < p.K; kc0 += KC) {
+    // Stage B[kc0 .. kc0 + KC) x NP, column by column (zeros beyond K and N):
+    // every load of the chunk is issued before the first store, so staging a
+    // chunk costs one round trip to L2.
+    {
+      constexpr int kIters = KC * NP / kSnThreads;
+      static_assert(kIters * kSnThreads == KC * NP && kIters <= 32, "staged values per thread");
+      Bt v[kIters];
+#pragma unroll
+      for (int u = 0; u < kIters; ++u) {
+        const int idx = u * kSnThreads + static_cast<int>(threadIdx.x);
+        const int gk = kc0 + idx / NP, n = idx % NP;
+        v[u] = Bt(0);
+        if (gk < p.K && n < p.N) {
+          if constexpr (T::kInt) {
+            v[u] = p.B[static_cast<int64_t>(gk) * p.ldb + n];
+          } else {
+            v[u] = to_float(p.B[static_cast<int64_t>(gk) * p.ldb + n]);
+          }
         }
       }
-      bt[n * S + k] = v;
+#pragma unroll
+      for (int u = 0; u < kIters; ++u) {
+        const int idx = u * kSnThreads + static_cast<int>(threadIdx.x);
+        bt[(idx % NP) * S + idx / NP] = v[u];
+      }
     }
     __syncthreads();
     // kG steps of 32 * kVec values of k at a time: all their loads of A are
     // issued before the first multiply, so kG * kRows 16-byte loads per lane
     // are in flight.
-    constexpr int kSteps = kKC / (32 * V);
-    constexpr int kG = kSteps < 4 ? kSteps : 4;
+    constexpr int kSteps = Sh::kSteps;
+    constexpr int kG = Sh::G;
     const bool rows_full = row0 + kRows <= p.M;  // the same for the whole warp
 #pragma unroll 1
     for (int s0 = 0; s0 < kSteps; s0 += kG) {
@@ -246,7 +271,8 @@ __global__ void __launch_bounds__(kSnThreads, 2)
   }
 
   // The lanes' partial sums: one fixed butterfly per element, after which
-  // every lane holds every total; lane r * NP + n writes element (r, n).
+  // every lane holds every total; lane (r * NP + n) mod 32 writes element
+  // (r, n) (one element per lane up to 8 columns, two for 16).
 #pragma unroll
   for (int r = 0; r < kRows; ++r)
 #pragma unroll
@@ -259,13 +285,21 @@ __global__ void __launch_bounds__(kSnThreads, 2)
   for (int r = 0; r < kRows; ++r)
 #pragma unroll
     for (int n = 0; n < NP; ++n)
-      if (lane == r * NP + n && row0 + r < p.M && n < p.N) {
+      if (lane == ((r * NP + n) & 31) && row0 + r < p.M && n < p.N) {
         Acc *cp = p.C + static_cast<int64_t>(row0 + r) * p.ldc + n;
         *cp = sn_axpby(p.alpha, acc[r][n], p.beta, use_c ? *cp : Acc(0), use_c);
       }
 }
-static_assert(kRows * kMaxNP <= 32, "one lane per output element of a warp");
-static_assert(kKC % (32 * 16) == 0, "whole steps of every element type in a chunk");
+static_assert(kRows * kMaxNP <= 64, "at most two output elements per lane");
+static_assert(SnShape<float, 16>::KC % (32 * 4) == 0 && SnShape<int8_t, 16>::KC % (32 * 16) == 0 &&
+                  SnShape<__nv_bfloat16, 2>::KC % (32 * 8) == 0,
+              "whole steps of every element type in a chunk");
+static_assert(SnShape<float, 16>::kSteps % SnShape<float, 16>::G == 0 &&
+                  SnShape<float, 8>::kSteps % SnShape<float, 8>::G == 0 &&
+                  SnShape<int8_t, 16>::kSteps % SnShape<int8_t, 16>::G == 0 &&
+                  SnShape<int8_t, 1>::kSteps % SnShape<int8_t, 1>::G == 0,
+              "whole groups of steps in a chunk");
+static_assert(SnShape<float, 16>::S * 16 * 4 <= 48 * 1024, "staged B within static shared memory");
 
 template <typename In, int NP>
 cudaError_t sn_launch(const SnArgs<In> &p, cudaStream_t stream) {
@@ -303,8 +337,13 @@ cudaError_t sn_dispatch(int M, int N, int K, typename SnType<In>::Acc alpha, con
   p.ldc = ldc;
   if (N <= 1) return sn_launch<In, 1>(p, stream);
   if (N <= 2) return sn_launch<In, 2>(p, stream);
-  if (N <= 4) return sn_launch<In, 4>(p, stream);
-  return sn_launch<In, 8>(p, stream);
+  if constexpr (sizeof(In) == 2) {
+    return cudaErrorInvalidValue;  // 16-bit inputs: up to 2 columns here
+  } else {
+    if (N <= 4) return sn_launch<In, 4>(p, stream);
+    if (N <= 8) return sn_launch<In, 8>(p, stream);
+    return sn_launch<In, 16>(p, stream);
+  }
 }
 
 }  // namespace

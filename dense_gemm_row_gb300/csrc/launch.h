@@ -157,7 +157,7 @@ cudaError_t launch_transpose_f32(const DeviceInfo &dev, const float *src, int64_
 // per (kernel, device); later calls only look the pair up.
 cudaError_t set_max_dynamic_smem(const void *kernel, int bytes, int device);
 
-// Tall, narrow problems (gemm_small_n.cu): N <= 8 columns (16-bit inputs:
+// Tall, narrow problems (gemm_small_n.cu): N <= 16 columns (16-bit inputs:
 // N <= 2) and at least
 // kSmallNMinM rows; A read once with 16-byte loads (A 16-byte aligned, rows a
 // whole number of 16-byte units: small_n_supported), B staged in shared

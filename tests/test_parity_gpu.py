@@ -430,18 +430,20 @@ def _ld16(dtype, cols):
 
 @pytest.mark.parametrize("dtype", ALL_DTYPES, ids=str)
 @pytest.mark.parametrize("shape", [(512, 1, 1000), (4097, 3, 3001), (2048, 8, 8192),
-                                   (600, 5, 4100), (8192, 1, 8192), (1111, 2, 37)],
+                                   (600, 5, 4100), (8192, 1, 8192), (1111, 2, 37),
+                                   (1500, 9, 2049), (2050, 16, 4100), (8192, 16, 1024)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_narrow_n_shapes(gemm_mod, oracle_mod, dtype, shape):
-    """Tall, narrow problems (N <= 8, at least 512 rows; 16-bit inputs N <= 2,
+    """Tall, narrow problems (N <= 16, at least 512 rows; 16-bit inputs N <= 2,
     wider ones take the tiled tensor-core kernel) on the narrow-N kernel:
     A streamed once with 16-byte loads (its row stride padded to 16 bytes),
-    B staged in shared memory in 1024-k chunks (a ragged last chunk, a K
-    shorter than one 16-byte load of a lane's slice), N rounded up to 1, 2, 4 or
-    8, rows that do not fill the last CTA; beta != 0 with an unaligned C; every
-    element checked, and a second call gives the same bits."""
+    B staged in shared memory in 1024-k chunks (512 for 16 fp32 columns; a
+    ragged last chunk, a K shorter than one 16-byte load of a lane's slice), N
+    rounded up to 1, 2, 4, 8 or 16 (two output elements per lane at 16), rows
+    that do not fill the last CTA; beta != 0 with an unaligned C; every element
+    checked, and a second call gives the same bits."""
     M, N, K = shape
-    ldb = 8 if dtype in (torch.bfloat16, torch.float16) else None  # 16-bit: ldb % 8 == 0
+    ldb = _ld16(dtype, N) if dtype in (torch.bfloat16, torch.float16) else None  # ldb % 8 == 0
     if dtype == torch.int8:
         p = w.problem(M, N, K, dtype, "int8", 951 + M, alpha=-3, beta=2, c_dist="int",
                       lda=_ld16(dtype, K))
