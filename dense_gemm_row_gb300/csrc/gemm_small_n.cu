@@ -91,6 +91,7 @@ struct SnArgs {
   int64_t ldb;
   Acc *C;
   int64_t ldc;
+  int b_vec;  // B 16-byte aligned (fp32) / 4-byte aligned (int8), row stride a multiple of 4
 };
 
 // One lane's k-slice of kRows rows (kVec values of A each, packed in a[r])
@@ -182,6 +183,133 @@ __device__ __forceinline__ int32_t sn_add(int32_t a, int32_t b) {
   return static_cast<int32_t>(static_cast<uint32_t>(a) + static_cast<uint32_t>(b));
 }
 
+// Staging of one chunk of B[kc0 .. kc0 + KC) x NP into bt (transposed: bt[n *
+// S + k] = B[kc0 + k][n], zeros beyond K and N). Every load of the chunk is
+// issued before the first store, so staging a chunk costs one round trip to
+// L2. Three forms: element by element (any B); fp32 with 16-byte loads of 4
+// columns (b_vec); int8 in blocks of 4 rows x 4 columns, one 4-byte load per
+// row and a byte transpose into 4 words of 4 consecutive k of one column
+// (b_vec).
+template <typename In, int NP>
+__device__ __forceinline__ void sn_stage_b(const SnArgs<In> &p, int kc0,
+                                           typename SnType<In>::Bt *bt) {
+  using T = SnType<In>;
+  using Bt = typename T::Bt;
+  constexpr int S = SnShape<In, NP>::S;
+  constexpr int KC = SnShape<In, NP>::KC;
+  const int tid = static_cast<int>(threadIdx.x);
+  if constexpr (std::is_same<In, float>::value && NP >= 4) {
+    if (p.b_vec) {
+      constexpr int kQ = NP / 4;  // 4-column groups per row of B
+      constexpr int kIt = KC * kQ / kSnThreads;
+      constexpr int kRound = kIt < 4 ? kIt : 4;  // 16-byte loads in flight per thread
+      static_assert(kIt * kSnThreads == KC * kQ && kIt % kRound == 0,
+                    "whole 4-column groups per thread");
+#pragma unroll 1
+      for (int u0 = 0; u0 < kIt; u0 += kRound) {
+        float4 v[kRound];
+#pragma unroll
+        for (int u = 0; u < kRound; ++u) {
+          const int idx = (u0 + u) * kSnThreads + tid;
+          const int gk = kc0 + idx / kQ, n0 = (idx % kQ) * 4;
+          v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (gk < p.K && n0 < p.N) {
+            const float *src = p.B + static_cast<int64_t>(gk) * p.ldb + n0;
+            if (n0 + 4 <= p.N) {
+              v[u] = *reinterpret_cast<const float4 *>(src);
+            } else {  // the last columns of a row: nothing past its end is read
+              v[u].x = src[0];
+              if (n0 + 1 < p.N) v[u].y = src[1];
+              if (n0 + 2 < p.N) v[u].z = src[2];
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kRound; ++u) {
+          const int idx = (u0 + u) * kSnThreads + tid;
+          const int k = idx / kQ, n0 = (idx % kQ) * 4;
+          bt[(n0 + 0) * S + k] = v[u].x;
+          bt[(n0 + 1) * S + k] = v[u].y;
+          bt[(n0 + 2) * S + k] = v[u].z;
+          bt[(n0 + 3) * S + k] = v[u].w;
+        }
+      }
+      return;
+    }
+  }
+  if constexpr (T::kInt && NP >= 4) {
+    if (p.b_vec) {
+      constexpr int kQ = NP / 4;  // 4-column groups per row of B
+      constexpr int kIt = KC / 4 * kQ / kSnThreads;  // 4 x 4 blocks per thread
+      static_assert(kIt * kSnThreads == KC / 4 * kQ, "whole 4 x 4 blocks per thread");
+      uint32_t w[kIt][4];
+#pragma unroll
+      for (int u = 0; u < kIt; ++u) {
+        const int idx = u * kSnThreads + tid;
+        const int gk = kc0 + (idx / kQ) * 4, n0 = (idx % kQ) * 4;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          w[u][r] = 0u;
+          if (gk + r < p.K && n0 < p.N) {
+            const int8_t *src = p.B + static_cast<int64_t>(gk + r) * p.ldb + n0;
+            if (n0 + 4 <= p.N) {
+              w[u][r] = *reinterpret_cast<const uint32_t *>(src);
+            } else {  // the last columns of a row: nothing past its end is read
+              uint32_t x = static_cast<uint8_t>(src[0]);
+              if (n0 + 1 < p.N) x |= static_cast<uint32_t>(static_cast<uint8_t>(src[1])) << 8;
+              if (n0 + 2 < p.N) x |= static_cast<uint32_t>(static_cast<uint8_t>(src[2])) << 16;
+              w[u][r] = x;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kIt; ++u) {
+        const int idx = u * kSnThreads + tid;
+        const int k = (idx / kQ) * 4, n0 = (idx % kQ) * 4;
+        // w[r] holds columns n0 .. n0+3 of row k + r; o[j] gets column n0 + j
+        // of rows k .. k+3 (byte r = row k + r).
+        const uint32_t t0 = __byte_perm(w[u][0], w[u][1], 0x5140);
+        const uint32_t t1 = __byte_perm(w[u][0], w[u][1], 0x7362);
+        const uint32_t t2 = __byte_perm(w[u][2], w[u][3], 0x5140);
+        const uint32_t t3 = __byte_perm(w[u][2], w[u][3], 0x7362);
+        *reinterpret_cast<uint32_t *>(bt + (n0 + 0) * S + k) = __byte_perm(t0, t2, 0x5410);
+        *reinterpret_cast<uint32_t *>(bt + (n0 + 1) * S + k) = __byte_perm(t0, t2, 0x7632);
+        *reinterpret_cast<uint32_t *>(bt + (n0 + 2) * S + k) = __byte_perm(t1, t3, 0x5410);
+        *reinterpret_cast<uint32_t *>(bt + (n0 + 3) * S + k) = __byte_perm(t1, t3, 0x7632);
+      }
+      return;
+    }
+  }
+  // Element by element, at most 16 values in flight per thread (the 64
+  // accumulators of 16 columns leave no room for more).
+  constexpr int kIters = KC * NP / kSnThreads;
+  constexpr int kRound = kIters < 16 ? kIters : 16;
+  static_assert(kIters * kSnThreads == KC * NP && kIters % kRound == 0, "staged values per thread");
+#pragma unroll 1
+  for (int u0 = 0; u0 < kIters; u0 += kRound) {
+    Bt v[kRound];
+#pragma unroll
+    for (int u = 0; u < kRound; ++u) {
+      const int idx = (u0 + u) * kSnThreads + tid;
+      const int gk = kc0 + idx / NP, n = idx % NP;
+      v[u] = Bt(0);
+      if (gk < p.K && n < p.N) {
+        if constexpr (T::kInt) {
+          v[u] = p.B[static_cast<int64_t>(gk) * p.ldb + n];
+        } else {
+          v[u] = to_float(p.B[static_cast<int64_t>(gk) * p.ldb + n]);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kRound; ++u) {
+      const int idx = (u0 + u) * kSnThreads + tid;
+      bt[(idx % NP) * S + idx / NP] = v[u];
+    }
+  }
+}
+
 // NP: N rounded up to 1, 2, 4, 8 or 16 (every per-column loop runs NP times).
 template <typename In, int NP>
 __global__ void __launch_bounds__(kSnThreads, 2)
@@ -210,32 +338,7 @@ __global__ void __launch_bounds__(kSnThreads, 2)
     for (int n = 0; n < NP; ++n) acc[r][n] = Acc(0);
 
   for (int kc0 = 0; kc0 < p.K; kc0 += KC) {
-    // Stage B[kc0 .. kc0 + KC) x NP, column by column (zeros beyond K and N):
-    // every load of the chunk is issued before the first store, so staging a
-    // chunk costs one round trip to L2.
-    {
-      constexpr int kIters = KC * NP / kSnThreads;
-      static_assert(kIters * kSnThreads == KC * NP && kIters <= 32, "staged values per thread");
-      Bt v[kIters];
-#pragma unroll
-      for (int u = 0; u < kIters; ++u) {
-        const int idx = u * kSnThreads + static_cast<int>(threadIdx.x);
-        const int gk = kc0 + idx / NP, n = idx % NP;
-        v[u] = Bt(0);
-        if (gk < p.K && n < p.N) {
-          if constexpr (T::kInt) {
-            v[u] = p.B[static_cast<int64_t>(gk) * p.ldb + n];
-          } else {
-            v[u] = to_float(p.B[static_cast<int64_t>(gk) * p.ldb + n]);
-          }
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kIters; ++u) {
-        const int idx = u * kSnThreads + static_cast<int>(threadIdx.x);
-        bt[(idx % NP) * S + idx / NP] = v[u];
-      }
-    }
+    sn_stage_b<In, NP>(p, kc0, bt);
     __syncthreads();
     // kG steps of 32 * kVec values of k at a time: all their loads of A are
     // issued before the first multiply, so kG * kRows 16-byte loads per lane
@@ -335,6 +438,8 @@ cudaError_t sn_dispatch(int M, int N, int K, typename SnType<In>::Acc alpha, con
   p.ldb = ldb;
   p.C = C;
   p.ldc = ldc;
+  p.b_vec = (sizeof(In) == 4 && reinterpret_cast<uintptr_t>(B) % 16 == 0 && ldb % 4 == 0) ||
+            (sizeof(In) == 1 && reinterpret_cast<uintptr_t>(B) % 4 == 0 && ldb % 4 == 0);
   if (N <= 1) return sn_launch<In, 1>(p, stream);
   if (N <= 2) return sn_launch<In, 2>(p, stream);
   if constexpr (sizeof(In) == 2) {

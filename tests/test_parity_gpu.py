@@ -457,6 +457,28 @@ def test_narrow_n_shapes(gemm_mod, oracle_mod, dtype, shape):
     assert torch.equal(got, again)
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.int8], ids=str)
+@pytest.mark.parametrize("shape,ldb", [((1030, 6, 2050), 8), ((2049, 13, 1500), 16),
+                                       ((600, 12, 3000), 12), ((512, 4, 1025), 4)],
+                         ids=["6in8", "13in16", "12in12", "4in4"])
+def test_narrow_n_vector_staging(gemm_mod, oracle_mod, dtype, shape, ldb):
+    """The narrow-N kernel's vector staging of B (row stride a multiple of 4:
+    fp32 in 16-byte loads of 4 columns, int8 in 4 x 4 byte blocks transposed
+    in registers), including a last group of columns that ends inside the row
+    padding (6 of 8, 13 of 16), a ragged last chunk of k, and K not a multiple
+    of 4 (rows of a block beyond K are zeros); every element checked."""
+    M, N, K = shape
+    if dtype == torch.int8:
+        p = w.problem(M, N, K, dtype, "int8", 77 + N, alpha=2, beta=-3, c_dist="int",
+                      lda=_ld16(dtype, K), ldb=ldb)
+    else:
+        p = w.problem(M, N, K, dtype, "normal", 77 + N, alpha=1.5, beta=0.25, c_dist="normal",
+                      lda=_ld16(dtype, K), ldb=ldb)
+    got, out = run_gpu(gemm_mod, p, ldc=N)
+    assert_parity(got, oracle_of(oracle_mod, p), exact=(dtype == torch.int8))
+    out.check_canaries()
+
+
 @pytest.mark.parametrize("dtype", ALL_DTYPES, ids=str)
 @pytest.mark.parametrize("shape", [(8, 520, 8192), (32, 1024, 4096), (1, 128, 16384),
                                    (3, 4096, 2048)], ids=lambda s: "x".join(map(str, s)))
