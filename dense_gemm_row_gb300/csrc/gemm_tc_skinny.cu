@@ -943,7 +943,22 @@ __global__ void __launch_bounds__(kRaw ? kClRawThreads : kThreads, kClCtasPerSm)
         const uint32_t rphase = static_cast<uint32_t>(i / kR) & 1u;
         const uint32_t wphase = static_cast<uint32_t>(i / kS) & 1u;
         int ok = 1;
-        if (!mbar_wait_bounded(smem_u32(&sm.full[r]), rphase, abort, p.err_word, kWaitFull) ||
+        // A ring whose length is not a multiple of the group count (3 raw
+        // stages for 17 to 64 rows) alternates each stage between the groups:
+        // the previous use of stage r, i - kR, belongs to the other group.
+        // Until that use is released, full[r] may still be in its phase, of
+        // the other parity, and a parity wait for use i would return at once
+        // (TMA copies can complete out of order, so this group can get ahead).
+        // Waiting for that release first makes the wait below unambiguous.
+        if constexpr (kR % kClConvGroups != 0) {
+          if (i >= kR &&
+              !mbar_wait_bounded(smem_u32(&sm.raw_free[r]),
+                                 static_cast<uint32_t>((i - kR) / kR) & 1u, abort, p.err_word,
+                                 kWaitEmpty))
+            ok = 0;
+        }
+        if (!ok ||
+            !mbar_wait_bounded(smem_u32(&sm.full[r]), rphase, abort, p.err_word, kWaitFull) ||
             !mbar_wait_bounded(smem_u32(&sm.empty[w]), wphase ^ 1u, abort, p.err_word,
                                kWaitEmpty))
           ok = 0;

@@ -391,6 +391,30 @@ def test_skinny_int8_cluster(gemm_mod, oracle_mod, shape):
     assert torch.equal(got, again)
 
 
+@pytest.mark.parametrize("M", [20, 64])
+def test_skinny_int8_cluster_cold_operands(gemm_mod, oracle_mod, M):
+    """The int8 cluster form on operands read from HBM, not L2: four
+    different 8192 x 8192 B matrices (268 MB, twice the L2) used in turn by
+    eight back-to-back calls, so that TMA copies of one k-block can land
+    after those of the next. With 17 to 64 rows the ring of raw stages has 3
+    stages shared by the two converter groups, whose waits must not run ahead
+    of the other group's use of a stage. Every output bit-exact."""
+    N = K = 8192
+    g = torch.Generator().manual_seed(4242 + M)
+    A = torch.randint(-128, 128, (M, K), generator=g, dtype=torch.int8)
+    Bs = [torch.randint(-128, 128, (K, N), generator=g, dtype=torch.int8) for _ in range(4)]
+    A_d = A.cuda()
+    B_d = [b.cuda() for b in Bs]
+    outs = [torch.empty(M, N, dtype=torch.int32, device="cuda") for _ in range(8)]
+    for j, C in enumerate(outs):
+        gemm_mod.gemm_s8(M, N, K, 1, A_d, K, B_d[j % 4], N, 0, C, N)
+    torch.cuda.synchronize()
+    assert gemm_mod.check_device_error() == 0
+    refs = [oracle_mod.gemm_s8(A, b) for b in Bs]
+    for j, C in enumerate(outs):
+        np.testing.assert_array_equal(C.cpu().numpy(), refs[j % 4])
+
+
 @pytest.mark.parametrize("shape", [(10, 2048, 2048, 1000), (16, 4100, 4112, 3072),
                                    (16, 8192, 8192, 4101), (24, 4096, 4096, 2048),
                                    (32, 2048, 2064, 3000), (33, 2048, 2064, 2049),
