@@ -14,9 +14,11 @@
 //             4-term dot product with A[m][k..k+3] into an exact int32 sum;
 //   * when there are fewer column blocks than SMs, k is split in parts: every
 //     part stores its partial sums into a workspace and counts itself done on
-//     its column block; the part that finishes last adds the partials in part
-//     order and writes alpha * sum + beta * C (deterministic; exact in int32
-//     with wrap-around). No part ever waits for another.
+//     its column block; once all parts of the block have stored, each part
+//     adds one slice of the block's partials in part order and writes
+//     alpha * sum + beta * C (deterministic; exact in int32 with
+//     wrap-around). The parts are resident at once (at most one CTA per SM),
+//     so this one wait at the end always ends; it is bounded all the same.
 // TMA needs 16-byte aligned bases and row strides (fp32: ld % 4 == 0; int8:
 // ld % 16 == 0); the entry points use this kernel only then.
 //
@@ -116,6 +118,103 @@ __device__ __forceinline__ int32_t axpby(int32_t a, int32_t x, int32_t b, int32_
   uint32_t r = static_cast<uint32_t>(a) * static_cast<uint32_t>(x);
   if (use_c) r += static_cast<uint32_t>(b) * static_cast<uint32_t>(c);
   return static_cast<int32_t>(r);
+}
+
+// Bounded wait until *count >= target (every part of a column block has
+// stored its partial sums). On giving up: sets *abort, records the timeout in
+// the error word, returns 0.
+__device__ __forceinline__ int wait_count(const uint32_t *count, uint32_t target,
+                                          volatile int *abort, uint32_t *err_word) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(count) : "memory");
+    if (v >= target) return 1;
+    __nanosleep(256);
+    if ((it & 63u) == 63u) {
+      if (*abort) return 0;
+      if (global_timer_ns() - t0 > kWaitLimitNs || it >= kWaitMaxPolls) {
+        *abort = 1;
+        record_timeout(err_word, kWaitFlag);
+        return 0;
+      }
+    }
+  }
+}
+
+// Part `part` of column block `blk`: its slice of the block's (row, 4-column
+// group) items, each summed over all parts' partial sums in part order (a few
+// loads in flight), then alpha * sum + beta * C. Out of line, so that the
+// register allocation of the k loop is not shaped by this code.
+// The fields it reads are passed by value: a reference to the kernel's
+// argument block would make the kernel keep a copy of it in local memory.
+template <bool kInt>
+struct SliceArgs {
+  using Out = typename SmCfg<kInt>::Out;
+  const Out *ws;
+  int64_t ws_ld, ldc;
+  Out *C;
+  Out alpha, beta;
+  int M, N, split, c_vec_ok;
+};
+template <bool kInt>
+__device__ __noinline__ void reduce_slice(const SliceArgs<kInt> p, int blk, int part, int n0,
+                                          int t) {
+  using Out = typename SmCfg<kInt>::Out;
+  using Vec = typename std::conditional<kInt, int4, float4>::type;
+  const bool use_c = p.beta != Out(0);
+  constexpr int kGroups = kCols / 4;
+  const int items = p.M * kGroups;
+  const int i1 = (part + 1) * items / p.split;
+#pragma unroll 1
+  for (int it = part * items / p.split + t; it < i1; it += 256) {
+    const int m = it / kGroups, g = it - (it / kGroups) * kGroups;
+    const int64_t wcol = static_cast<int64_t>(blk) * kCols + 4 * g;
+    const int nn = n0 + 4 * g;
+    Out sum[4] = {Out(0), Out(0), Out(0), Out(0)};
+    constexpr int kBatch = 8;  // loads in flight
+#pragma unroll 1
+    for (int q0 = 0; q0 < p.split; q0 += kBatch) {
+      Vec v[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u)
+        if (q0 + u < p.split)
+          v[u] = __ldcg(reinterpret_cast<const Vec *>(
+              p.ws + (static_cast<int64_t>(q0 + u) * p.M + m) * p.ws_ld + wcol));
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u)
+        if (q0 + u < p.split) {
+          if constexpr (kInt) {  // int32 wrap-around
+            sum[0] = static_cast<int32_t>(static_cast<uint32_t>(sum[0]) + static_cast<uint32_t>(v[u].x));
+            sum[1] = static_cast<int32_t>(static_cast<uint32_t>(sum[1]) + static_cast<uint32_t>(v[u].y));
+            sum[2] = static_cast<int32_t>(static_cast<uint32_t>(sum[2]) + static_cast<uint32_t>(v[u].z));
+            sum[3] = static_cast<int32_t>(static_cast<uint32_t>(sum[3]) + static_cast<uint32_t>(v[u].w));
+          } else {
+            sum[0] += v[u].x;
+            sum[1] += v[u].y;
+            sum[2] += v[u].z;
+            sum[3] += v[u].w;
+          }
+        }
+    }
+    if (nn < p.N) {
+      Out *cp = p.C + static_cast<int64_t>(m) * p.ldc + nn;
+      if (p.c_vec_ok && nn + 3 < p.N) {
+        Vec c = {};
+        if (use_c) c = *reinterpret_cast<const Vec *>(cp);
+        Vec o;
+        o.x = axpby(p.alpha, sum[0], p.beta, c.x, use_c);
+        o.y = axpby(p.alpha, sum[1], p.beta, c.y, use_c);
+        o.z = axpby(p.alpha, sum[2], p.beta, c.z, use_c);
+        o.w = axpby(p.alpha, sum[3], p.beta, c.w, use_c);
+        *reinterpret_cast<Vec *>(cp) = o;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (nn + j < p.N) cp[j] = axpby(p.alpha, sum[j], p.beta, use_c ? cp[j] : Out(0), use_c);
+      }
+    }
+  }
 }
 
 // MP: rows of A staged per stage (M rounded up to 1, 2, 4, 8, 16 or 32); every
@@ -335,49 +434,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       __threadfence();
       consumer_sync();
-      __shared__ int last;
-      if (t == 0) last = (atomicAdd(p.counters + blk, 1u) == static_cast<uint32_t>(p.split - 1));
+      if (t == 0) atomicAdd(p.counters + blk, 1u);
+      // Once every part of this column block has stored, each part sums one
+      // slice of the block's (row, 4-column group) items over all parts, in
+      // part order. All parts are resident at once (the grid never exceeds one
+      // CTA per SM), so the wait ends; it is bounded all the same.
+      __shared__ int ready;
+      if (t == 0)
+        ready = wait_count(p.counters + blk, static_cast<uint32_t>(p.split), abort, p.err_word);
       consumer_sync();
-      if (last) {
-        // The last part of this column block: sum the parts in order.
+      if (ready) {
         __threadfence();
-        const bool use_c = p.beta != Out(0);
-#pragma unroll 1
-        for (int m = 0; m < p.M; ++m) {
-          Out sum[4] = {Out(0), Out(0), Out(0), Out(0)};
-          for (int q = 0; q < p.split; ++q) {
-            const Vec v = __ldcg(reinterpret_cast<const Vec *>(
-                p.ws + (static_cast<int64_t>(q) * p.M + m) * p.ws_ld + nl));
-            if constexpr (kInt) {  // int32 wrap-around
-              sum[0] = static_cast<int32_t>(static_cast<uint32_t>(sum[0]) + static_cast<uint32_t>(v.x));
-              sum[1] = static_cast<int32_t>(static_cast<uint32_t>(sum[1]) + static_cast<uint32_t>(v.y));
-              sum[2] = static_cast<int32_t>(static_cast<uint32_t>(sum[2]) + static_cast<uint32_t>(v.z));
-              sum[3] = static_cast<int32_t>(static_cast<uint32_t>(sum[3]) + static_cast<uint32_t>(v.w));
-            } else {
-              sum[0] += v.x;
-              sum[1] += v.y;
-              sum[2] += v.z;
-              sum[3] += v.w;
-            }
-          }
-          if (n < p.N) {
-            Out *cp = p.C + static_cast<int64_t>(m) * p.ldc + n;
-            if (vec) {
-              Vec c = {};
-              if (use_c) c = *reinterpret_cast<const Vec *>(cp);
-              Vec o;
-              o.x = axpby(p.alpha, sum[0], p.beta, c.x, use_c);
-              o.y = axpby(p.alpha, sum[1], p.beta, c.y, use_c);
-              o.z = axpby(p.alpha, sum[2], p.beta, c.z, use_c);
-              o.w = axpby(p.alpha, sum[3], p.beta, c.w, use_c);
-              *reinterpret_cast<Vec *>(cp) = o;
-            } else {
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                if (n + j < p.N) cp[j] = axpby(p.alpha, sum[j], p.beta, use_c ? cp[j] : Out(0), use_c);
-            }
-          }
-        }
+        SliceArgs<kInt> sa;
+        sa.ws = p.ws;
+        sa.ws_ld = p.ws_ld;
+        sa.ldc = p.ldc;
+        sa.C = p.C;
+        sa.alpha = p.alpha;
+        sa.beta = p.beta;
+        sa.M = p.M;
+        sa.N = p.N;
+        sa.split = p.split;
+        sa.c_vec_ok = p.c_vec_ok;
+        reduce_slice<kInt>(sa, blk, part, n0, t);
       }
     }
   }
