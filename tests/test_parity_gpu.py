@@ -327,6 +327,42 @@ def test_skinny_shapes(gemm_mod, oracle_mod, dtype, M):
         out.check_canaries()
 
 
+@pytest.mark.parametrize("dtype", ALL_DTYPES, ids=str)
+@pytest.mark.parametrize("shape", [(1, 8192, 8192), (16, 8192, 8192), (64, 8192, 8192),
+                                   (8192, 1, 8192), (8192, 16, 8192)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_bench_memory_bound_shapes_from_hbm(gemm_mod, oracle_mod, dtype, shape):
+    """The short, wide and tall, narrow shapes the bench times, at its sizes,
+    with the large operand read from HBM: several different large operands
+    (together more than twice the L2; four for int8, two otherwise) are used
+    by back-to-back calls in turn, as the bench does, so TMA and load
+    completions arrive in the order DRAM gives them. Every element of every
+    call against the oracle (int8 bit-exact)."""
+    M, N, K = shape
+    if dtype in (torch.bfloat16, torch.float16) and N < 8:
+        pytest.skip("16-bit B rows must be a whole number of 16-byte units")
+    tall = M > N
+    copies = 4 if dtype == torch.int8 else 2
+    dist = "int8" if dtype == torch.int8 else "normal"
+    small = w.matrix(*((K, N) if tall else (M, K)), dtype, dist, 7100 + M + N)
+    bigs = [w.matrix(*((M, K) if tall else (K, N)), dtype, dist, 7200 + j) for j in range(copies)]
+    small_d = small.cuda()
+    bigs_d = [b.cuda() for b in bigs]
+    out_dt = torch.int32 if dtype == torch.int8 else torch.float32
+    outs = [torch.zeros(M, N, dtype=out_dt, device="cuda") for _ in range(copies)]
+    for j in range(copies):
+        A, B = (bigs_d[j], small_d) if tall else (small_d, bigs_d[j])
+        gemm_mod.gemm(A, B, outs[j])
+    torch.cuda.synchronize()
+    assert gemm_mod.check_device_error() == 0
+    for j in range(copies):
+        A, B = (bigs[j], small) if tall else (small, bigs[j])
+        if dtype == torch.int8:
+            np.testing.assert_array_equal(outs[j].cpu().numpy(), oracle_mod.gemm_s8(A, B))
+        else:
+            assert_parity(outs[j].cpu(), oracle_mod.gemm(A, B), exact=False)
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.int8], ids=str)
 @pytest.mark.parametrize("shape", [(9, 2048, 4096), (24, 4160, 8200), (32, 8192, 2048),
                                    (16, 19200, 1024), (40, 3000, 3000), (64, 4096, 4096)],
