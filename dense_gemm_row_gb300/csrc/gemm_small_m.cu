@@ -17,8 +17,9 @@
 //     its column block; once all parts of the block have stored, each part
 //     adds one slice of the block's partials in part order and writes
 //     alpha * sum + beta * C (deterministic; exact in int32 with
-//     wrap-around). The parts are resident at once (at most one CTA per SM),
-//     so this one wait at the end always ends; it is bounded all the same.
+//     wrap-around). The grid is at most one CTA per SM and is launched
+//     cooperatively, so all parts are resident at once and this one wait at
+//     the end always ends; it is bounded all the same.
 // TMA needs 16-byte aligned bases and row strides (fp32: ld % 4 == 0; int8:
 // ld % 16 == 0); the entry points use this kernel only then.
 //
@@ -437,8 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t == 0) atomicAdd(p.counters + blk, 1u);
       // Once every part of this column block has stored, each part sums one
       // slice of the block's (row, 4-column group) items over all parts, in
-      // part order. All parts are resident at once (the grid never exceeds one
-      // CTA per SM), so the wait ends; it is bounded all the same.
+      // part order. All parts are resident at once (a cooperative launch of
+      // at most one CTA per SM), so the wait ends; it is bounded all the same.
       __shared__ int ready;
       if (t == 0)
         ready = wait_count(p.counters + blk, static_cast<uint32_t>(p.split), abort, p.err_word);
@@ -558,8 +559,22 @@ cudaError_t launch(const DeviceInfo &dev, int M, int N, int K, typename SmArgs<k
   cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void *>(kern),
                                        static_cast<int>(smem), dev.device);
   if (e == cudaSuccess) {
-    kern<<<static_cast<unsigned>(blocks * split), kThreads, smem, stream>>>(tmA, tmB, p);
-    e = cudaGetLastError();
+    // With k split, the parts of a column block wait for one another at the
+    // end: a cooperative launch starts the grid only when all of its CTAs can
+    // be resident together (another stream's kernels cannot leave it half
+    // resident).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks * split), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = split > 1 ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
   }
   if (pool_ws) {
     cudaError_t f = cudaFreeAsync(pool_ws, stream);

@@ -36,15 +36,18 @@
  *   M or N == 0  Nothing is launched; GEMM_OK is returned.
  *   Stream  The call only enqueues work on `stream` (0 = the legacy default
  *           stream) and returns; results are ready when the stream is.
- *           Calls on different streams may overlap on the GPU. The kernels
- *           that split k across CTAs (the tensor-core kernel's last wave,
- *           the short-wide SIMT kernel) size their grid to be resident all at
- *           once, and their CTAs wait on one another at the end. When another
- *           stream's work holds part of the GPU for longer than that wait's
- *           bound (2 s), the call gives up, like any other bounded wait: its
- *           C is incomplete and gemm_check_device_error() returns
- *           GEMM_ERR_TIMEOUT. Two such calls can do this to each other. Order
- *           calls that must not fail this way on one stream.
+ *           Calls on different streams may overlap on the GPU. The
+ *           tensor-core kernel splits the k range of its last wave's tiles
+ *           across CTAs, sizes its grid to be resident all at once, and a
+ *           later part waits for the one before. When another stream's work
+ *           holds part of the GPU for longer than that wait's bound (2 s),
+ *           the call gives up, like any other bounded wait: its C is
+ *           incomplete and gemm_check_device_error() returns
+ *           GEMM_ERR_TIMEOUT. Two such calls can do this to each other.
+ *           Order calls that must not fail this way on one stream. (The
+ *           short-wide SIMT kernel, whose split parts also wait for one
+ *           another, is launched cooperatively and so is always resident
+ *           in full.)
  *   Device  The current CUDA device must be an sm_103 (GB300) GPU.
  *   Errors  Never aborts and never prints. Argument checks run on the host
  *           before anything is enqueued; a failed check returns a status and
