@@ -42,3 +42,35 @@ def test_traffic_records_are_well_formed():
         assert re.fullmatch(r"[0-9a-f]{16}", digest)
         assert int(nbytes) > 0
         assert os.path.exists(os.path.join(ROOT, profile)), profile
+
+
+def test_reference_arm_prints_the_contract_line(monkeypatch, capsys):
+    """`bench.py --impl reference` times the CPU oracle and prints one JSON line
+    with the same metric as the GPU arm, marked impl=reference, with a
+    cpu_baseline describing the run and an e2e of zero copied bytes; ranks
+    other than 0 print nothing. Run here on a small seeded problem standing in
+    for the workload's inputs."""
+    import argparse
+    import json
+
+    import torch
+
+    small = w.problem(64, 48, 40, torch.bfloat16, "normal", 5)
+    monkeypatch.setattr(w, "config", lambda name: small)
+    args = argparse.Namespace(workload="bf16_8192", steps=2, warmup=1)
+    assert bench.run_reference(args, 1, 1) == 0
+    assert capsys.readouterr().out == ""
+    assert bench.run_reference(args, 1, 0) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert line["metric"] == bench.METRIC
+    assert line["unit"] == "TFLOP/s" and line["higher_is_better"] is True
+    assert line["steps"] == 2 and line["warmup"] == 1 and line["n_gpus"] == 1
+    assert line["value"] > 0 and line["ms_per_step"] > 0
+    assert line["dtype"] == "f64" and line["data"] == "synthetic"
+    assert line["config"]["workload"] == bench.WORKLOADS["bf16_8192"][0]
+    cpu = line["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and cpu["cores"] >= 1 and cpu["value"] == line["value"]
+    assert "rows 0..63 of A (64 of 64)" in cpu["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
