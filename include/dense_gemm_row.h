@@ -37,9 +37,10 @@
  *   Stream  The call only enqueues work on `stream` (0 = the legacy default
  *           stream) and returns; results are ready when the stream is.
  *           Calls on different streams may overlap on the GPU. The
- *           tensor-core kernel splits the k range of its last wave's tiles
- *           across CTAs, sizes its grid to be resident all at once, and a
- *           later part waits for the one before. When another stream's work
+ *           tensor-core kernel, and the SIMT SGEMM on grids of under two
+ *           waves, split the k range of their last wave's tiles across CTAs,
+ *           size their grids to be resident all at once, and a later part
+ *           waits for the one before. When another stream's work
  *           holds part of the GPU for longer than that wait's bound (2 s),
  *           the call gives up, like any other bounded wait: its C is
  *           incomplete and gemm_check_device_error() returns
