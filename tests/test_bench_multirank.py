@@ -31,7 +31,9 @@ def _worker(rank, world, port, out):
 
 def test_aggregate_two_ranks_gloo():
     port = _free_port()
-    with mp.Manager() as m:
+    # spawn, not fork: earlier tests in this process may have started threads
+    # (the oracle's OpenMP pool), and a fork of a threaded process can hang.
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
         res = dict(out)
